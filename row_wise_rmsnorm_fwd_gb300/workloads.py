@@ -1,0 +1,170 @@
+"""Seeded synthetic inputs for the RMSNorm forward workloads.
+
+This module draws random numbers and nothing else: it holds none of the
+normalisation arithmetic, so the CUDA path and the CPU oracle can both be fed
+from it without sharing any of the method.
+
+Shapes and distributions follow the workloads of the page "A hackable Python
+ML compiler, part 2" (its RMSNorm example ``torch.nn.RMSNorm(2048)`` on a
+``(1,32,2048)`` fp32 input with eps 1e-6, and the TinyLlama / Qwen2.5-7B block
+shapes it benchmarks), widened to the bandwidth-bound and bf16 sizes this
+library is measured on:
+
+=========  =======================  =====  ================  ===============  ======
+name       x shape                  dtype  x distribution    w distribution   eps
+=========  =======================  =====  ================  ===============  ======
+c1         (1, 32, 2048)            f32    N(0,1)            N(1,0.1)         1e-6
+c2         (1, 128, 2048)           f32    N(0,1)            N(1,0.1)         1e-5
+c2t        (1, 128, 2050)           f32    N(0,1)            N(1,0.1)         1e-5
+c3         (4, 512, 3584)           f32    N(0,1), 36 outlier columns x50     1e-6
+c4         (65536, 4096)            f32    N(0,1)            U(0.5,1.5)       1e-6
+c5a        (262144, 8192)           bf16   N(0,2) (std 2)    N(1,0.1)         1e-6
+c5b        (8, 262144)              bf16   N(0,2)            N(1,0.1)         1e-6
+=========  =======================  =====  ================  ===============  ======
+
+Readings: "N(0,2)" is mean 0, standard deviation 2; the Qwen-shaped case's
+"1% outlier channels" are round(0.01*3584) = 36 whole columns, picked by a
+seeded permutation and multiplied by 50 in every row.  bf16 values are drawn
+in fp32 and rounded to bf16 by torch's round-to-nearest-even cast.
+
+Seeds: x uses 1000+k, w uses 2000+k, the outlier columns 3000+k, where k is
+the workload's index in the table.  On the CPU the draws are bit-reproducible;
+``device="cuda"`` draws from torch's CUDA generator with the same seed (a
+different but equally seeded stream), used where the full tensor is too large
+to build on the host.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    index: int
+    shape: tuple
+    dtype: str            # "f32" or "bf16"
+    x_dist: tuple         # ("normal", mean, std)
+    w_dist: tuple         # ("normal", mean, std) or ("uniform", lo, hi)
+    eps: float
+    outlier_cols: int = 0
+    outlier_scale: float = 1.0
+    description: str = ""
+
+    @property
+    def rows(self) -> int:
+        r = 1
+        for d in self.shape[:-1]:
+            r *= d
+        return r
+
+    @property
+    def hidden(self) -> int:
+        return self.shape[-1]
+
+    @property
+    def elem_bytes(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    @property
+    def bytes_per_call(self) -> int:
+        """Algorithmic bytes: read x once, write y once, read w once."""
+        return (2 * self.rows * self.hidden + self.hidden) * self.elem_bytes
+
+
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("c1", 0, (1, 32, 2048), "f32", ("normal", 0.0, 1.0),
+                 ("normal", 1.0, 0.1), 1e-6,
+                 description="page example torch.nn.RMSNorm(2048) on (1,32,2048)"),
+        Workload("c2", 1, (1, 128, 2048), "f32", ("normal", 0.0, 1.0),
+                 ("normal", 1.0, 0.1), 1e-5,
+                 description="TinyLlama-shaped (1,128,2048)"),
+        Workload("c2t", 1, (1, 128, 2050), "f32", ("normal", 0.0, 1.0),
+                 ("normal", 1.0, 0.1), 1e-5,
+                 description="ragged row width 2050 (8200-byte row pitch)"),
+        Workload("c3", 2, (4, 512, 3584), "f32", ("normal", 0.0, 1.0),
+                 ("normal", 1.0, 0.1), 1e-6, outlier_cols=36,
+                 outlier_scale=50.0,
+                 description="Qwen2.5-7B-shaped (4,512,3584), 36 outlier columns x50"),
+        Workload("c4", 3, (65536, 4096), "f32", ("normal", 0.0, 1.0),
+                 ("uniform", 0.5, 1.5), 1e-6,
+                 description="bandwidth-bound fp32 (65536,4096)"),
+        Workload("c5a", 4, (262144, 8192), "bf16", ("normal", 0.0, 2.0),
+                 ("normal", 1.0, 0.1), 1e-6,
+                 description="bandwidth-bound bf16 (262144,8192), 2^31 elements"),
+        Workload("c5b", 4, (8, 262144), "bf16", ("normal", 0.0, 2.0),
+                 ("normal", 1.0, 0.1), 1e-6,
+                 description="few rows, wide bf16 (8,262144)"),
+    ]
+}
+
+
+def _torch_dtype(dtype: str):
+    return torch.float32 if dtype == "f32" else torch.bfloat16
+
+
+def _generator(seed: int, device: str) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _draw(shape, dist, gen, device) -> torch.Tensor:
+    kind, a, b = dist
+    if kind == "normal":
+        t = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+        return t.mul_(b).add_(a)
+    if kind == "uniform":
+        t = torch.rand(shape, generator=gen, device=device, dtype=torch.float32)
+        return t.mul_(b - a).add_(a)
+    raise ValueError(f"unknown distribution {kind}")
+
+
+def outlier_columns(wl: Workload) -> torch.Tensor:
+    """The seeded set of outlier columns (empty if the workload has none)."""
+    if wl.outlier_cols == 0:
+        return torch.empty(0, dtype=torch.long)
+    g = _generator(3000 + wl.index, "cpu")
+    return torch.randperm(wl.hidden, generator=g)[: wl.outlier_cols].sort().values
+
+
+def make_x(wl: Workload, device: str = "cpu", rows: int | None = None,
+           seed_offset: int = 0) -> torch.Tensor:
+    """x for workload ``wl`` with its full shape, or ``rows`` rows of width H.
+
+    ``rows`` draws a prefix-shaped sample (rows x hidden) from the same
+    distribution; ``seed_offset`` varies the seed for repeated samples.
+    """
+    shape = wl.shape if rows is None else (rows, wl.hidden)
+    g = _generator(1000 + wl.index + seed_offset, device)
+    x = _draw(shape, wl.x_dist, g, device)
+    if wl.outlier_cols:
+        cols = outlier_columns(wl).to(device)
+        x[..., cols] *= wl.outlier_scale
+    return x.to(_torch_dtype(wl.dtype))
+
+
+def make_w(wl: Workload, device: str = "cpu") -> torch.Tensor:
+    g = _generator(2000 + wl.index, device)
+    return _draw((wl.hidden,), wl.w_dist, g, device).to(_torch_dtype(wl.dtype))
+
+
+def make_random(shape, dtype: str, seed: int, dist=("normal", 0.0, 1.0),
+                device: str = "cpu") -> torch.Tensor:
+    """A seeded tensor of any shape (for sweeps over widths and row counts)."""
+    g = _generator(seed, device)
+    return _draw(tuple(shape), dist, g, device).to(_torch_dtype(dtype))
+
+
+def bf16_bits(t: torch.Tensor):
+    """bfloat16 tensor -> numpy uint16 bit patterns (host copy)."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def from_bf16_bits(bits) -> torch.Tensor:
+    """numpy uint16 bit patterns -> bfloat16 tensor (host)."""
+    import numpy as np
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)

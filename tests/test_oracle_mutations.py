@@ -1,0 +1,93 @@
+"""The oracle's pins catch planted mistakes (CPU only).
+
+Each case copies the oracle's C source, plants one plausible slip, compiles the
+copy into a temporary directory and runs a subset of the pins against it.  The
+pins must reject every mutant; the unmodified copy must pass.  Nothing here
+touches the real oracle build or the CUDA library.
+"""
+import ctypes
+import json
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+from test_oracle_pins import GOLDEN, _eval_closed_form
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                   "oracle", "rmsnorm_oracle.c")
+
+MUTANTS = {
+    "unmodified": None,
+    "sum_not_mean": ("double ms = acc / (double)hidden;", "double ms = acc;"),
+    "eps_outside_root": ("double rstd = 1.0 / sqrt(ms + eps);",
+                         "double rstd = 1.0 / sqrt(ms) + eps;"),
+    "eps_dropped": ("double rstd = 1.0 / sqrt(ms + eps);",
+                    "double rstd = 1.0 / sqrt(ms);"),
+    "weight_index": ("yr[j] = (xr[j] * rstd) * w[j];",
+                     "yr[j] = (xr[j] * rstd) * w[hidden - 1 - j];"),
+    "lost_sign": ("yr[j] = (xr[j] * rstd) * w[j];",
+                  "yr[j] = (fabs(xr[j]) * rstd) * w[j];"),
+    "sqrt_not_rsqrt": ("double rstd = 1.0 / sqrt(ms + eps);",
+                       "double rstd = sqrt(ms + eps);"),
+    "row_offset": ("rms_row_f64(x + r * hidden, w, y + r * hidden, hidden, eps);",
+                   "rms_row_f64(x, w, y + r * hidden, hidden, eps);"),
+    "bf16_truncate": ("double r = round_half_even(n);", "double r = floor(n);"),
+    "bf16_double_round": ("double n = ldexp(a, -(int)q_exp);",
+                          "double n = ldexp((double)(float)a, -(int)q_exp);"),
+    "bf16_ties_away": ("return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;",
+                       "return fl + 1.0;"),
+}
+
+
+def _build(tmp_path, name, mutation):
+    src = open(SRC).read()
+    if mutation is not None:
+        old, new = mutation
+        assert src.count(old) >= 1, f"mutation site for {name} not found"
+        src = src.replace(old, new)
+    c = tmp_path / f"{name}.c"
+    c.write_text(src)
+    so = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+                    "-ffp-contract=off", "-o", str(so), str(c), "-lm"],
+                   check=True)
+    lib = ctypes.CDLL(str(so))
+    vp, i64, dbl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double
+    lib.oracle_rmsnorm_f64.argtypes = [vp, vp, vp, i64, i64, dbl]
+    lib.oracle_f64_to_bf16_rne.argtypes = [dbl]
+    lib.oracle_f64_to_bf16_rne.restype = ctypes.c_uint16
+    return lib
+
+
+def _pins_pass(lib) -> bool:
+    """A compact subset of the pins: worked examples and bf16 rounding."""
+    with open(GOLDEN) as f:
+        cases = json.load(f)["cases"]
+    for case in cases:
+        x = np.ascontiguousarray(case["x"], dtype=np.float64)
+        w = np.ascontiguousarray(case["w"], dtype=np.float64)
+        y = np.empty_like(x)
+        lib.oracle_rmsnorm_f64(x.ctypes.data, w.ctypes.data, y.ctypes.data,
+                               x.shape[0], x.shape[1], case["eps"])
+        expect = np.array([[float(_eval_closed_form(e)) for e in row]
+                           for row in case["y"]])
+        if not np.allclose(y, expect, rtol=4e-16, atol=0):
+            return False
+    # bf16: a tie (1 + 2^-8 -> 1.0), a tie to the odd side's even neighbour
+    # (1 + 3*2^-8 -> 0x3F82), and a hair above a tie (must round up)
+    probes = {1.0 + 2.0 ** -8: 0x3F80, 1.0 + 3 * 2.0 ** -8: 0x3F82,
+              (1.0 + 2.0 ** -8) * (1 + 2.0 ** -40): 0x3F81, 1.0: 0x3F80}
+    return all(lib.oracle_f64_to_bf16_rne(v) == b for v, b in probes.items())
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(tmp_path, name):
+    lib = _build(tmp_path, name, MUTANTS[name])
+    if name == "unmodified":
+        assert _pins_pass(lib)
+    else:
+        assert not _pins_pass(lib), f"pins did not catch mutant {name}"
