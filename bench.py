@@ -1,0 +1,439 @@
+"""Benchmark of the RMSNorm forward hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5a]
+                    [--impl ours|reference] [--no-cpu-baseline] [--no-e2e]
+
+A step is one full RMSNorm forward over the workload (all rows) through the
+C ABI.  Prints ONE JSON line (rank 0).  Default workload: c5a, x (262144, 8192)
+bf16 in/out with fp32 arithmetic, 8.59 GB moved per step (larger than L2, so
+no L2 flush is needed between steps).  Under torchrun (N > 1) every rank runs
+the same workload on its own GPU (rows are independent: weak scaling, no
+data-path collective); the time is the max over ranks.
+
+``--impl reference`` times the CPU oracle on the host cores on a bounded
+sample of the same workload (the only other leg that executes ``oracle/``).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "RMSNorm GB/s and rows/s on 1 GB300; % of HBM roofline"
+
+
+# ------------------------------------------------------------------ helpers --
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources; a profile's traffic figure is valid only for
+    the sources it was captured from."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "row_wise_rmsnorm_fwd_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this workload
+    (profiles/*_<workload>.txt, lines 'traffic_bytes_per_launch:' and
+    'kernel_source_hash:'); None if absent or taken from other sources."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    want = kernel_source_hash()
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith(f"_{workload}.txt"):
+            continue
+        fields = {}
+        with open(os.path.join(pdir, name)) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("kernel_source_hash") == want and "traffic_bytes_per_launch" in fields:
+            return int(float(fields["traffic_bytes_per_launch"]))
+    return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._thread = threading.Thread(target=self._read, daemon=True)
+            self._thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------ CPU baseline --
+
+def cpu_oracle_sample(wl, budget_s: float = 10.0, chunk_rows: int = 2048, max_chunks: int = 48):
+    """Time the oracle (as it stands, one host thread) on chunks of the
+    workload's rows until about `budget_s` seconds of CPU work are done."""
+    import oracle
+    from row_wise_rmsnorm_fwd_gb300 import workloads
+
+    oracle.build()
+    w = workloads.make_w(wl)
+    chunk_rows = min(chunk_rows, wl.rows)
+    done_rows, elapsed, k = 0, 0.0, 0
+    if wl.dtype == "bf16":
+        wb = workloads.bf16_bits(w)
+    while elapsed < budget_s and k < max_chunks:
+        x = workloads.make_x(wl, rows=chunk_rows, seed_offset=k)
+        if wl.dtype == "bf16":
+            xb = workloads.bf16_bits(x)
+            t0 = time.perf_counter()
+            oracle.rmsnorm_bf16(xb, wb, wl.eps)
+        else:
+            xn, wn = x.numpy(), w.numpy()
+            t0 = time.perf_counter()
+            oracle.rmsnorm_f32(xn, wn, wl.eps)
+        elapsed += time.perf_counter() - t0
+        done_rows += chunk_rows
+        k += 1
+    bytes_done = (2 * done_rows * wl.hidden) * wl.elem_bytes + wl.hidden * wl.elem_bytes
+    return {
+        "value": bytes_done / elapsed / 1e9,
+        "unit": "GB/s",
+        "rows_per_s": done_rows / elapsed,
+        "cores": 1,
+        "kind": "oracle",
+        "sample": f"{done_rows} rows x {wl.hidden} of workload {wl.name} in {k} chunks "
+                  f"of {chunk_rows} rows ({elapsed:.1f} s of single-thread fp64 oracle time)",
+        "seconds": elapsed,
+    }
+
+
+def run_reference(args, wl):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    budget = max(1.0, 10.0 / max(1, args.steps))
+    cb = None
+    for _ in range(args.warmup):
+        cpu_oracle_sample(wl, budget_s=0.5, max_chunks=1)
+    per = []
+    for _ in range(args.steps):
+        cb = cpu_oracle_sample(wl, budget_s=budget)
+        per.append(cb)
+    total_bytes = sum(c["value"] * c["seconds"] for c in per)
+    total_s = sum(c["seconds"] for c in per)
+    value = total_bytes / total_s
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(wl, world),
+        "rows_per_s": sum(c["rows_per_s"] * c["seconds"] for c in per) / total_s,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} steps, each: {per[-1]['sample']}"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(wl, world):
+    return {
+        "workload": f"{wl.name}: {wl.description}",
+        "shape": list(wl.shape), "io_dtype": wl.dtype, "eps": wl.eps,
+        "bytes_per_step_per_gpu": wl.bytes_per_call,
+        "rows_per_step_per_gpu": wl.rows,
+        "l2": "inputs larger than L2 (no flush needed)" if wl.bytes_per_call > 4 * 129e6
+              else "L2 flushed between steps",
+        "parallelism": f"rows replicated per GPU x{world} (independent rows, no collective)",
+    }
+
+
+# -------------------------------------------------------------- GPU timing --
+
+def run_ours(args, wl):
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from row_wise_rmsnorm_fwd_gb300 import binding, workloads
+
+    x = workloads.make_x(wl, device="cuda")
+    w = workloads.make_w(wl, device="cuda")
+    y = torch.empty_like(x)
+    rows, hidden = wl.rows, wl.hidden
+    stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream
+    fwd = binding.raw.rmsnorm_fwd_bf16 if wl.dtype == "bf16" else binding.raw.rmsnorm_fwd_f32
+    plan = binding.rmsnorm_plan(x, w, y)
+    flush = None
+    if wl.bytes_per_call <= 4 * 129e6:
+        flush = torch.empty(int(2 * 129e6) // 4 + 1024, dtype=torch.float32, device=dev)
+
+    def step():
+        st = fwd(x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, hidden, wl.eps, handle)
+        if st != 0:
+            raise RuntimeError(f"rmsnorm failed: {binding.rmsnorm_status_string(st)}")
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.fill_(1.0)
+        step()
+    barrier()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)          # let the sampler start before the timed region
+        barrier()
+        t_begin = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_begin.record(stream)
+        for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(1.0)   # outside the per-launch event pair
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t_end.record(stream)
+        barrier()
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms = sum(per_launch_ms)          # device time of the K launches
+    region_ms = t_begin.elapsed_time(t_end)  # whole timed region
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([kernel_ms, region_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        kernel_ms, region_ms = float(t[0]), float(t[1])
+    ms_per_step = kernel_ms / args.steps
+    bytes_step = wl.bytes_per_call
+    value = world * bytes_step * args.steps / (kernel_ms / 1e3) / 1e9
+    rows_per_s = world * rows * args.steps / (kernel_ms / 1e3)
+
+    peak, peak_src = peaks()
+    avg_launch_s = (sum(per_launch_ms) / len(per_launch_ms)) / 1e3
+    achieved = bytes_step / avg_launch_s / 1e9
+    per_launch_sorted = sorted(per_launch_ms)
+    traffic = profiled_traffic(wl.name)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, wl, x, w, y, fwd, binding, world)
+
+    del x, y
+    torch.cuda.empty_cache()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(wl)
+        cpu.pop("seconds", None)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic", "config": config_block(wl, world),
+            "rows_per_s": rows_per_s,
+            "kernel": {"name": plan["kernel"], "path": plan["path_name"],
+                       "grid": plan["grid"], "block": plan["block_threads"],
+                       "cluster": plan["cluster"], "vec_bytes": plan["vec_bytes"],
+                       "vecs_per_thread": plan["vecs_per_thread"],
+                       "threads_per_row": plan["threads_per_row"],
+                       "launch_ms_median": per_launch_sorted[len(per_launch_sorted) // 2],
+                       "launch_ms_min": per_launch_sorted[0],
+                       "launch_ms_max": per_launch_sorted[-1]},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": f"{peak_src} (hbm_gbs)",
+                         "traffic": traffic},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "timed_region_ms": region_ms,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def measure_e2e(args, wl, x_dev, w_dev, y_dev, fwd, binding, world):
+    """Same metric end to end: pinned host x,w -> device, the C-ABI call, device
+    y -> pinned host, every step.  The row range is split into chunks run on
+    two streams so that copies in both directions overlap the kernel."""
+    import torch
+
+    dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+    x_h = torch.empty(wl.shape, dtype=dt, pin_memory=True)
+    x_h.copy_(x_dev.cpu())
+    w_h = w_dev.cpu().pin_memory()
+    y_h = torch.empty(wl.shape, dtype=dt, pin_memory=True)
+    rows, hidden = wl.rows, wl.hidden
+    xh2, yh2 = x_h.view(rows, hidden), y_h.view(rows, hidden)
+    xd2, yd2 = x_dev.view(rows, hidden), y_dev.view(rows, hidden)
+    nchunks = 16 if rows >= 16 else 1
+    bounds = [rows * i // nchunks for i in range(nchunks + 1)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    launches = [0]
+
+    def step():
+        ev_w = torch.cuda.Event()
+        s0 = streams[0]
+        with torch.cuda.stream(s0):
+            w_dev.copy_(w_h, non_blocking=True)
+            ev_w.record(s0)
+        for i in range(nchunks):
+            s = streams[i % 2]
+            a, b = bounds[i], bounds[i + 1]
+            with torch.cuda.stream(s):
+                s.wait_event(ev_w)
+                xd2[a:b].copy_(xh2[a:b], non_blocking=True)
+                st = fwd(xd2[a:b].data_ptr(), w_dev.data_ptr(), yd2[a:b].data_ptr(),
+                         b - a, hidden, wl.eps, s.cuda_stream)
+                if st != 0:
+                    raise RuntimeError(binding.rmsnorm_status_string(st))
+                launches[0] += 1
+                yh2[a:b].copy_(yd2[a:b], non_blocking=True)
+        for s in streams:
+            s.synchronize()
+
+    for _ in range(max(3, min(args.warmup, 5))):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 10))
+    launches[0] = 0
+    t0 = time.perf_counter()
+    for _ in range(n):
+        step()
+    dt_s = time.perf_counter() - t0
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([dt_s], device=x_dev.device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dt_s = float(t[0])
+    # check the round trip landed (cheap spot check of one row against the device)
+    if not torch.equal(yh2[-1].to(y_dev.device), yd2[-1]):
+        raise RuntimeError("end-to-end copy-back mismatch")
+    return {"value": world * wl.bytes_per_call * n / dt_s / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": (rows * hidden + hidden) * wl.elem_bytes,
+            "d2h_bytes_per_step": rows * hidden * wl.elem_bytes,
+            "steps": n, "ms_per_step": 1e3 * dt_s / n, "chunks_per_step": nchunks,
+            "streams": 2, "gpu_launches": launches[0], "timing": "host wall clock"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="c5a")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    from row_wise_rmsnorm_fwd_gb300 import workloads
+    wl = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

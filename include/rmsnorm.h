@@ -1,0 +1,170 @@
+/*
+ * rmsnorm.h -- C ABI of librmsnorm, a fused row-wise RMSNorm forward pass for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (page "A hackable Python ML compiler, part 2", the RMSNorm
+ * Loop-IR listing and the epilogue of the generated kernel) is, for every row
+ * r of a row-major matrix x with `hidden` columns:
+ *
+ *     ms[r]   = (1/hidden) * sum_j x[r,j]^2
+ *     rstd[r] = rsqrt(ms[r] + eps)
+ *     y[r,j]  = (x[r,j] * rstd[r]) * w[j]
+ *
+ * Arithmetic is fp32 for both entry points (bf16 inputs are widened exactly;
+ * the bf16 output is one round-to-nearest-even rounding of the fp32 product).
+ *
+ * Common contract of the compute entry points
+ * -------------------------------------------
+ *  - x, w, y are DEVICE pointers owned by the caller.  x and y hold
+ *    rows*hidden elements, contiguous and row-major (row pitch == hidden);
+ *    w holds hidden elements.  Any alignment of the element type is accepted;
+ *    the library picks the widest vector width the pointers and the row pitch
+ *    allow.
+ *  - y == x (exact in-place) is allowed; any other overlap of x and y is
+ *    rejected.  w may not overlap y.
+ *  - The call is asynchronous on `stream` (NULL = the legacy default stream)
+ *    and allocates no memory.  Argument errors are detected on the host
+ *    before any launch and leave the device untouched.
+ *  - rows == 0 returns RMSNORM_OK without a launch.
+ *  - The library's only device state is one status word per device, written
+ *    by a kernel whose bounded wait ran out (see rmsnorm_last_device_status).
+ *
+ * Thread safety: calls may be made from several host threads; per-device set-up
+ * is done once under a lock.
+ */
+#ifndef RMSNORM_H_
+#define RMSNORM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; spelled out so this header needs no CUDA headers. */
+typedef struct CUstream_st* rmsnorm_stream_t;
+
+typedef enum {
+    RMSNORM_OK = 0,
+    RMSNORM_ERR_INVALID_ARG = 1,  /* bad pointer, size, eps or overlap; nothing launched */
+    RMSNORM_ERR_UNSUPPORTED = 2,  /* a forced path/option cannot serve these arguments */
+    RMSNORM_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    RMSNORM_ERR_TIMEOUT = 4       /* a kernel's bounded wait expired (device status) */
+} rmsnorm_status_t;
+
+typedef enum {
+    RMSNORM_DTYPE_F32 = 0,
+    RMSNORM_DTYPE_BF16 = 1
+} rmsnorm_dtype_t;
+
+/* Kernel families.  AUTO lets the dispatcher choose. */
+typedef enum {
+    RMSNORM_PATH_AUTO = 0,
+    RMSNORM_PATH_ROWREG = 1,   /* single pass, the row held in registers; a group of
+                                  threads per row, persistent grid-stride over rows   */
+    RMSNORM_PATH_STAGED = 2,   /* rows staged in shared memory by 1-D bulk copies
+                                  (cp.async.bulk + mbarrier), multi-stage prefetch    */
+    RMSNORM_PATH_CLUSTER = 3,  /* split row: a thread-block cluster per row, slices in
+                                  registers, partial sums exchanged through DSMEM     */
+    RMSNORM_PATH_TWOPASS = 4   /* generic fallback: read x twice (any width/alignment) */
+} rmsnorm_path_t;
+
+/* Options for rmsnorm_fwd_ex / rmsnorm_plan.  Zero-initialise, then set what you
+ * need; every zero field means "automatic". */
+typedef struct {
+    int32_t path;            /* rmsnorm_path_t */
+    int32_t cluster;         /* CTAs per row for CLUSTER (2..16) or STAGED (1..16) */
+    int32_t threads;         /* threads per row group (multiple of 32, <= 1024) */
+    int32_t grid;            /* CTAs to launch (rounded to the cluster size) */
+    int32_t vec_bytes;       /* 16, 8, 4 or 2 (bf16 only); must suit the alignment */
+    int32_t chunk_bytes;     /* STAGED: bytes per bulk copy (multiple of 16) */
+    uint64_t wait_timeout_ns;/* limit of every device-side wait; 0 = 2 seconds */
+} rmsnorm_options_t;
+
+/* What a call with these arguments would launch. */
+typedef struct {
+    int32_t path;            /* rmsnorm_path_t actually chosen */
+    int32_t cluster;         /* CTAs per row (1 unless split) */
+    int32_t threads_per_row; /* threads cooperating on one row (or one slice) */
+    int32_t block_threads;   /* threads per CTA */
+    int32_t rows_per_cta;    /* rows one CTA works on at a time */
+    int32_t grid;            /* CTAs launched */
+    int32_t vec_bytes;       /* bytes per global load/store instruction */
+    int32_t vecs_per_thread; /* register-resident vectors per thread and row */
+    int32_t smem_bytes;      /* dynamic shared memory per CTA */
+    int32_t chunk_bytes;     /* STAGED: bytes per bulk copy */
+    char kernel[48];         /* kernel family name, for profiles */
+} rmsnorm_plan_t;
+
+/*
+ * rmsnorm_fwd_f32 -- y = RMSNorm(x) * w for fp32 tensors.
+ * x, y: rows*hidden floats (device); w: hidden floats (device);
+ * rows >= 0; 1 <= hidden <= 2^31-1; eps finite and >= 0.
+ * Returns RMSNORM_OK once launched; RMSNORM_ERR_INVALID_ARG for NULL pointers,
+ * bad sizes, bad eps or partial overlap; RMSNORM_ERR_CUDA if a CUDA call fails
+ * (see rmsnorm_last_cuda_error).
+ */
+rmsnorm_status_t rmsnorm_fwd_f32(const float* x, const float* w, float* y,
+                                 int64_t rows, int64_t hidden, float eps,
+                                 rmsnorm_stream_t stream);
+
+/*
+ * rmsnorm_fwd_bf16 -- the same for bfloat16 tensors, passed as raw 16-bit
+ * patterns.  Accumulation, rstd and the products are fp32; each output is
+ * rounded once to bfloat16 (round-to-nearest-even).  Arguments and errors as
+ * for rmsnorm_fwd_f32.
+ */
+rmsnorm_status_t rmsnorm_fwd_bf16(const uint16_t* x, const uint16_t* w, uint16_t* y,
+                                  int64_t rows, int64_t hidden, float eps,
+                                  rmsnorm_stream_t stream);
+
+/*
+ * rmsnorm_fwd_ex -- either dtype, with explicit options (forced kernel family,
+ * cluster size, launch shape, wait limit).  `opt` may be NULL (= automatic).
+ * Returns RMSNORM_ERR_UNSUPPORTED when a forced option cannot serve the call
+ * (e.g. STAGED on a row pitch that is not a multiple of 16 bytes); nothing is
+ * launched in that case.
+ */
+rmsnorm_status_t rmsnorm_fwd_ex(int32_t dtype, const void* x, const void* w, void* y,
+                                int64_t rows, int64_t hidden, float eps,
+                                const rmsnorm_options_t* opt, rmsnorm_stream_t stream);
+
+/*
+ * rmsnorm_plan -- fill *plan with what rmsnorm_fwd_ex(dtype, x, w, y, rows,
+ * hidden, ., opt, .) would launch on the current device, without launching.
+ * Pointers are used only for their alignment (they may be any non-NULL values).
+ */
+rmsnorm_status_t rmsnorm_plan(int32_t dtype, const void* x, const void* w, const void* y,
+                              int64_t rows, int64_t hidden,
+                              const rmsnorm_options_t* opt, rmsnorm_plan_t* plan);
+
+/*
+ * rmsnorm_last_device_status -- synchronise `stream`, then read and clear the
+ * current device's status word.  RMSNORM_OK if no kernel's bounded wait has
+ * expired since the last read; RMSNORM_ERR_TIMEOUT otherwise (outputs of the
+ * affected call are undefined); RMSNORM_ERR_CUDA if synchronisation failed.
+ */
+rmsnorm_status_t rmsnorm_last_device_status(rmsnorm_stream_t stream);
+
+/* Static English text for a status code (never NULL). */
+const char* rmsnorm_status_string(rmsnorm_status_t status);
+
+/*
+ * rmsnorm_last_cuda_error -- the cudaError_t of the last CUDA runtime call of
+ * this library that failed on the calling host thread (0 if none), and clears
+ * it.  If msg != NULL and len > 0, writes "<name>: <description>" there
+ * (truncated, NUL-terminated).  The library links the CUDA runtime
+ * statically, so this -- not the caller's cudaGetLastError -- is where an
+ * RMSNORM_ERR_CUDA is explained.
+ */
+int32_t rmsnorm_last_cuda_error(char* msg, size_t len);
+
+/* ABI version of this header: major*10000 + minor*100 + patch. */
+int32_t rmsnorm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_H_ */

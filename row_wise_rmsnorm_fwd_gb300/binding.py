@@ -1,0 +1,274 @@
+"""ctypes binding of librmsnorm's C ABI (``include/rmsnorm.h``).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``librmsnorm.so``.  Functions carry the C names.  Tensor-level
+functions take torch CUDA tensors (torch supplies device memory and the
+current stream); the ``raw`` namespace takes plain integers (device pointers
+and a ``cudaStream_t`` handle) and returns the C status code.
+
+If the library has not been built this module raises on first use: there is
+no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from types import SimpleNamespace
+
+from . import build as _build
+
+RMSNORM_OK = 0
+RMSNORM_ERR_INVALID_ARG = 1
+RMSNORM_ERR_UNSUPPORTED = 2
+RMSNORM_ERR_CUDA = 3
+RMSNORM_ERR_TIMEOUT = 4
+
+RMSNORM_DTYPE_F32 = 0
+RMSNORM_DTYPE_BF16 = 1
+
+PATHS = {"auto": 0, "rowreg": 1, "staged": 2, "cluster": 3, "twopass": 4}
+PATH_NAMES = {v: k for k, v in PATHS.items()}
+
+
+class rmsnorm_options_t(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("cluster", ctypes.c_int32),
+                ("threads", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("vec_bytes", ctypes.c_int32), ("chunk_bytes", ctypes.c_int32),
+                ("wait_timeout_ns", ctypes.c_uint64)]
+
+
+class rmsnorm_plan_t(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("cluster", ctypes.c_int32),
+                ("threads_per_row", ctypes.c_int32), ("block_threads", ctypes.c_int32),
+                ("rows_per_cta", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("vec_bytes", ctypes.c_int32), ("vecs_per_thread", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32), ("chunk_bytes", ctypes.c_int32),
+                ("kernel", ctypes.c_char * 48)]
+
+
+class RmsnormError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        detail = ""
+        if status == RMSNORM_ERR_CUDA:
+            code, text = rmsnorm_last_cuda_error()
+            detail = f" [{text}]" if code else ""
+        super().__init__(f"{what}: {rmsnorm_status_string(status)} (status {status}){detail}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load librmsnorm.so (built in-tree by ``build.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with row_wise_rmsnorm_fwd_gb300.build.build() "
+                "(there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+        for name in ("rmsnorm_fwd_f32", "rmsnorm_fwd_bf16"):
+            fn = getattr(lib, name)
+            fn.argtypes = [vp, vp, vp, i64, i64, f32, vp]
+            fn.restype = ctypes.c_int
+        lib.rmsnorm_fwd_ex.argtypes = [i32, vp, vp, vp, i64, i64, f32,
+                                       ctypes.POINTER(rmsnorm_options_t), vp]
+        lib.rmsnorm_fwd_ex.restype = ctypes.c_int
+        lib.rmsnorm_plan.argtypes = [i32, vp, vp, vp, i64, i64,
+                                     ctypes.POINTER(rmsnorm_options_t),
+                                     ctypes.POINTER(rmsnorm_plan_t)]
+        lib.rmsnorm_plan.restype = ctypes.c_int
+        lib.rmsnorm_last_device_status.argtypes = [vp]
+        lib.rmsnorm_last_device_status.restype = ctypes.c_int
+        lib.rmsnorm_status_string.argtypes = [ctypes.c_int]
+        lib.rmsnorm_status_string.restype = ctypes.c_char_p
+        lib.rmsnorm_last_cuda_error.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
+        lib.rmsnorm_last_cuda_error.restype = ctypes.c_int32
+        lib.rmsnorm_abi_version.argtypes = []
+        lib.rmsnorm_abi_version.restype = ctypes.c_int32
+        _lib = lib
+        return lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions declared in include/*.h (for export checks)."""
+    names = []
+    inc = os.path.join(_build.ROOT, "include")
+    for fname in sorted(os.listdir(inc)):
+        if not fname.endswith(".h"):
+            continue
+        text = open(os.path.join(inc, fname)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b(rmsnorm_[a-z0-9_]+)\s*\(", text):
+            if m.group(1) not in names:
+                names.append(m.group(1))
+    return names
+
+
+def make_options(path="auto", cluster=0, threads=0, grid=0, vec_bytes=0,
+                 chunk_bytes=0, wait_timeout_ns=0) -> rmsnorm_options_t:
+    o = rmsnorm_options_t()
+    o.path = PATHS[path] if isinstance(path, str) else int(path)
+    o.cluster, o.threads, o.grid = int(cluster), int(threads), int(grid)
+    o.vec_bytes, o.chunk_bytes = int(vec_bytes), int(chunk_bytes)
+    o.wait_timeout_ns = int(wait_timeout_ns)
+    return o
+
+
+# ------------------------------------------------------------ raw pointers --
+
+def _raw_fwd_f32(x, w, y, rows, hidden, eps, stream=0) -> int:
+    return load().rmsnorm_fwd_f32(x, w, y, rows, hidden, eps, stream or None)
+
+
+def _raw_fwd_bf16(x, w, y, rows, hidden, eps, stream=0) -> int:
+    return load().rmsnorm_fwd_bf16(x, w, y, rows, hidden, eps, stream or None)
+
+
+def _raw_fwd_ex(dtype, x, w, y, rows, hidden, eps, options=None, stream=0) -> int:
+    opt = ctypes.byref(options) if options is not None else None
+    return load().rmsnorm_fwd_ex(dtype, x, w, y, rows, hidden, eps, opt, stream or None)
+
+
+def _raw_plan(dtype, x, w, y, rows, hidden, options=None):
+    plan = rmsnorm_plan_t()
+    opt = ctypes.byref(options) if options is not None else None
+    st = load().rmsnorm_plan(dtype, x, w, y, rows, hidden, opt, ctypes.byref(plan))
+    return st, plan
+
+
+raw = SimpleNamespace(rmsnorm_fwd_f32=_raw_fwd_f32, rmsnorm_fwd_bf16=_raw_fwd_bf16,
+                      rmsnorm_fwd_ex=_raw_fwd_ex, rmsnorm_plan=_raw_plan)
+
+
+# ------------------------------------------------------------------ tensors --
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check_tensors(x, w, y, dtype):
+    torch = _torch()
+    want = torch.float32 if dtype == RMSNORM_DTYPE_F32 else torch.bfloat16
+    for name, t in (("x", x), ("w", w), ("y", y)):
+        if t.dtype != want:
+            raise TypeError(f"{name} must be {want}, got {t.dtype}")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    hidden = x.shape[-1] if x.dim() > 0 else 0
+    if w.dim() != 1 or w.shape[0] != hidden:
+        raise ValueError(f"w must have shape ({hidden},), got {tuple(w.shape)}")
+    if y.shape != x.shape:
+        raise ValueError(f"y must have the shape of x {tuple(x.shape)}, got {tuple(y.shape)}")
+    rows = x.numel() // hidden if hidden else 0
+    return rows, hidden
+
+
+def _fwd(dtype, x, w, y, eps, options, stream):
+    if y is None:
+        y = _torch().empty_like(x)
+    rows, hidden = _check_tensors(x, w, y, dtype)
+    st = _raw_fwd_ex(dtype, x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, hidden,
+                     float(eps), options, _stream_handle(stream))
+    if st != RMSNORM_OK:
+        raise RmsnormError(st, "rmsnorm forward")
+    return y
+
+
+def rmsnorm_fwd_f32(x, w, y=None, eps: float = 1e-6, stream=None):
+    """y = RMSNorm(x) * w for float32 CUDA tensors (last dim = hidden)."""
+    if y is None:
+        y = _torch().empty_like(x)
+    rows, hidden = _check_tensors(x, w, y, RMSNORM_DTYPE_F32)
+    st = _raw_fwd_f32(x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, hidden, float(eps),
+                      _stream_handle(stream))
+    if st != RMSNORM_OK:
+        raise RmsnormError(st, "rmsnorm_fwd_f32")
+    return y
+
+
+def rmsnorm_fwd_bf16(x, w, y=None, eps: float = 1e-6, stream=None):
+    """y = RMSNorm(x) * w for bfloat16 CUDA tensors (fp32 arithmetic)."""
+    if y is None:
+        y = _torch().empty_like(x)
+    rows, hidden = _check_tensors(x, w, y, RMSNORM_DTYPE_BF16)
+    st = _raw_fwd_bf16(x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, hidden, float(eps),
+                       _stream_handle(stream))
+    if st != RMSNORM_OK:
+        raise RmsnormError(st, "rmsnorm_fwd_bf16")
+    return y
+
+
+def rmsnorm_fwd_ex(x, w, y=None, eps: float = 1e-6, options=None, stream=None):
+    """Either dtype, with explicit options (see ``make_options``)."""
+    torch = _torch()
+    dtype = RMSNORM_DTYPE_F32 if x.dtype == torch.float32 else RMSNORM_DTYPE_BF16
+    if isinstance(options, dict):
+        options = make_options(**options)
+    return _fwd(dtype, x, w, y, eps, options, stream)
+
+
+def rmsnorm_plan(x, w, y=None, options=None) -> dict:
+    """What rmsnorm_fwd_ex would launch for these tensors (no launch)."""
+    torch = _torch()
+    dtype = RMSNORM_DTYPE_F32 if x.dtype == torch.float32 else RMSNORM_DTYPE_BF16
+    if isinstance(options, dict):
+        options = make_options(**options)
+    y_ptr = (y if y is not None else x).data_ptr()
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden
+    st, plan = _raw_plan(dtype, x.data_ptr(), w.data_ptr(), y_ptr, rows, hidden, options)
+    if st != RMSNORM_OK:
+        raise RmsnormError(st, "rmsnorm_plan")
+    d = {f: getattr(plan, f) for f, _ in rmsnorm_plan_t._fields_ if f != "kernel"}
+    d["kernel"] = plan.kernel.decode()
+    d["path_name"] = PATH_NAMES.get(plan.path, "?")
+    return d
+
+
+def rmsnorm_last_device_status(stream=None) -> int:
+    return load().rmsnorm_last_device_status(_stream_handle(stream) or None)
+
+
+def rmsnorm_status_string(status: int) -> str:
+    try:
+        return load().rmsnorm_status_string(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def rmsnorm_last_cuda_error():
+    """(cudaError_t code, "name: description") of the library's last failed
+    CUDA call on this thread; clears it."""
+    buf = ctypes.create_string_buffer(256)
+    code = load().rmsnorm_last_cuda_error(buf, len(buf))
+    return code, buf.value.decode(errors="replace")
+
+
+def rmsnorm_abi_version() -> int:
+    return load().rmsnorm_abi_version()

@@ -1,0 +1,535 @@
+// api.cu -- the C ABI of librmsnorm: argument validation, per-device set-up,
+// kernel-family selection (the launch heuristics) and the launch itself.
+//
+// Operation: page "A hackable Python ML compiler, part 2", RMSNorm Loop IR:
+// y[r,j] = (x[r,j] * rsqrt(mean_j x[r,j]^2 + eps)) * w[j].
+#include "rmsnorm.h"
+#include "launch.h"
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+// The device status word: written only by a kernel whose bounded wait
+// expired; read and cleared by rmsnorm_last_device_status.
+__device__ unsigned g_rmsnorm_status = 0u;
+
+namespace rmsnorm {
+
+KernelFn rowreg_kernel_ptr(int dtype, int vb, int nv) {
+    return dtype == 0 ? rowreg_kernel_f32(vb, nv) : rowreg_kernel_bf16(vb, nv);
+}
+int rowreg_max_block(int nv) { return nv >= 4 ? 512 : 1024; }
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s
+
+// The CUDA runtime is linked statically, so its error state is private to
+// this library; the last failing call's error is kept per host thread.
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+cudaError_t note(cudaError_t e) {
+    if (e != cudaSuccess) t_last_cuda_error = e;
+    return e;
+}
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    int sms = 0;
+    int smem_optin = 0;
+    unsigned* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+cudaError_t init_device(DeviceInfo& d, int dev) {
+    cudaError_t e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess)
+        e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_rmsnorm_status);
+    return e;
+}
+
+cudaError_t current_device(DeviceInfo** out, int* dev_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return note(e);
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    DeviceInfo& d = g_dev[dev];
+    std::call_once(d.once, [&] { d.err = init_device(d, dev); });
+    *out = &d;
+    if (dev_out) *dev_out = dev;
+    return note(d.err);
+}
+
+// Kernels are prepared once per device; occupancy answers are cached per
+// (device, kernel, block, smem, cluster).
+std::mutex g_occ_mu;
+std::map<std::tuple<int, KernelFn, int, int, int>, int> g_occ;
+std::map<std::pair<int, KernelFn>, cudaError_t> g_prepared;
+
+cudaError_t ensure_prepared(int dev, KernelFn fn, int smem_limit) {
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    const auto key = std::make_pair(dev, fn);
+    auto it = g_prepared.find(key);
+    if (it != g_prepared.end()) return it->second;
+    const cudaError_t e = prepare_kernel(fn, smem_limit);
+    g_prepared[key] = e;
+    return note(e);
+}
+
+cudaError_t cached_occupancy(int dev, KernelFn fn, int block, int smem, int cluster, int* out) {
+    const auto key = std::make_tuple(dev, fn, block, smem, cluster);
+    {
+        std::lock_guard<std::mutex> lk(g_occ_mu);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) { *out = it->second; return cudaSuccess; }
+    }
+    int v = 0;
+    cudaError_t e = ensure_prepared(dev, fn, g_dev[dev].smem_optin);
+    if (e == cudaSuccess) {
+        if (cluster > 1) {
+            e = max_active_clusters(fn, block, smem, cluster, &v);
+        } else {
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &v, reinterpret_cast<const void*>(fn), block, static_cast<size_t>(smem));
+        }
+    }
+    if (e != cudaSuccess) {
+        // A cluster shape the device cannot run is "zero clusters", not an error.
+        if (cluster > 1) { cudaGetLastError(); v = 0; e = cudaSuccess; }
+        else return note(e);
+    }
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    g_occ[key] = v;
+    *out = v;
+    return cudaSuccess;
+}
+
+struct Call {
+    int dtype;
+    int sz;                 // element bytes
+    uintptr_t x, w, y;
+    int64_t rows;
+    int64_t hidden;
+    rmsnorm_options_t opt;
+    int dev;
+    DeviceInfo* info;
+};
+
+struct Plan {
+    int path = 0;
+    int cluster = 1;
+    int group = 0;
+    int block = 0;
+    int rpc = 1;
+    int grid = 0;
+    int vb = 0;
+    int nv = 0;
+    int smem = 0;
+    int chunk = 0;
+    int nchunks = 0;
+    int nvec = 0;
+    int slice_vecs = 0;
+    KernelFn fn = nullptr;
+    const char* name = "";
+};
+
+int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+int round_up(int64_t a, int64_t b) { return static_cast<int>(((a + b - 1) / b) * b); }
+int pow2_ceil(int v) { int p = 1; while (p < v) p <<= 1; return p; }
+int pow2_floor(int64_t v) { int p = 1; while (static_cast<int64_t>(p) * 2 <= v) p <<= 1; return p; }
+
+// Widest vector width that the pointers and the row pitch allow.
+int widest_vb(const Call& c) {
+    const uintptr_t a = c.x | c.w | c.y;
+    const int64_t pitch = c.hidden * c.sz;
+    for (int vb = 16; vb >= c.sz; vb >>= 1)
+        if (a % vb == 0 && pitch % vb == 0) return vb;
+    return c.sz;
+}
+
+rmsnorm_status_t pick_vb(const Call& c, int* vb) {
+    const int widest = widest_vb(c);
+    const int f = c.opt.vec_bytes;
+    if (f == 0) { *vb = widest; return RMSNORM_OK; }
+    if (f != 2 && f != 4 && f != 8 && f != 16) return RMSNORM_ERR_INVALID_ARG;
+    if (f < c.sz || f > widest) return RMSNORM_ERR_UNSUPPORTED;
+    *vb = f;
+    return RMSNORM_OK;
+}
+
+// Register-resident kernel; cluster > 1 splits each row over a cluster.
+rmsnorm_status_t plan_rowreg(const Call& c, int cluster, Plan* P) {
+    int vb;
+    rmsnorm_status_t st = pick_vb(c, &vb);
+    if (st != RMSNORM_OK) return st;
+    const int epv = vb / c.sz;
+    const int64_t nvec = c.hidden / epv;
+    const int64_t per = cluster > 1 ? (nvec + cluster - 1) / cluster : nvec;
+    int G, NV;
+    if (c.opt.threads > 0) {
+        G = c.opt.threads;
+        if (G % 32 != 0 || G > 1024) return RMSNORM_ERR_INVALID_ARG;
+        const int64_t need = (per + G - 1) / G;
+        if (need > 8) return RMSNORM_ERR_UNSUPPORTED;
+        NV = pow2_ceil(static_cast<int>(need));
+    } else if (cluster == 1 && per <= 32 * 4) {
+        G = 32;
+        NV = pow2_ceil(ceil_div(per, 32));
+    } else {
+        // 4 vectors per thread (64 B at 16-byte vectors) with a register double
+        // buffer; rows wider than 512 threads x 4 vectors use 8 per thread.
+        NV = 4;
+        int64_t g = round_up((per + NV - 1) / NV, 32);
+        if (g > rowreg_max_block(NV)) {
+            NV = 8;
+            g = round_up((per + NV - 1) / NV, 32);
+        }
+        if (g > rowreg_max_block(NV)) return RMSNORM_ERR_UNSUPPORTED;
+        G = static_cast<int>(g);
+    }
+    if (G > rowreg_max_block(NV)) return RMSNORM_ERR_UNSUPPORTED;
+    KernelFn fn = rowreg_kernel_ptr(c.dtype, vb, NV);
+    if (!fn) return RMSNORM_ERR_UNSUPPORTED;
+    const int rpc = cluster == 1 ? (G >= 256 ? 1 : 256 / G) : 1;
+    const int block = G * rpc;
+    int occ = 0;
+    if (cached_occupancy(c.dev, fn, block, 0, cluster, &occ) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
+    int grid;
+    if (cluster == 1) {
+        const int64_t nblocks = (c.rows + rpc - 1) / rpc;
+        const int64_t resident = static_cast<int64_t>(c.info->sms) * occ;
+        grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
+                                               : (nblocks < resident ? nblocks : resident));
+    } else {
+        const int64_t nclusters = c.opt.grid > 0 ? (c.opt.grid + cluster - 1) / cluster
+                                                 : (c.rows < occ ? c.rows : occ);
+        grid = static_cast<int>(nclusters * cluster);
+    }
+    P->path = cluster == 1 ? RMSNORM_PATH_ROWREG : RMSNORM_PATH_CLUSTER;
+    P->cluster = cluster;
+    P->group = G;
+    P->block = block;
+    P->rpc = rpc;
+    P->grid = grid;
+    P->vb = vb;
+    P->nv = NV;
+    P->smem = 0;
+    P->nvec = static_cast<int>(nvec);
+    P->slice_vecs = static_cast<int>(per);
+    P->fn = fn;
+    P->name = cluster == 1 ? "rowreg" : "cluster_rowreg";
+    return RMSNORM_OK;
+}
+
+// Bulk-copy staged kernel; needs 16-byte aligned pointers and row pitch.
+rmsnorm_status_t plan_staged(const Call& c, int cluster, Plan* P) {
+    if (c.opt.vec_bytes != 0 && c.opt.vec_bytes != 16) return RMSNORM_ERR_UNSUPPORTED;
+    if (widest_vb(c) != 16) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t row_bytes = c.hidden * c.sz;
+    const int64_t vecs = row_bytes / 16;
+    const int64_t slice_vecs = (vecs + cluster - 1) / cluster;
+    const int64_t slice_bytes = slice_vecs * 16;
+    int64_t chunk = c.opt.chunk_bytes;
+    if (chunk != 0) {
+        if (chunk % 16 != 0 || chunk <= 0) return RMSNORM_ERR_INVALID_ARG;
+    } else {
+        chunk = slice_bytes < 16384 ? slice_bytes : 16384;
+    }
+    int64_t nchunks = (slice_bytes + chunk - 1) / chunk;
+    if (nchunks > kStagedMaxChunksHost) {
+        if (c.opt.chunk_bytes != 0) return RMSNORM_ERR_UNSUPPORTED;
+        chunk = round_up((slice_bytes + kStagedMaxChunksHost - 1) / kStagedMaxChunksHost, 16);
+        nchunks = (slice_bytes + chunk - 1) / chunk;
+    }
+    if (chunk * nchunks > c.info->smem_optin) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t smem = staged_smem_bytes(static_cast<int>(chunk), static_cast<int>(nchunks));
+    if (smem <= 0 || smem > c.info->smem_optin) return RMSNORM_ERR_UNSUPPORTED;
+    KernelFn fn = staged_kernel_ptr(c.dtype);
+    int occ = 0;
+    if (cached_occupancy(c.dev, fn, kStagedThreads, static_cast<int>(smem), cluster, &occ) !=
+        cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
+    int grid;
+    if (cluster == 1) {
+        const int64_t resident = static_cast<int64_t>(c.info->sms) * occ;
+        grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
+                                               : (c.rows < resident ? c.rows : resident));
+    } else {
+        const int64_t nclusters = c.opt.grid > 0 ? (c.opt.grid + cluster - 1) / cluster
+                                                 : (c.rows < occ ? c.rows : occ);
+        grid = static_cast<int>(nclusters * cluster);
+    }
+    P->path = RMSNORM_PATH_STAGED;
+    P->cluster = cluster;
+    P->group = 32 * kStagedConsumerWarps;
+    P->block = kStagedThreads;
+    P->rpc = 1;
+    P->grid = grid;
+    P->vb = 16;
+    P->nv = 0;
+    P->smem = static_cast<int>(smem);
+    P->chunk = static_cast<int>(chunk);
+    P->nchunks = static_cast<int>(nchunks);
+    P->nvec = static_cast<int>(vecs);
+    P->slice_vecs = static_cast<int>(slice_vecs);
+    P->fn = fn;
+    P->name = cluster == 1 ? "staged_bulk" : "staged_bulk_cluster";
+    return RMSNORM_OK;
+}
+
+// Generic fallback: any width and alignment.
+rmsnorm_status_t plan_twopass(const Call& c, Plan* P) {
+    int vb;
+    rmsnorm_status_t st = pick_vb(c, &vb);
+    if (st != RMSNORM_OK) return st;
+    KernelFn fn = twopass_kernel_ptr(c.dtype, vb);
+    if (!fn) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t nvec = c.hidden / (vb / c.sz);
+    int block = c.opt.threads > 0 ? c.opt.threads
+                                  : (nvec >= twopass_block() ? twopass_block()
+                                                             : round_up(nvec, 32));
+    if (block % 32 != 0 || block > twopass_block()) return RMSNORM_ERR_INVALID_ARG;
+    int occ = 0;
+    if (cached_occupancy(c.dev, fn, block, 0, 1, &occ) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t resident = static_cast<int64_t>(c.info->sms) * occ;
+    P->path = RMSNORM_PATH_TWOPASS;
+    P->cluster = 1;
+    P->group = block;
+    P->block = block;
+    P->rpc = 1;
+    P->grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
+                                              : (c.rows < resident ? c.rows : resident));
+    P->vb = vb;
+    P->nv = 0;
+    P->nvec = static_cast<int>(nvec);
+    P->slice_vecs = static_cast<int>(nvec);
+    P->fn = fn;
+    P->name = "twopass";
+    return RMSNORM_OK;
+}
+
+// The launch heuristics.  Enough rows to give every SM a row: one CTA (or a
+// warp) per row.  Few rows: split each row over a cluster so that about one
+// CTA per SM works, keeping slices of at least 4 KB.  Rows too wide for one
+// CTA's registers go to the staged kernel, then to wider clusters, and
+// finally to the two-pass kernel.
+rmsnorm_status_t plan_auto(const Call& c, Plan* P) {
+    const int64_t row_bytes = c.hidden * c.sz;
+    int want = 1;
+    if (c.rows < c.info->sms) {
+        want = pow2_floor(c.info->sms / (c.rows > 0 ? c.rows : 1));
+        if (want > 16) want = 16;
+        while (want > 1 && row_bytes / want < 4096) want >>= 1;
+    }
+    rmsnorm_status_t st;
+    for (int cl = want; cl <= 16; cl <<= 1) {
+        st = plan_rowreg(c, cl, P);
+        if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+    }
+    for (int cl = want; cl <= 16; cl <<= 1) {
+        st = plan_staged(c, cl, P);
+        if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+    }
+    return plan_twopass(c, P);
+}
+
+rmsnorm_status_t make_plan(const Call& c, Plan* P) {
+    const int cl = c.opt.cluster;
+    if (cl < 0 || cl > 16) return RMSNORM_ERR_INVALID_ARG;
+    switch (c.opt.path) {
+        case RMSNORM_PATH_AUTO:
+            if (cl != 0 || c.opt.threads != 0 || c.opt.chunk_bytes != 0)
+                return RMSNORM_ERR_INVALID_ARG;
+            return plan_auto(c, P);
+        case RMSNORM_PATH_ROWREG:
+            if (cl > 1) return RMSNORM_ERR_INVALID_ARG;
+            return plan_rowreg(c, 1, P);
+        case RMSNORM_PATH_CLUSTER:
+            if (cl == 1 || (cl & (cl - 1)) != 0) return RMSNORM_ERR_INVALID_ARG;
+            return plan_rowreg(c, cl == 0 ? 2 : cl, P);
+        case RMSNORM_PATH_STAGED:
+            return plan_staged(c, cl == 0 ? 1 : cl, P);
+        case RMSNORM_PATH_TWOPASS:
+            if (cl > 1) return RMSNORM_ERR_INVALID_ARG;
+            return plan_twopass(c, P);
+        default:
+            return RMSNORM_ERR_INVALID_ARG;
+    }
+}
+
+bool ranges_overlap(uintptr_t a, uintptr_t b, uint64_t na, uint64_t nb) {
+    return a < b + nb && b < a + na;
+}
+
+// Host-side validation; fills `c` on success.
+rmsnorm_status_t validate(int32_t dtype, const void* x, const void* w, const void* y,
+                          int64_t rows, int64_t hidden, const rmsnorm_options_t* opt,
+                          Call* c) {
+    if (dtype != RMSNORM_DTYPE_F32 && dtype != RMSNORM_DTYPE_BF16) return RMSNORM_ERR_INVALID_ARG;
+    if (!x || !w || !y) return RMSNORM_ERR_INVALID_ARG;
+    if (rows < 0 || hidden <= 0 || hidden > 0x7FFFFFFFll) return RMSNORM_ERR_INVALID_ARG;
+    const int sz = dtype == RMSNORM_DTYPE_F32 ? 4 : 2;
+    if (rows > 0 && rows > (INT64_MAX / sz) / hidden) return RMSNORM_ERR_INVALID_ARG;
+    const uintptr_t ux = reinterpret_cast<uintptr_t>(x);
+    const uintptr_t uw = reinterpret_cast<uintptr_t>(w);
+    const uintptr_t uy = reinterpret_cast<uintptr_t>(y);
+    if (ux % sz || uw % sz || uy % sz) return RMSNORM_ERR_INVALID_ARG;
+    const uint64_t nbytes = static_cast<uint64_t>(rows) * static_cast<uint64_t>(hidden) * sz;
+    const uint64_t wbytes = static_cast<uint64_t>(hidden) * sz;
+    if (ux != uy && ranges_overlap(ux, uy, nbytes, nbytes)) return RMSNORM_ERR_INVALID_ARG;
+    if (rows > 0 && ranges_overlap(uw, uy, wbytes, nbytes)) return RMSNORM_ERR_INVALID_ARG;
+    std::memset(c, 0, sizeof(*c));
+    c->dtype = dtype;
+    c->sz = sz;
+    c->x = ux;
+    c->w = uw;
+    c->y = uy;
+    c->rows = rows;
+    c->hidden = hidden;
+    if (opt) c->opt = *opt;
+    return RMSNORM_OK;
+}
+
+rmsnorm_status_t run(int32_t dtype, const void* x, const void* w, void* y, int64_t rows,
+                     int64_t hidden, float eps, const rmsnorm_options_t* opt,
+                     cudaStream_t stream) {
+    Call c;
+    rmsnorm_status_t st = validate(dtype, x, w, y, rows, hidden, opt, &c);
+    if (st != RMSNORM_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
+    if (rows == 0) return RMSNORM_OK;
+    if (current_device(&c.info, &c.dev) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    Plan P;
+    st = make_plan(c, &P);
+    if (st != RMSNORM_OK) return st;
+
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = x;
+    p.w = w;
+    p.y = y;
+    p.rows = rows;
+    p.hidden = static_cast<int32_t>(hidden);
+    p.nvec = P.nvec;
+    p.inv_hidden = 1.0f / static_cast<float>(hidden);
+    p.eps = eps;
+    p.group = P.group;
+    p.rows_per_cta = P.rpc;
+    p.cluster = P.cluster;
+    p.slice_vecs = P.slice_vecs;
+    p.chunk_bytes = P.chunk;
+    p.nchunks = P.nchunks;
+    p.status = c.info->status;
+    p.timeout_ns = c.opt.wait_timeout_ns ? c.opt.wait_timeout_ns : kDefaultTimeoutNs;
+
+    LaunchShape s{P.grid, P.block, P.cluster, P.smem};
+    if (ensure_prepared(c.dev, P.fn, c.info->smem_optin) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (note(launch_ex(P.fn, s, stream, p)) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    return RMSNORM_OK;
+}
+
+}  // namespace
+}  // namespace rmsnorm
+
+using namespace rmsnorm;
+
+extern "C" {
+
+rmsnorm_status_t rmsnorm_fwd_f32(const float* x, const float* w, float* y, int64_t rows,
+                                 int64_t hidden, float eps, rmsnorm_stream_t stream) {
+    return run(RMSNORM_DTYPE_F32, x, w, y, rows, hidden, eps, nullptr,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+rmsnorm_status_t rmsnorm_fwd_bf16(const uint16_t* x, const uint16_t* w, uint16_t* y,
+                                  int64_t rows, int64_t hidden, float eps,
+                                  rmsnorm_stream_t stream) {
+    return run(RMSNORM_DTYPE_BF16, x, w, y, rows, hidden, eps, nullptr,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+rmsnorm_status_t rmsnorm_fwd_ex(int32_t dtype, const void* x, const void* w, void* y,
+                                int64_t rows, int64_t hidden, float eps,
+                                const rmsnorm_options_t* opt, rmsnorm_stream_t stream) {
+    return run(dtype, x, w, y, rows, hidden, eps, opt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+rmsnorm_status_t rmsnorm_plan(int32_t dtype, const void* x, const void* w, const void* y,
+                              int64_t rows, int64_t hidden, const rmsnorm_options_t* opt,
+                              rmsnorm_plan_t* plan) {
+    if (!plan) return RMSNORM_ERR_INVALID_ARG;
+    Call c;
+    rmsnorm_status_t st = validate(dtype, x, w, y, rows, hidden, opt, &c);
+    if (st != RMSNORM_OK) return st;
+    if (current_device(&c.info, &c.dev) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (c.rows == 0) c.rows = 1;   // describe the launch a one-row call would make
+    Plan P;
+    st = make_plan(c, &P);
+    if (st != RMSNORM_OK) return st;
+    std::memset(plan, 0, sizeof(*plan));
+    plan->path = P.path;
+    plan->cluster = P.cluster;
+    plan->threads_per_row = P.group;
+    plan->block_threads = P.block;
+    plan->rows_per_cta = P.rpc;
+    plan->grid = P.grid;
+    plan->vec_bytes = P.vb;
+    plan->vecs_per_thread = P.nv;
+    plan->smem_bytes = P.smem;
+    plan->chunk_bytes = P.chunk;
+    std::snprintf(plan->kernel, sizeof(plan->kernel), "%s", P.name);
+    return RMSNORM_OK;
+}
+
+rmsnorm_status_t rmsnorm_last_device_status(rmsnorm_stream_t stream) {
+    DeviceInfo* info = nullptr;
+    if (current_device(&info, nullptr) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (note(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    unsigned word = 0;
+    if (note(cudaMemcpy(&word, info->status, sizeof(word), cudaMemcpyDeviceToHost)) !=
+        cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (word != 0) {
+        const unsigned zero = 0;
+        if (note(cudaMemcpy(info->status, &zero, sizeof(zero), cudaMemcpyHostToDevice)) !=
+            cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+    }
+    return word == 0 ? RMSNORM_OK : static_cast<rmsnorm_status_t>(word & 0xFFu);
+}
+
+const char* rmsnorm_status_string(rmsnorm_status_t status) {
+    switch (status) {
+        case RMSNORM_OK: return "ok";
+        case RMSNORM_ERR_INVALID_ARG: return "invalid argument";
+        case RMSNORM_ERR_UNSUPPORTED: return "unsupported option for these arguments";
+        case RMSNORM_ERR_CUDA: return "CUDA runtime error";
+        case RMSNORM_ERR_TIMEOUT: return "device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int32_t rmsnorm_last_cuda_error(char* msg, size_t len) {
+    const cudaError_t e = t_last_cuda_error;
+    if (msg && len > 0)
+        std::snprintf(msg, len, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    t_last_cuda_error = cudaSuccess;
+    return static_cast<int32_t>(e);
+}
+
+int32_t rmsnorm_abi_version(void) { return 10000; }
+
+}  // extern "C"

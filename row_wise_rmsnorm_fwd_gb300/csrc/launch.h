@@ -1,0 +1,89 @@
+// launch.h -- host-side interface between the C ABI (api.cu) and the
+// translation units that instantiate the kernels.  Internal to the library.
+#pragma once
+#include <cuda_runtime.h>
+#include "common.cuh"
+
+namespace rmsnorm {
+
+using KernelFn = void (*)(Params);
+
+struct LaunchShape {
+    int grid;       // CTAs
+    int block;      // threads per CTA
+    int cluster;    // CTAs per cluster (1 = plain launch)
+    int smem;       // dynamic shared memory bytes
+};
+
+// Kernel instances; nullptr when the combination is not compiled.
+// dtype: 0 = fp32, 1 = bf16.  vb = bytes per vector, nv = vectors per thread.
+KernelFn rowreg_kernel_f32(int vb, int nv);
+KernelFn rowreg_kernel_bf16(int vb, int nv);
+KernelFn rowreg_kernel_ptr(int dtype, int vb, int nv);
+int rowreg_max_block(int nv);
+KernelFn twopass_kernel_ptr(int dtype, int vb);
+int twopass_block();
+KernelFn staged_kernel_ptr(int dtype);
+
+// Staged kernel geometry: one producer warp plus consumer warps.
+constexpr int kStagedConsumerWarps = 8;
+constexpr int kStagedThreads = 32 * (kStagedConsumerWarps + 1);
+constexpr int kStagedMaxChunksHost = 32;
+// Dynamic shared memory of the staged kernel: header + nchunks staging chunks
+// (-1 if nchunks is out of range).
+int staged_smem_bytes(int chunk_bytes, int nchunks);
+
+// cudaLaunchKernelEx with an optional cluster shape.
+inline cudaError_t launch_ex(KernelFn kernel, const LaunchShape& s, cudaStream_t stream,
+                             const Params& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(s.grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(s.block), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(s.smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (s.cluster > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(s.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+// One-time kernel set-up: allow dynamic shared memory up to the per-block
+// opt-in limit `smem_optin` minus the kernel's static shared memory, and
+// clusters above the portable size of 8.
+inline cudaError_t prepare_kernel(KernelFn kernel, int smem_optin) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(kernel));
+    const int dyn_limit = smem_optin - static_cast<int>(fa.sharedSizeBytes);
+    if (e == cudaSuccess && dyn_limit > 48 * 1024)
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_limit);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel),
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+}
+
+// How many clusters of `cluster` CTAs can be resident at once (0 = cannot launch).
+inline cudaError_t max_active_clusters(KernelFn kernel, int block, int smem, int cluster,
+                                       int* clusters) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(block), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(clusters, kernel, &cfg);
+}
+
+}  // namespace rmsnorm

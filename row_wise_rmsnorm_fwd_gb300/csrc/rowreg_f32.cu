@@ -1,0 +1,6 @@
+// rowreg_f32.cu -- fp32 instances of the register-resident kernel.
+#include "rowreg_instances.cuh"
+
+namespace rmsnorm {
+KernelFn rowreg_kernel_f32(int vb, int nv) { return rowreg_pick<float>(vb, nv); }
+}  // namespace rmsnorm

@@ -1,0 +1,79 @@
+"""Helpers for the GPU parity tests: run the oracle on the same inputs and
+compare element by element within the stated tolerances.
+
+Tolerances (fixed by the accuracy targets of the work and derived from the
+arithmetic: fp32 sums of at most a few hundred terms per thread plus a
+butterfly/tree of at most 10 levels, rsqrtf (a few ulp), two products):
+  fp32: |y_gpu - y_ref| <= max(1e-5 * |y_ref|, 1e-6)
+  bf16: the GPU's bf16 bits are within 1 ulp of the oracle's single RNE
+        rounding of the binary64 result (+0 and -0 are equal).
+NaN in the reference must be NaN on the GPU and nowhere else.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from row_wise_rmsnorm_fwd_gb300 import workloads
+
+F32_RTOL = 1e-5
+F32_ATOL = 1e-6
+BF16_MAX_ULP = 1
+
+
+def oracle_for(x_cpu: torch.Tensor, w_cpu: torch.Tensor, eps: float):
+    """Oracle output for host tensors: float64 array (fp32) or uint16 bits (bf16)."""
+    if x_cpu.dtype == torch.float32:
+        return oracle.rmsnorm_f32(x_cpu.numpy(), w_cpu.numpy(), eps)
+    _, y16 = oracle.rmsnorm_bf16(workloads.bf16_bits(x_cpu), workloads.bf16_bits(w_cpu), eps)
+    return y16
+
+
+def check_f32(y_gpu: np.ndarray, y_ref: np.ndarray, what: str = ""):
+    y = y_gpu.astype(np.float64)
+    ref_nan = np.isnan(y_ref)
+    assert np.array_equal(np.isnan(y), ref_nan), f"{what}: NaN pattern differs"
+    ok = ~ref_nan
+    err = np.abs(y[ok] - y_ref[ok])
+    tol = np.maximum(F32_RTOL * np.abs(y_ref[ok]), F32_ATOL)
+    bad = err > tol
+    if bad.any():
+        i = np.flatnonzero(bad)[0]
+        raise AssertionError(
+            f"{what}: {bad.sum()} of {bad.size} elements out of tolerance; first at flat "
+            f"index {np.flatnonzero(ok)[i]}: gpu {y[ok][i]!r} ref {y_ref[ok][i]!r}")
+
+
+def _ordered(bits: np.ndarray) -> np.ndarray:
+    b = bits.astype(np.int32)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def _is_nan_bits(bits: np.ndarray) -> np.ndarray:
+    b = bits.astype(np.int32)
+    return ((b & 0x7F80) == 0x7F80) & ((b & 0x7F) != 0)
+
+
+def check_bf16(bits_gpu: np.ndarray, bits_ref: np.ndarray, what: str = ""):
+    nan_ref = _is_nan_bits(bits_ref)
+    assert np.array_equal(_is_nan_bits(bits_gpu), nan_ref), f"{what}: NaN pattern differs"
+    ok = ~nan_ref
+    d = np.abs(_ordered(bits_gpu[ok]) - _ordered(bits_ref[ok]))
+    bad = d > BF16_MAX_ULP
+    if bad.any():
+        i = np.flatnonzero(bad)[0]
+        raise AssertionError(
+            f"{what}: {bad.sum()} of {bad.size} bf16 values differ by more than "
+            f"{BF16_MAX_ULP} ulp; first: gpu 0x{int(bits_gpu[ok][i]):04x} "
+            f"ref 0x{int(bits_ref[ok][i]):04x} ({int(d[i])} ulp)")
+
+
+def compare(y_gpu: torch.Tensor, ref, what: str = ""):
+    """Compare a GPU result (any device) with the oracle's output for it."""
+    y = y_gpu.detach().cpu().contiguous()
+    if y.dtype == torch.float32:
+        check_f32(y.numpy(), ref, what)
+    else:
+        check_bf16(workloads.bf16_bits(y), ref, what)

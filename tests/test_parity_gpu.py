@@ -1,0 +1,282 @@
+"""GPU parity: librmsnorm's kernels against the fp64 CPU oracle, element by
+element, through the C ABI (ctypes binding).  Needs a GB300 (sm_103a)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from _parity import compare, oracle_for
+from row_wise_rmsnorm_fwd_gb300 import binding, build, workloads
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    build.build()
+    binding.load()
+    torch.cuda.init()
+    yield
+    torch.cuda.synchronize()
+    assert binding.rmsnorm_last_device_status() == binding.RMSNORM_OK
+
+
+def sms() -> int:
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def run(x, w, eps, y=None, **opts):
+    """One call through the C ABI; forced options go through rmsnorm_fwd_ex."""
+    if y is None:
+        y = torch.empty_like(x)
+    if opts:
+        binding.rmsnorm_fwd_ex(x, w, y, eps, options=opts)
+    elif x.dtype == torch.float32:
+        binding.rmsnorm_fwd_f32(x, w, y, eps)
+    else:
+        binding.rmsnorm_fwd_bf16(x, w, y, eps)
+    torch.cuda.synchronize()
+    return y
+
+
+def rand_case(rows, hidden, dtype, seed, xdist=("normal", 0.0, 1.0)):
+    x = workloads.make_random((rows, hidden), dtype, seed, xdist)
+    w = workloads.make_random((hidden,), dtype, seed + 1, ("normal", 1.0, 0.1))
+    return x, w
+
+
+def check_case(x_cpu, w_cpu, eps, what, **opts):
+    y = run(x_cpu.cuda(), w_cpu.cuda(), eps, **opts)
+    compare(y, oracle_for(x_cpu, w_cpu, eps), what)
+    return y
+
+
+# ------------------------------------------------------------- workloads --
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c2t", "c3", "c5b"])
+def test_workload_full(name):
+    wl = workloads.WORKLOADS[name]
+    x, w = workloads.make_x(wl), workloads.make_w(wl)
+    check_case(x, w, wl.eps, name)
+
+
+@pytest.mark.parametrize("name", ["c4", "c5a"])
+def test_workload_full_size_sampled_rows(name):
+    """Full-size workload in the bench's launch configuration (automatic
+    path, current stream); full rows sampled and checked against the oracle."""
+    wl = workloads.WORKLOADS[name]
+    x = workloads.make_x(wl, device="cuda")
+    w = workloads.make_w(wl, device="cuda")
+    y = run(x, w, wl.eps)
+    rows, hidden = wl.rows, wl.hidden
+    x2, y2 = x.view(rows, hidden), y.view(rows, hidden)
+    g = torch.Generator().manual_seed(5)
+    pick = torch.cat([torch.arange(64), torch.arange(rows - 64, rows),
+                      torch.randint(0, rows, (768,), generator=g)]).unique()
+    xs = x2[pick.cuda()].cpu()
+    ref = oracle_for(xs, w.cpu(), wl.eps)
+    compare(y2[pick.cuda()], ref, f"{name} sampled rows")
+    del x, y, x2, y2
+    torch.cuda.empty_cache()
+
+
+# ----------------------------------------------------------------- sweeps --
+
+WIDTHS = [1, 2, 3, 4, 7, 8, 31, 32, 33, 127, 128, 255, 256, 1000, 2047, 2048, 2049,
+          2050, 4095, 4096, 8191, 8192, 8193, 16384, 65536]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("hidden", WIDTHS)
+def test_width_sweep(dtype, hidden):
+    rows = 37 if hidden <= 8193 else 9
+    x, w = rand_case(rows, hidden, dtype, seed=hidden)
+    check_case(x, w, 1e-6, f"{dtype} H={hidden}")
+
+
+@pytest.mark.parametrize("dtype,hidden", [("f32", 4096), ("bf16", 8192), ("f32", 3584)])
+def test_row_sweep(dtype, hidden):
+    n = sms()
+    for rows in [1, 2, 7, 31, 32, 33, n - 1, n, n + 1, 4096]:
+        x, w = rand_case(rows, hidden, dtype, seed=rows)
+        check_case(x, w, 1e-5, f"{dtype} H={hidden} rows={rows}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,hidden", [(1, 262144), (8, 262144), (3, 100000), (2, 1 << 20)])
+def test_wide_rows(dtype, rows, hidden):
+    x, w = rand_case(rows, hidden, dtype, seed=rows + hidden, xdist=("normal", 0.0, 2.0))
+    check_case(x, w, 1e-6, f"{dtype} {rows}x{hidden}")
+
+
+# ----------------------------------------------------------- forced paths --
+
+FORCED = [
+    ("rowreg", {}), ("twopass", {}), ("staged", {}), ("staged", {"chunk_bytes": 4096}),
+    ("staged", {"cluster": 2}), ("staged", {"cluster": 4}),
+    ("cluster", {"cluster": 2}), ("cluster", {"cluster": 4}), ("cluster", {"cluster": 8}),
+    ("cluster", {"cluster": 16}),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("path,extra", FORCED, ids=lambda v: str(v))
+@pytest.mark.parametrize("rows,hidden", [(5, 4096), (300, 2048), (3, 16384), (2, 8200),
+                                         (40, 1000)])
+def test_forced_paths(dtype, path, extra, rows, hidden):
+    x, w = rand_case(rows, hidden, dtype, seed=7 * rows + hidden)
+    opts = dict(path=path, **extra)
+    try:
+        y = run(x.cuda(), w.cuda(), 1e-6, **opts)
+    except binding.RmsnormError as e:
+        if e.status == binding.RMSNORM_ERR_UNSUPPORTED:
+            pytest.skip(f"{path} {extra} cannot serve {rows}x{hidden}")
+        raise
+    compare(y, oracle_for(x, w, 1e-6), f"{path} {extra} {dtype} {rows}x{hidden}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_forced_launch_shapes(dtype):
+    """Grid and group sizes that leave some CTAs with no rows, or many."""
+    x, w = rand_case(333, 2048, dtype, seed=11)
+    ref = oracle_for(x, w, 1e-6)
+    xc, wc = x.cuda(), w.cuda()
+    for grid in (1, 3, 152, 1000):
+        compare(run(xc, wc, 1e-6, path="rowreg", grid=grid), ref, f"grid {grid}")
+    for threads in (64, 96, 128, 256, 512):
+        compare(run(xc, wc, 1e-6, path="rowreg", threads=threads), ref, f"G {threads}")
+    for vb in (4, 8, 16):
+        compare(run(xc, wc, 1e-6, path="rowreg", vec_bytes=vb), ref, f"vb {vb}")
+    compare(run(xc, wc, 1e-6, path="twopass", threads=96), ref, "twopass 96")
+
+
+# ----------------------------------------------------- layout edge cases --
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("offset", [1, 2, 3, 4, 5])
+def test_misaligned_pointers(dtype, offset):
+    """x, y and w at element offsets that rule out 16-byte (or any) vectors."""
+    rows, hidden = 19, 2050
+    x, w = rand_case(rows, hidden, dtype, seed=offset)
+    n = rows * hidden
+    xb = torch.zeros(n + 16, dtype=DT[dtype], device="cuda")
+    yb = torch.zeros(n + 16, dtype=DT[dtype], device="cuda")
+    wb = torch.zeros(hidden + 16, dtype=DT[dtype], device="cuda")
+    xv = xb[offset:offset + n].view(rows, hidden)
+    yv = yb[offset + 1:offset + 1 + n].view(rows, hidden)
+    wv = wb[offset + 2:offset + 2 + hidden]
+    xv.copy_(x)
+    wv.copy_(w)
+    run(xv, wv, 1e-6, y=yv)
+    compare(yv, oracle_for(x, w, 1e-6), f"offset {offset}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,hidden", [(64, 4096), (8, 65536), (4, 262144), (33, 1000)])
+def test_in_place(dtype, rows, hidden):
+    x, w = rand_case(rows, hidden, dtype, seed=99)
+    xc = x.cuda()
+    run(xc, w.cuda(), 1e-6, y=xc)
+    compare(xc, oracle_for(x, w, 1e-6), "in place")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("path", ["auto", "rowreg", "staged", "cluster", "twopass"])
+def test_guard_regions_untouched(dtype, path):
+    """Sentinels before and after y stay intact (no out-of-bounds stores)."""
+    rows, hidden = 21, 4104
+    x, w = rand_case(rows, hidden, dtype, seed=3)
+    guard = 4096
+    n = rows * hidden
+    sentinel = -12345.0
+    buf = torch.full((guard + n + guard,), sentinel, dtype=DT[dtype], device="cuda")
+    y = buf[guard:guard + n].view(rows, hidden)
+    opts = {} if path == "auto" else {"path": path}
+    try:
+        run(x.cuda(), w.cuda(), 1e-6, y=y, **opts)
+    except binding.RmsnormError as e:
+        if e.status == binding.RMSNORM_ERR_UNSUPPORTED:
+            pytest.skip("path cannot serve this shape")
+        raise
+    assert bool((buf[:guard] == sentinel).all()) and bool((buf[guard + n:] == sentinel).all())
+    compare(y, oracle_for(x, w, 1e-6), f"guarded {path}")
+
+
+# --------------------------------------------------- numerics edge cases --
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_special_rows(dtype):
+    """Zero rows, constant rows, NaN and Inf propagation, tiny and huge rows."""
+    hidden = 2048
+    x = workloads.make_random((8, hidden), "f32", 77)
+    x[0] = 0.0
+    x[1] = 0.5
+    x[2, 5] = float("nan")
+    x[3, 7] = float("inf")
+    x[4] *= 1e-20
+    x[5] *= 1e17   # large but inside the fp32 range of the squared sum
+    x[6, :] = -3.0
+    x = x.to(DT[dtype])
+    w = workloads.make_random((hidden,), dtype, 78, ("normal", 1.0, 0.1))
+    check_case(x, w, 1e-6, "special rows")
+    check_case(x[:2].contiguous(), w, 0.25, "special rows, large eps")
+
+
+def test_eps_zero_zero_row_is_nan():
+    x = torch.zeros(3, 512)
+    x[1] = 1.0
+    w = torch.ones(512)
+    y = run(x.cuda(), w.cuda(), 0.0).cpu()
+    assert torch.isnan(y[0]).all() and torch.isnan(y[2]).all()
+    assert torch.allclose(y[1], torch.ones(512))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("path", ["auto", "rowreg", "staged", "cluster", "twopass"])
+def test_deterministic(dtype, path):
+    x, w = rand_case(64, 8192, dtype, seed=123)
+    xc, wc = x.cuda(), w.cuda()
+    opts = {} if path == "auto" else {"path": path}
+    try:
+        a = run(xc, wc, 1e-6, **opts)
+    except binding.RmsnormError as e:
+        if e.status == binding.RMSNORM_ERR_UNSUPPORTED:
+            pytest.skip("path cannot serve this shape")
+        raise
+    for _ in range(3):
+        assert torch.equal(run(xc, wc, 1e-6, **opts), a)
+
+
+def test_non_default_stream():
+    x, w = rand_case(500, 4096, "f32", seed=1)
+    xc, wc = x.cuda(), w.cuda()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y = binding.rmsnorm_fwd_f32(xc, wc, eps=1e-6)
+    s.synchronize()
+    compare(y, oracle_for(x, w, 1e-6), "side stream")
+
+
+def test_plan_reports_families():
+    x = torch.empty(65536, 4096, device="cuda")
+    w = torch.empty(4096, device="cuda")
+    p = binding.rmsnorm_plan(x, w)
+    assert p["path_name"] == "rowreg" and p["vec_bytes"] == 16
+    xb = torch.empty(8, 262144, device="cuda", dtype=torch.bfloat16)
+    wb = torch.empty(262144, device="cuda", dtype=torch.bfloat16)
+    p = binding.rmsnorm_plan(xb, wb)
+    assert p["cluster"] > 1
+
+
+def test_unsupported_forced_option_launches_nothing():
+    x = torch.ones(4, 2050, device="cuda")   # 8200-byte rows: no 16-byte pitch
+    w = torch.ones(2050, device="cuda")
+    y = torch.full_like(x, 7.0)
+    with pytest.raises(binding.RmsnormError) as ei:
+        binding.rmsnorm_fwd_ex(x, w, y, 1e-6, options={"path": "staged"})
+    assert ei.value.status == binding.RMSNORM_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert bool((y == 7.0).all())
