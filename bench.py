@@ -43,37 +43,40 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources; a profile's traffic figure is valid only for
-    the sources it was captured from."""
+def kernel_source_hash(files=None) -> str:
+    """Hash of CUDA sources (all of csrc/, or the named files); a profile's
+    traffic figure is valid only for the sources it was captured from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_wise_rmsnorm_fwd_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    names = sorted(files) if files else sorted(
+        n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h")))
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary of this workload
-    (profiles/*_<workload>.txt, lines 'traffic_bytes_per_launch:' and
-    'kernel_source_hash:'); None if absent or taken from other sources."""
-    pdir = os.path.join(ROOT, "profiles")
-    if not os.path.isdir(pdir):
+def profiled_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary profiles/<kernel>_<workload>.txt (lines 'traffic_bytes_per_launch:',
+    'kernel_source_files:' and 'kernel_source_hash:'); None if there is none or
+    if those sources have changed since the capture."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
-    for name in sorted(os.listdir(pdir)):
-        if not name.endswith(f"_{workload}.txt"):
-            continue
-        fields = {}
-        with open(os.path.join(pdir, name)) as f:
-            for line in f:
-                if ":" in line:
-                    k, v = line.split(":", 1)
-                    fields[k.strip()] = v.strip()
-        if fields.get("kernel_source_hash") == want and "traffic_bytes_per_launch" in fields:
-            return int(float(fields["traffic_bytes_per_launch"]))
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith(" "):
+                k, v = line.split(":", 1)
+                fields.setdefault(k.strip(), v.strip())
+    files = fields.get("kernel_source_files", "").split()
+    try:
+        ok = fields.get("kernel_source_hash") == kernel_source_hash(files or None)
+    except OSError:
+        ok = False
+    if ok and "traffic_bytes_per_launch" in fields:
+        return int(float(fields["traffic_bytes_per_launch"].split()[0]))
     return None
 
 
@@ -217,8 +220,16 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
-def config_block(wl, world):
-    return {
+def forced(args) -> bool:
+    return bool(args.path != "auto" or args.cluster or args.grid or args.threads or args.chunk)
+
+
+def config_block(wl, world, args=None):
+    extra = {}
+    if args is not None and forced(args):
+        extra["forced"] = {"path": args.path, "cluster": args.cluster, "grid": args.grid,
+                           "threads": args.threads, "chunk_bytes": args.chunk}
+    return {**extra,
         "workload": f"{wl.name}: {wl.description}",
         "shape": list(wl.shape), "io_dtype": wl.dtype, "eps": wl.eps,
         "bytes_per_step_per_gpu": wl.bytes_per_call,
@@ -251,8 +262,17 @@ def run_ours(args, wl):
     rows, hidden = wl.rows, wl.hidden
     stream = torch.cuda.current_stream()
     handle = stream.cuda_stream
-    fwd = binding.raw.rmsnorm_fwd_bf16 if wl.dtype == "bf16" else binding.raw.rmsnorm_fwd_f32
-    plan = binding.rmsnorm_plan(x, w, y)
+    options = None
+    if forced(args):
+        options = binding.make_options(path=args.path, cluster=args.cluster, grid=args.grid,
+                                       threads=args.threads, chunk_bytes=args.chunk)
+        dt_code = binding.RMSNORM_DTYPE_BF16 if wl.dtype == "bf16" else binding.RMSNORM_DTYPE_F32
+
+        def fwd(xp, wp, yp, r, h, eps, s):
+            return binding.raw.rmsnorm_fwd_ex(dt_code, xp, wp, yp, r, h, eps, options, s)
+    else:
+        fwd = binding.raw.rmsnorm_fwd_bf16 if wl.dtype == "bf16" else binding.raw.rmsnorm_fwd_f32
+    plan = binding.rmsnorm_plan(x, w, y, options=options)
     flush = None
     if wl.bytes_per_call <= 4 * 129e6:
         flush = torch.empty(int(2 * 129e6) // 4 + 1024, dtype=torch.float32, device=dev)
@@ -308,7 +328,7 @@ def run_ours(args, wl):
     avg_launch_s = (sum(per_launch_ms) / len(per_launch_ms)) / 1e3
     achieved = bytes_step / avg_launch_s / 1e9
     per_launch_sorted = sorted(per_launch_ms)
-    traffic = profiled_traffic(wl.name)
+    traffic = profiled_traffic(wl.name, plan["kernel"])
 
     e2e = None
     if not args.no_e2e:
@@ -326,7 +346,7 @@ def run_ours(args, wl):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic", "config": config_block(wl, world),
+            "dtype": "f32", "data": "synthetic", "config": config_block(wl, world, args),
             "rows_per_s": rows_per_s,
             "kernel": {"name": plan["kernel"], "path": plan["path_name"],
                        "grid": plan["grid"], "block": plan["block_threads"],
@@ -418,17 +438,31 @@ def measure_e2e(args, wl, x_dev, w_dev, y_dev, fwd, binding, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="c5a")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--rows", type=int, default=0,
+                    help="use only this many rows of the workload (small profiling cases)")
+    ap.add_argument("--path", default="auto",
+                    choices=["auto", "rowreg", "staged", "cluster", "twopass"],
+                    help="force a kernel family through rmsnorm_fwd_ex (evidence runs)")
+    ap.add_argument("--cluster", type=int, default=0)
+    ap.add_argument("--grid", type=int, default=0, help="force the CTA count")
+    ap.add_argument("--threads", type=int, default=0, help="force threads per row group")
+    ap.add_argument("--chunk", type=int, default=0, help="staged path: bytes per bulk copy")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    import dataclasses
     from row_wise_rmsnorm_fwd_gb300 import workloads
     wl = workloads.WORKLOADS[args.workload]
+    if args.rows:
+        wl = dataclasses.replace(wl, name=f"{wl.name}_rows{args.rows}",
+                                 shape=(args.rows, wl.hidden),
+                                 description=f"first {args.rows} rows of {wl.description}")
     if args.impl == "reference":
         run_reference(args, wl)
     else:

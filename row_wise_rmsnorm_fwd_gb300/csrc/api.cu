@@ -37,6 +37,7 @@ cudaError_t note(cudaError_t e) {
     return e;
 }
 constexpr int kMaxDevices = 64;
+constexpr int kRowregWaves = 4;   // row-block CTAs per resident CTA slot
 
 struct DeviceInfo {
     std::once_flag once;
@@ -206,10 +207,13 @@ rmsnorm_status_t plan_rowreg(const Call& c, int cluster, Plan* P) {
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
     int grid;
     if (cluster == 1) {
+        // Grid-stride over row blocks with about four waves of resident CTAs:
+        // measured on GB300 to keep HBM busier than exactly one resident wave
+        // (CTAs fall out of phase, so loads, reductions and stores overlap).
         const int64_t nblocks = (c.rows + rpc - 1) / rpc;
-        const int64_t resident = static_cast<int64_t>(c.info->sms) * occ;
+        const int64_t target = static_cast<int64_t>(c.info->sms) * occ * kRowregWaves;
         grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
-                                               : (nblocks < resident ? nblocks : resident));
+                                               : (nblocks < target ? nblocks : target));
     } else {
         const int64_t nclusters = c.opt.grid > 0 ? (c.opt.grid + cluster - 1) / cluster
                                                  : (c.rows < occ ? c.rows : occ);

@@ -63,12 +63,52 @@ template <typename T, int VB> struct VecTraits {
     static constexpr int kElems = VB / Elem<T>::kBytes;
 };
 
-// Streaming (evict-first) global load of one vector.
-template <int VB>
+// Load-policy codes for the streamed input x (read exactly once):
+//   0  ld.global.cs                                  (cache-streaming)
+//   1  ld.global.nc.L1::no_allocate.L2::256B         (no L1 line, 256-B L2 prefetch)
+//   2  ld.global.nc.L1::no_allocate                  (no L1 line)
+//   3  ld.global.L1::no_allocate.L2::cache_hint      (L2 evict-first policy)
+// Store-policy codes for y (written exactly once):
+//   0  st.global.cs    1  st.global    2  st.global.L1::no_allocate
+template <int LD>
+__device__ __forceinline__ uint4 ld_v4(const void* p) {
+    uint4 t;
+    if constexpr (LD == 0) {
+        t = __ldcs(reinterpret_cast<const uint4*>(p));
+    } else if constexpr (LD == 1) {
+        asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(t.x), "=r"(t.y), "=r"(t.z), "=r"(t.w) : "l"(p));
+    } else if constexpr (LD == 2) {
+        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(t.x), "=r"(t.y), "=r"(t.z), "=r"(t.w) : "l"(p));
+    } else {
+        uint64_t pol;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+        asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                     : "=r"(t.x), "=r"(t.y), "=r"(t.z), "=r"(t.w) : "l"(p), "l"(pol));
+    }
+    return t;
+}
+
+template <int ST>
+__device__ __forceinline__ void st_v4(void* p, uint4 t) {
+    if constexpr (ST == 0) {
+        __stcs(reinterpret_cast<uint4*>(p), t);
+    } else if constexpr (ST == 1) {
+        asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                     :: "l"(p), "r"(t.x), "r"(t.y), "r"(t.z), "r"(t.w) : "memory");
+    } else {
+        asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};"
+                     :: "l"(p), "r"(t.x), "r"(t.y), "r"(t.z), "r"(t.w) : "memory");
+    }
+}
+
+// Streaming global load of one vector (x is read exactly once).
+template <int VB, int LD = 0>
 __device__ __forceinline__ Vec<VB> ld_stream(const void* p) {
     Vec<VB> v;
     if constexpr (VB == 16) {
-        uint4 t = __ldcs(reinterpret_cast<const uint4*>(p));
+        uint4 t = ld_v4<LD>(p);
         v.u[0] = t.x; v.u[1] = t.y; v.u[2] = t.z; v.u[3] = t.w;
     } else if constexpr (VB == 8) {
         uint2 t = __ldcs(reinterpret_cast<const uint2*>(p));
@@ -117,11 +157,11 @@ __device__ __forceinline__ Vec<VB> ld_ro(const void* p) {
     return v;
 }
 
-// Streaming global store of one vector.
-template <int VB>
+// Streaming global store of one vector (y is written exactly once).
+template <int VB, int ST = 0>
 __device__ __forceinline__ void st_stream(void* p, const Vec<VB>& v) {
     if constexpr (VB == 16) {
-        __stcs(reinterpret_cast<uint4*>(p), make_uint4(v.u[0], v.u[1], v.u[2], v.u[3]));
+        st_v4<ST>(p, make_uint4(v.u[0], v.u[1], v.u[2], v.u[3]));
     } else if constexpr (VB == 8) {
         __stcs(reinterpret_cast<uint2*>(p), make_uint2(v.u[0], v.u[1]));
     } else if constexpr (VB == 4) {
@@ -130,6 +170,10 @@ __device__ __forceinline__ void st_stream(void* p, const Vec<VB>& v) {
         __stcs(reinterpret_cast<unsigned short*>(p), v.h);
     }
 }
+
+// Keep a value opaque to the optimiser inside a loop (it is then neither
+// hoisted nor re-expanded outside): used to keep packed bf16 weights packed.
+__device__ __forceinline__ void opaque(uint32_t& r) { asm volatile("" : "+r"(r)); }
 
 // Element k of a vector, widened exactly to fp32.
 template <typename T, int VB>

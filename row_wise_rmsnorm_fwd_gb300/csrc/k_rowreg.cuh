@@ -21,6 +21,10 @@
 // Rows are scheduled persistently: a CTA (or a cluster, for split rows) walks
 // row blocks with a grid-wide stride, and the next row's loads are issued
 // before the current row's reduction (register double buffer, PF).
+//
+// Compile-time choices: PF (register prefetch of the next row), WREG (weights
+// held in registers across rows, packed; otherwise re-read from L1 per row),
+// LD / ST (cache policies of the x loads and y stores, see common.cuh).
 #pragma once
 #include "common.cuh"
 
@@ -29,7 +33,7 @@ namespace rmsnorm {
 template <int NV>
 constexpr int rowreg_max_threads() { return NV >= 4 ? 512 : 1024; }
 
-template <typename T, int VB, int NV, bool PF>
+template <typename T, int VB, int NV, bool PF, bool WREG, int LD, int ST>
 __global__ void __launch_bounds__(rowreg_max_threads<NV>())
 rowreg_kernel(const Params p) {
     constexpr int EPV = VecTraits<T, VB>::kElems;
@@ -72,9 +76,11 @@ rowreg_kernel(const Params p) {
     const int64_t row_bytes = static_cast<int64_t>(p.hidden) * sizeof(T);
 
     Vec<VB> wv[NV];
+    if (WREG) {
 #pragma unroll
-    for (int i = 0; i < NV; ++i)
-        if (valid[i]) wv[i] = ld_ro<VB>(wb + static_cast<int64_t>(vidx[i]) * VB);
+        for (int i = 0; i < NV; ++i)
+            if (valid[i]) wv[i] = ld_ro<VB>(wb + static_cast<int64_t>(vidx[i]) * VB);
+    }
 
     const int RPC = p.rows_per_cta;
     const int64_t nblocks = (p.rows + RPC - 1) / RPC;
@@ -86,7 +92,8 @@ rowreg_kernel(const Params p) {
             const char* src = xb + row * row_bytes;
 #pragma unroll
             for (int i = 0; i < NV; ++i)
-                if (valid[i]) dst[i] = ld_stream<VB>(src + static_cast<int64_t>(vidx[i]) * VB);
+                if (valid[i])
+                    dst[i] = ld_stream<VB, LD>(src + static_cast<int64_t>(vidx[i]) * VB);
         }
     };
 
@@ -138,11 +145,22 @@ rowreg_kernel(const Params p) {
 #pragma unroll
             for (int i = 0; i < NV; ++i) {
                 if (valid[i]) {
+                    Vec<VB> wi;
+                    if (WREG) {
+                        wi = wv[i];
+                        if constexpr (sizeof(T) == 2 && VB >= 4) {
+#pragma unroll
+                            for (int k = 0; k < VB / 4; ++k) opaque(wi.u[k]);
+                        }
+                    } else {
+                        wi = ld_ro<VB>(wb + static_cast<int64_t>(vidx[i]) * VB);
+                    }
                     float o[EPV];
 #pragma unroll
                     for (int k = 0; k < EPV; ++k)
-                        o[k] = (get<T, VB>(cur[i], k) * rstd) * get<T, VB>(wv[i], k);
-                    st_stream<VB>(dst + static_cast<int64_t>(vidx[i]) * VB, pack<T, VB>(o));
+                        o[k] = (get<T, VB>(cur[i], k) * rstd) * get<T, VB>(wi, k);
+                    st_stream<VB, ST>(dst + static_cast<int64_t>(vidx[i]) * VB,
+                                      pack<T, VB>(o));
                 }
             }
         }

@@ -20,7 +20,13 @@ c3         (4, 512, 3584)           f32    N(0,1), 36 outlier columns x50     1e
 c4         (65536, 4096)            f32    N(0,1)            U(0.5,1.5)       1e-6
 c5a        (262144, 8192)           bf16   N(0,2) (std 2)    N(1,0.1)         1e-6
 c5b        (8, 262144)              bf16   N(0,2)            N(1,0.1)         1e-6
+w32k       (8192, 32768)            f32    N(0,1)            N(1,0.1)         1e-6
+w64k       (16384, 65536)           bf16   N(0,2)            N(1,0.1)         1e-6
 =========  =======================  =====  ================  ===============  ======
+
+c1..c5b are the measured workloads; w32k and w64k are extra wide-row cases
+(128 KiB rows, too wide to hold in one CTA's registers) used to measure the
+shared-memory staged and cluster kernels on HBM-sized inputs.
 
 Readings: "N(0,2)" is mean 0, standard deviation 2; the Qwen-shaped case's
 "1% outlier channels" are round(0.01*3584) = 36 whole columns, picked by a
@@ -98,6 +104,12 @@ WORKLOADS = {
         Workload("c5b", 4, (8, 262144), "bf16", ("normal", 0.0, 2.0),
                  ("normal", 1.0, 0.1), 1e-6,
                  description="few rows, wide bf16 (8,262144)"),
+        Workload("w32k", 5, (8192, 32768), "f32", ("normal", 0.0, 1.0),
+                 ("normal", 1.0, 0.1), 1e-6,
+                 description="wide fp32 rows (8192,32768), 128 KiB per row"),
+        Workload("w64k", 6, (16384, 65536), "bf16", ("normal", 0.0, 2.0),
+                 ("normal", 1.0, 0.1), 1e-6,
+                 description="wide bf16 rows (16384,65536), 128 KiB per row"),
     ]
 }
 
