@@ -75,10 +75,22 @@ typedef enum {
 typedef struct {
     int32_t path;            /* rmsnorm_path_t */
     int32_t cluster;         /* CTAs per row for CLUSTER (2..16) or STAGED (1..16) */
-    int32_t threads;         /* threads per row group (multiple of 32, <= 1024) */
+    int32_t threads;         /* threads per row group (multiple of 32, <= 1024);
+                                STAGED: consumer threads, 128 or 256 */
     int32_t grid;            /* CTAs to launch (rounded to the cluster size) */
     int32_t vec_bytes;       /* 16, 8, 4 or 2 (bf16 only); must suit the alignment */
     int32_t chunk_bytes;     /* STAGED: bytes per bulk copy (multiple of 16) */
+    int32_t stages;          /* STAGED: chunk slots in the shared-memory ring (>= chunks per
+                                row slice, <= 32) */
+    int32_t weights;         /* STAGED: 1 = weight slice copied to shared memory once,
+                                2 = weights read through L1/L2 every row */
+    int32_t fault_inject;    /* failure-detection tests only: 1 = the staged kernel's
+                                producer withholds its first copy, 2 = one CTA of a
+                                split-row cluster withholds its partial sum.  Honoured
+                                only by the test build of the library (compiled with
+                                RMSNORM_FAULT_INJECT); the product library returns
+                                RMSNORM_ERR_UNSUPPORTED for any non-zero value. */
+    int32_t reserved;        /* must be 0 */
     uint64_t wait_timeout_ns;/* limit of every device-side wait; 0 = 2 seconds */
 } rmsnorm_options_t;
 
@@ -94,6 +106,8 @@ typedef struct {
     int32_t vecs_per_thread; /* register-resident vectors per thread and row */
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t chunk_bytes;     /* STAGED: bytes per bulk copy */
+    int32_t stages;          /* STAGED: chunk slots in the ring */
+    int32_t weights_staged;  /* STAGED: 1 if the weight slice is held in shared memory */
     char kernel[48];         /* kernel family name, for profiles */
 } rmsnorm_plan_t;
 
@@ -159,6 +173,10 @@ const char* rmsnorm_status_string(rmsnorm_status_t status);
  * RMSNORM_ERR_CUDA is explained.
  */
 int32_t rmsnorm_last_cuda_error(char* msg, size_t len);
+
+/* 1 in the test build of the library that honours rmsnorm_options_t.fault_inject
+ * (compiled with RMSNORM_FAULT_INJECT), 0 in the product library. */
+int32_t rmsnorm_fault_injection_enabled(void);
 
 /* ABI version of this header: major*10000 + minor*100 + patch. */
 int32_t rmsnorm_abi_version(void);

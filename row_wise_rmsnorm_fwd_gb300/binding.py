@@ -36,6 +36,8 @@ class rmsnorm_options_t(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("vec_bytes", ctypes.c_int32), ("chunk_bytes", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("weights", ctypes.c_int32),
+                ("fault_inject", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("wait_timeout_ns", ctypes.c_uint64)]
 
 
@@ -45,6 +47,7 @@ class rmsnorm_plan_t(ctypes.Structure):
                 ("rows_per_cta", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("vec_bytes", ctypes.c_int32), ("vecs_per_thread", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("chunk_bytes", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("weights_staged", ctypes.c_int32),
                 ("kernel", ctypes.c_char * 48)]
 
 
@@ -66,40 +69,45 @@ def library_path() -> str:
     return _build.LIB_PATH
 
 
+def open_library(path: str):
+    """dlopen a build of librmsnorm at `path` and declare its C signatures."""
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with row_wise_rmsnorm_fwd_gb300.build.build() "
+            "(there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    for name in ("rmsnorm_fwd_f32", "rmsnorm_fwd_bf16"):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, vp, vp, i64, i64, f32, vp]
+        fn.restype = ctypes.c_int
+    lib.rmsnorm_fwd_ex.argtypes = [i32, vp, vp, vp, i64, i64, f32,
+                                   ctypes.POINTER(rmsnorm_options_t), vp]
+    lib.rmsnorm_fwd_ex.restype = ctypes.c_int
+    lib.rmsnorm_plan.argtypes = [i32, vp, vp, vp, i64, i64,
+                                 ctypes.POINTER(rmsnorm_options_t),
+                                 ctypes.POINTER(rmsnorm_plan_t)]
+    lib.rmsnorm_plan.restype = ctypes.c_int
+    lib.rmsnorm_last_device_status.argtypes = [vp]
+    lib.rmsnorm_last_device_status.restype = ctypes.c_int
+    lib.rmsnorm_status_string.argtypes = [ctypes.c_int]
+    lib.rmsnorm_status_string.restype = ctypes.c_char_p
+    lib.rmsnorm_last_cuda_error.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
+    lib.rmsnorm_last_cuda_error.restype = ctypes.c_int32
+    lib.rmsnorm_fault_injection_enabled.argtypes = []
+    lib.rmsnorm_fault_injection_enabled.restype = ctypes.c_int32
+    lib.rmsnorm_abi_version.argtypes = []
+    lib.rmsnorm_abi_version.restype = ctypes.c_int32
+    return lib
+
+
 def load():
     """Load librmsnorm.so (built in-tree by ``build.build()``)."""
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        path = library_path()
-        if not os.path.exists(path):
-            raise RuntimeError(
-                f"{path} is missing: build it with row_wise_rmsnorm_fwd_gb300.build.build() "
-                "(there is no CPU fallback)")
-        lib = ctypes.CDLL(path)
-        vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
-        for name in ("rmsnorm_fwd_f32", "rmsnorm_fwd_bf16"):
-            fn = getattr(lib, name)
-            fn.argtypes = [vp, vp, vp, i64, i64, f32, vp]
-            fn.restype = ctypes.c_int
-        lib.rmsnorm_fwd_ex.argtypes = [i32, vp, vp, vp, i64, i64, f32,
-                                       ctypes.POINTER(rmsnorm_options_t), vp]
-        lib.rmsnorm_fwd_ex.restype = ctypes.c_int
-        lib.rmsnorm_plan.argtypes = [i32, vp, vp, vp, i64, i64,
-                                     ctypes.POINTER(rmsnorm_options_t),
-                                     ctypes.POINTER(rmsnorm_plan_t)]
-        lib.rmsnorm_plan.restype = ctypes.c_int
-        lib.rmsnorm_last_device_status.argtypes = [vp]
-        lib.rmsnorm_last_device_status.restype = ctypes.c_int
-        lib.rmsnorm_status_string.argtypes = [ctypes.c_int]
-        lib.rmsnorm_status_string.restype = ctypes.c_char_p
-        lib.rmsnorm_last_cuda_error.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
-        lib.rmsnorm_last_cuda_error.restype = ctypes.c_int32
-        lib.rmsnorm_abi_version.argtypes = []
-        lib.rmsnorm_abi_version.restype = ctypes.c_int32
-        _lib = lib
-        return lib
+        if _lib is None:
+            _lib = open_library(library_path())
+        return _lib
 
 
 def declared_functions() -> list[str]:
@@ -118,12 +126,19 @@ def declared_functions() -> list[str]:
     return names
 
 
+WEIGHTS = {"auto": 0, "smem": 1, "l2": 2}
+
+
 def make_options(path="auto", cluster=0, threads=0, grid=0, vec_bytes=0,
-                 chunk_bytes=0, wait_timeout_ns=0) -> rmsnorm_options_t:
+                 chunk_bytes=0, stages=0, weights=0, wait_timeout_ns=0,
+                 fault_inject=0) -> rmsnorm_options_t:
     o = rmsnorm_options_t()
     o.path = PATHS[path] if isinstance(path, str) else int(path)
     o.cluster, o.threads, o.grid = int(cluster), int(threads), int(grid)
     o.vec_bytes, o.chunk_bytes = int(vec_bytes), int(chunk_bytes)
+    o.stages = int(stages)
+    o.weights = WEIGHTS[weights] if isinstance(weights, str) else int(weights)
+    o.fault_inject = int(fault_inject)
     o.wait_timeout_ns = int(wait_timeout_ns)
     return o
 

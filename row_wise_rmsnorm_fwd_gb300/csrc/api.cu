@@ -19,8 +19,8 @@ __device__ unsigned g_rmsnorm_status = 0u;
 
 namespace rmsnorm {
 
-KernelFn rowreg_kernel_ptr(int dtype, int vb, int nv) {
-    return dtype == 0 ? rowreg_kernel_f32(vb, nv) : rowreg_kernel_bf16(vb, nv);
+KernelFn rowreg_kernel_ptr(int dtype, int vb, int nv, bool pf) {
+    return dtype == 0 ? rowreg_kernel_f32(vb, nv, pf) : rowreg_kernel_bf16(vb, nv, pf);
 }
 int rowreg_max_block(int nv) { return nv >= 4 ? 512 : 1024; }
 
@@ -38,6 +38,11 @@ cudaError_t note(cudaError_t e) {
 }
 constexpr int kMaxDevices = 64;
 constexpr int kRowregWaves = 4;   // row-block CTAs per resident CTA slot
+constexpr int64_t kStagedChunk = 16384;   // bytes per bulk copy
+constexpr int64_t kStagedLookahead = 6;   // ring slots beyond one row slice
+constexpr int kStagedConsumerWarps = 8;   // default consumer warps per CTA
+constexpr int64_t kRowregMaxRowBytes = 32768;   // auto: register-resident up to here
+constexpr int64_t kStagedMaxRowBytes = 65536;   // auto: fp32 staged up to here
 
 struct DeviceInfo {
     std::once_flag once;
@@ -136,6 +141,8 @@ struct Plan {
     int smem = 0;
     int chunk = 0;
     int nchunks = 0;
+    int nslots = 0;
+    int w_staged = 0;
     int nvec = 0;
     int slice_vecs = 0;
     KernelFn fn = nullptr;
@@ -197,7 +204,7 @@ rmsnorm_status_t plan_rowreg(const Call& c, int cluster, Plan* P) {
         G = static_cast<int>(g);
     }
     if (G > rowreg_max_block(NV)) return RMSNORM_ERR_UNSUPPORTED;
-    KernelFn fn = rowreg_kernel_ptr(c.dtype, vb, NV);
+    KernelFn fn = rowreg_kernel_ptr(c.dtype, vb, NV, cluster > 1);
     if (!fn) return RMSNORM_ERR_UNSUPPORTED;
     const int rpc = cluster == 1 ? (G >= 256 ? 1 : 256 / G) : 1;
     const int block = G * rpc;
@@ -236,6 +243,9 @@ rmsnorm_status_t plan_rowreg(const Call& c, int cluster, Plan* P) {
 }
 
 // Bulk-copy staged kernel; needs 16-byte aligned pointers and row pitch.
+// Geometry: chunks of at most 16 KB, a ring of chunks-per-slice + 6 slots
+// (about 96 KB of copies in flight beyond the row being consumed), and the
+// weight slice in shared memory when that still fits next to the ring.
 rmsnorm_status_t plan_staged(const Call& c, int cluster, Plan* P) {
     if (c.opt.vec_bytes != 0 && c.opt.vec_bytes != 16) return RMSNORM_ERR_UNSUPPORTED;
     if (widest_vb(c) != 16) return RMSNORM_ERR_UNSUPPORTED;
@@ -243,24 +253,55 @@ rmsnorm_status_t plan_staged(const Call& c, int cluster, Plan* P) {
     const int64_t vecs = row_bytes / 16;
     const int64_t slice_vecs = (vecs + cluster - 1) / cluster;
     const int64_t slice_bytes = slice_vecs * 16;
+    const int64_t budget = c.info->smem_optin;
+    if (slice_bytes + kStagedHeaderHost > budget) return RMSNORM_ERR_UNSUPPORTED;
     int64_t chunk = c.opt.chunk_bytes;
     if (chunk != 0) {
         if (chunk % 16 != 0 || chunk <= 0) return RMSNORM_ERR_INVALID_ARG;
     } else {
-        chunk = slice_bytes < 16384 ? slice_bytes : 16384;
+        chunk = slice_bytes < kStagedChunk ? slice_bytes : kStagedChunk;
     }
     int64_t nchunks = (slice_bytes + chunk - 1) / chunk;
-    if (nchunks > kStagedMaxChunksHost) {
+    if (nchunks > kStagedMaxSlotsHost) {
         if (c.opt.chunk_bytes != 0) return RMSNORM_ERR_UNSUPPORTED;
-        chunk = round_up((slice_bytes + kStagedMaxChunksHost - 1) / kStagedMaxChunksHost, 16);
+        chunk = round_up((slice_bytes + kStagedMaxSlotsHost - 1) / kStagedMaxSlotsHost, 16);
         nchunks = (slice_bytes + chunk - 1) / chunk;
     }
-    if (chunk * nchunks > c.info->smem_optin) return RMSNORM_ERR_UNSUPPORTED;
-    const int64_t smem = staged_smem_bytes(static_cast<int>(chunk), static_cast<int>(nchunks));
-    if (smem <= 0 || smem > c.info->smem_optin) return RMSNORM_ERR_UNSUPPORTED;
-    KernelFn fn = staged_kernel_ptr(c.dtype);
+    // Ring slots: forced, or chunks per slice + lookahead, within the budget.
+    const int wmode = c.opt.weights;
+    if (wmode < 0 || wmode > 2 || c.opt.stages < 0) return RMSNORM_ERR_INVALID_ARG;
+    auto fits = [&](int64_t slots, int64_t wbytes) {
+        return kStagedHeaderHost + wbytes + slots * chunk <= budget;
+    };
+    int64_t want = c.opt.stages > 0 ? c.opt.stages : nchunks + kStagedLookahead;
+    if (want > kStagedMaxSlotsHost) want = kStagedMaxSlotsHost;
+    if (want < nchunks) return RMSNORM_ERR_UNSUPPORTED;
+    bool wstaged;
+    if (wmode == 1) {
+        wstaged = true;
+    } else if (wmode == 2) {
+        wstaged = false;
+    } else {
+        wstaged = fits(want, slice_bytes);
+    }
+    const int64_t wres = wstaged ? slice_bytes : 0;
+    int64_t slots = want;
+    while (slots > nchunks && !fits(slots, wres)) --slots;
+    if (!fits(slots, wres)) return RMSNORM_ERR_UNSUPPORTED;
+    if (c.opt.stages > 0 && slots != c.opt.stages) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t smem = staged_smem_bytes(chunk, static_cast<int>(slots), wres);
+    if (smem <= 0 || smem > budget) return RMSNORM_ERR_UNSUPPORTED;
+    // Consumer warps: forced through `threads` (128 or 256), else 8.
+    int ncw = kStagedConsumerWarps;
+    if (c.opt.threads != 0) {
+        if (c.opt.threads != 128 && c.opt.threads != 256) return RMSNORM_ERR_UNSUPPORTED;
+        ncw = c.opt.threads / 32;
+    }
+    const int block = 32 * (ncw + 1);
+    KernelFn fn = staged_kernel_ptr(c.dtype, ncw);
+    if (!fn) return RMSNORM_ERR_UNSUPPORTED;
     int occ = 0;
-    if (cached_occupancy(c.dev, fn, kStagedThreads, static_cast<int>(smem), cluster, &occ) !=
+    if (cached_occupancy(c.dev, fn, block, static_cast<int>(smem), cluster, &occ) !=
         cudaSuccess)
         return RMSNORM_ERR_CUDA;
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
@@ -276,8 +317,8 @@ rmsnorm_status_t plan_staged(const Call& c, int cluster, Plan* P) {
     }
     P->path = RMSNORM_PATH_STAGED;
     P->cluster = cluster;
-    P->group = 32 * kStagedConsumerWarps;
-    P->block = kStagedThreads;
+    P->group = 32 * ncw;
+    P->block = block;
     P->rpc = 1;
     P->grid = grid;
     P->vb = 16;
@@ -285,6 +326,8 @@ rmsnorm_status_t plan_staged(const Call& c, int cluster, Plan* P) {
     P->smem = static_cast<int>(smem);
     P->chunk = static_cast<int>(chunk);
     P->nchunks = static_cast<int>(nchunks);
+    P->nslots = static_cast<int>(slots);
+    P->w_staged = wstaged ? 1 : 0;
     P->nvec = static_cast<int>(vecs);
     P->slice_vecs = static_cast<int>(slice_vecs);
     P->fn = fn;
@@ -324,26 +367,38 @@ rmsnorm_status_t plan_twopass(const Call& c, Plan* P) {
     return RMSNORM_OK;
 }
 
-// The launch heuristics.  Enough rows to give every SM a row: one CTA (or a
-// warp) per row.  Few rows: split each row over a cluster so that about one
-// CTA per SM works, keeping slices of at least 4 KB.  Rows too wide for one
-// CTA's registers go to the staged kernel, then to wider clusters, and
-// finally to the two-pass kernel.
+// The launch heuristics, from measurements on GB300 (profiles/kernel_choices.md):
+//  - few rows (fewer than SMs): split each row over a cluster so that about one
+//    CTA per SM works, keeping slices of at least 4 KB;
+//  - rows up to 32 KB: register-resident, one CTA (or warp) per row (93-101% of
+//    the measured HBM copy peak);
+//  - fp32 rows up to 64 KB: shared-memory staged by bulk copies (96%);
+//  - wider rows (and bf16 rows above 32 KB): two-pass, the second read served
+//    by L2 (81-95%).
+// Each choice falls through to the next family if it cannot serve the call.
 rmsnorm_status_t plan_auto(const Call& c, Plan* P) {
     const int64_t row_bytes = c.hidden * c.sz;
-    int want = 1;
+    rmsnorm_status_t st;
     if (c.rows < c.info->sms) {
-        want = pow2_floor(c.info->sms / (c.rows > 0 ? c.rows : 1));
+        int want = pow2_floor(c.info->sms / (c.rows > 0 ? c.rows : 1));
         if (want > 16) want = 16;
         while (want > 1 && row_bytes / want < 4096) want >>= 1;
+        for (int cl = want; cl <= 16; cl <<= 1) {
+            st = plan_rowreg(c, cl, P);
+            if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+        }
+        for (int cl = want; cl <= 16; cl <<= 1) {
+            st = plan_staged(c, cl, P);
+            if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+        }
+        return plan_twopass(c, P);
     }
-    rmsnorm_status_t st;
-    for (int cl = want; cl <= 16; cl <<= 1) {
-        st = plan_rowreg(c, cl, P);
+    if (row_bytes <= kRowregMaxRowBytes) {
+        st = plan_rowreg(c, 1, P);
         if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
     }
-    for (int cl = want; cl <= 16; cl <<= 1) {
-        st = plan_staged(c, cl, P);
+    if (row_bytes <= kStagedMaxRowBytes && c.dtype == RMSNORM_DTYPE_F32) {
+        st = plan_staged(c, 1, P);
         if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
     }
     return plan_twopass(c, P);
@@ -351,10 +406,14 @@ rmsnorm_status_t plan_auto(const Call& c, Plan* P) {
 
 rmsnorm_status_t make_plan(const Call& c, Plan* P) {
     const int cl = c.opt.cluster;
+    if (c.opt.reserved != 0) return RMSNORM_ERR_INVALID_ARG;
+    if (c.opt.fault_inject < 0 || c.opt.fault_inject > 2) return RMSNORM_ERR_INVALID_ARG;
+    if (c.opt.fault_inject != 0 && !RMSNORM_FAULT_INJECT) return RMSNORM_ERR_UNSUPPORTED;
     if (cl < 0 || cl > 16) return RMSNORM_ERR_INVALID_ARG;
     switch (c.opt.path) {
         case RMSNORM_PATH_AUTO:
-            if (cl != 0 || c.opt.threads != 0 || c.opt.chunk_bytes != 0)
+            if (cl != 0 || c.opt.threads != 0 || c.opt.chunk_bytes != 0 || c.opt.stages != 0 ||
+                c.opt.weights != 0)
                 return RMSNORM_ERR_INVALID_ARG;
             return plan_auto(c, P);
         case RMSNORM_PATH_ROWREG:
@@ -435,6 +494,9 @@ rmsnorm_status_t run(int32_t dtype, const void* x, const void* w, void* y, int64
     p.slice_vecs = P.slice_vecs;
     p.chunk_bytes = P.chunk;
     p.nchunks = P.nchunks;
+    p.nslots = P.nslots;
+    p.w_staged = P.w_staged;
+    p.fault = c.opt.fault_inject;
     p.status = c.info->status;
     p.timeout_ns = c.opt.wait_timeout_ns ? c.opt.wait_timeout_ns : kDefaultTimeoutNs;
 
@@ -493,6 +555,8 @@ rmsnorm_status_t rmsnorm_plan(int32_t dtype, const void* x, const void* w, const
     plan->vecs_per_thread = P.nv;
     plan->smem_bytes = P.smem;
     plan->chunk_bytes = P.chunk;
+    plan->stages = P.nslots;
+    plan->weights_staged = P.w_staged;
     std::snprintf(plan->kernel, sizeof(plan->kernel), "%s", P.name);
     return RMSNORM_OK;
 }
@@ -535,5 +599,8 @@ int32_t rmsnorm_last_cuda_error(char* msg, size_t len) {
 }
 
 int32_t rmsnorm_abi_version(void) { return 10000; }
+
+// Present in every build; non-zero only in the failure-injection test build.
+int32_t rmsnorm_fault_injection_enabled(void) { return RMSNORM_FAULT_INJECT; }
 
 }  // extern "C"

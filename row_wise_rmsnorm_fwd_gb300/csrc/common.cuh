@@ -9,7 +9,18 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#ifndef RMSNORM_FAULT_INJECT
+#define RMSNORM_FAULT_INJECT 0
+#endif
+
 namespace rmsnorm {
+
+// Failure-injection modes, compiled only into the test build of the library.
+enum : int {
+    kFaultNone = 0,
+    kFaultStagedWithholdCopy = 1,      // producer arms a barrier, issues no copy
+    kFaultClusterWithholdPartial = 2,  // one cluster CTA never sends its partial
+};
 
 // Device status word codes (low byte = rmsnorm_status_t, next byte = site).
 enum : unsigned {
@@ -35,6 +46,9 @@ struct Params {
     int32_t slice_vecs;    // vectors per CTA slice when cluster > 1
     int32_t chunk_bytes;   // staged path: bytes per bulk copy
     int32_t nchunks;       // staged path: bulk copies per row slice
+    int32_t nslots;        // staged path: chunk slots in the shared-memory ring
+    int32_t w_staged;      // staged path: weight slice held in shared memory
+    int32_t fault;         // failure-detection test builds only (else always 0)
     unsigned* status;      // per-device status word
     uint64_t timeout_ns;   // limit for every bounded wait
 };
@@ -304,6 +318,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
 }
 
+// The same without a cache policy.
+__device__ __forceinline__ void bulk_g2s_plain(uint32_t dst, const void* src, uint32_t bytes,
+                                               uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -382,7 +404,11 @@ __device__ __forceinline__ bool cluster_allreduce(ClusterExchange* ex, float par
                                                   uint32_t rank, uint32_t it,
                                                   const Params& p, float* total, int lt) {
     const uint32_t b = it & 1u;
-    if (lt < ncta) {
+    bool send = lt < ncta;
+#if RMSNORM_FAULT_INJECT
+    if (p.fault == kFaultClusterWithholdPartial && rank == 0 && it == 0) send = false;
+#endif
+    if (send) {
         const uint32_t peer = static_cast<uint32_t>(lt);
         const uint32_t slot = map_to_rank(smem_addr(&ex->slot[b][rank]), peer);
         const uint32_t bar = map_to_rank(smem_addr(&ex->bar[b]), peer);

@@ -17,21 +17,20 @@ struct LaunchShape {
 
 // Kernel instances; nullptr when the combination is not compiled.
 // dtype: 0 = fp32, 1 = bf16.  vb = bytes per vector, nv = vectors per thread.
-KernelFn rowreg_kernel_f32(int vb, int nv);
-KernelFn rowreg_kernel_bf16(int vb, int nv);
-KernelFn rowreg_kernel_ptr(int dtype, int vb, int nv);
+// pf = register prefetch of the next row (used by the cluster split-row path).
+KernelFn rowreg_kernel_f32(int vb, int nv, bool pf);
+KernelFn rowreg_kernel_bf16(int vb, int nv, bool pf);
+KernelFn rowreg_kernel_ptr(int dtype, int vb, int nv, bool pf);
 int rowreg_max_block(int nv);
 KernelFn twopass_kernel_ptr(int dtype, int vb);
 int twopass_block();
-KernelFn staged_kernel_ptr(int dtype);
-
-// Staged kernel geometry: one producer warp plus consumer warps.
-constexpr int kStagedConsumerWarps = 8;
-constexpr int kStagedThreads = 32 * (kStagedConsumerWarps + 1);
-constexpr int kStagedMaxChunksHost = 32;
-// Dynamic shared memory of the staged kernel: header + nchunks staging chunks
-// (-1 if nchunks is out of range).
-int staged_smem_bytes(int chunk_bytes, int nchunks);
+// Staged kernel: one producer warp plus 4 or 8 consumer warps.
+KernelFn staged_kernel_ptr(int dtype, int consumer_warps);
+constexpr int kStagedMaxSlotsHost = 32;
+constexpr int kStagedHeaderHost = 1024;
+// Dynamic shared memory of the staged kernel: header + weight slice (0 if the
+// weights come through L1/L2) + nslots chunk slots (-1 if nslots is out of range).
+int64_t staged_smem_bytes(int64_t chunk_bytes, int nslots, int64_t w_bytes);
 
 // cudaLaunchKernelEx with an optional cluster shape.
 inline cudaError_t launch_ex(KernelFn kernel, const LaunchShape& s, cudaStream_t stream,

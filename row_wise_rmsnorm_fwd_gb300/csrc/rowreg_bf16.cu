@@ -2,5 +2,7 @@
 #include "rowreg_instances.cuh"
 
 namespace rmsnorm {
-KernelFn rowreg_kernel_bf16(int vb, int nv) { return rowreg_pick<__nv_bfloat16>(vb, nv); }
+KernelFn rowreg_kernel_bf16(int vb, int nv, bool pf) {
+    return rowreg_pick<__nv_bfloat16>(vb, nv, pf);
+}
 }  // namespace rmsnorm

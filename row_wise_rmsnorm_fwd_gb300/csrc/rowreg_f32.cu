@@ -2,5 +2,7 @@
 #include "rowreg_instances.cuh"
 
 namespace rmsnorm {
-KernelFn rowreg_kernel_f32(int vb, int nv) { return rowreg_pick<float>(vb, nv); }
+KernelFn rowreg_kernel_f32(int vb, int nv, bool pf) {
+    return rowreg_pick<float>(vb, nv, pf);
+}
 }  // namespace rmsnorm

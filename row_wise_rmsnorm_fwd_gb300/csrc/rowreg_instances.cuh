@@ -27,11 +27,22 @@ KernelFn rowreg_instance() {
                          RMSNORM_ROWREG_ST>;
 }
 
+// `pf` asks for the register-prefetch instance (used when a cluster splits
+// rows: the next row's loads then overlap the cross-CTA exchange).  Eight
+// vectors per thread never prefetch (the register budget holds one row).
 template <typename T, int VB>
-KernelFn rowreg_pick_nv(int nv) {
+KernelFn rowreg_pick_nv(int nv, bool pf) {
     constexpr bool kPF = RMSNORM_ROWREG_PF != 0;
     if constexpr (VB < static_cast<int>(sizeof(T))) {
         return nullptr;
+    } else if (pf) {
+        switch (nv) {
+            case 1: return rowreg_instance<T, VB, 1, true>();
+            case 2: return rowreg_instance<T, VB, 2, true>();
+            case 4: return rowreg_instance<T, VB, 4, true>();
+            case 8: return rowreg_instance<T, VB, 8, false>();
+            default: return nullptr;
+        }
     } else {
         switch (nv) {
             case 1: return rowreg_instance<T, VB, 1, kPF>();
@@ -44,12 +55,12 @@ KernelFn rowreg_pick_nv(int nv) {
 }
 
 template <typename T>
-KernelFn rowreg_pick(int vb, int nv) {
+KernelFn rowreg_pick(int vb, int nv, bool pf) {
     switch (vb) {
-        case 16: return rowreg_pick_nv<T, 16>(nv);
-        case 8: return rowreg_pick_nv<T, 8>(nv);
-        case 4: return rowreg_pick_nv<T, 4>(nv);
-        case 2: return rowreg_pick_nv<T, 2>(nv);
+        case 16: return rowreg_pick_nv<T, 16>(nv, pf);
+        case 8: return rowreg_pick_nv<T, 8>(nv, pf);
+        case 4: return rowreg_pick_nv<T, 4>(nv, pf);
+        case 2: return rowreg_pick_nv<T, 2>(nv, pf);
         default: return nullptr;
     }
 }

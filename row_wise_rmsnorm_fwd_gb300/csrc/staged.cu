@@ -4,18 +4,22 @@
 
 namespace rmsnorm {
 
-static_assert(kStagedBlock == kStagedThreads, "staged block size mismatch");
-static_assert(kStagedConsumers == kStagedConsumerWarps, "staged warp count mismatch");
-static_assert(16 * kStagedMaxChunks + 256 + sizeof(ClusterExchange) <= kStagedHeader,
+static_assert(16 * kStagedMaxSlots + 16 + 256 + sizeof(ClusterExchange) <= kStagedHeader,
               "staged header overflows");
+static_assert(kStagedMaxSlots == kStagedMaxSlotsHost, "staged slot limit mismatch");
+static_assert(kStagedHeader == kStagedHeaderHost, "staged header size mismatch");
 
-KernelFn staged_kernel_ptr(int dtype) {
-    return dtype == 0 ? staged_kernel<float> : staged_kernel<__nv_bfloat16>;
+KernelFn staged_kernel_ptr(int dtype, int consumer_warps) {
+    if (consumer_warps == 4)
+        return dtype == 0 ? staged_kernel<float, 4> : staged_kernel<__nv_bfloat16, 4>;
+    if (consumer_warps == 8)
+        return dtype == 0 ? staged_kernel<float, 8> : staged_kernel<__nv_bfloat16, 8>;
+    return nullptr;
 }
 
-int staged_smem_bytes(int chunk_bytes, int nchunks) {
-    if (nchunks < 1 || nchunks > kStagedMaxChunks) return -1;
-    return kStagedHeader + chunk_bytes * nchunks;
+int64_t staged_smem_bytes(int64_t chunk_bytes, int nslots, int64_t w_bytes) {
+    if (nslots < 1 || nslots > kStagedMaxSlots) return -1;
+    return kStagedHeader + w_bytes + chunk_bytes * nslots;
 }
 
 }  // namespace rmsnorm

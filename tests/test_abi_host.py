@@ -43,9 +43,9 @@ def test_status_strings(lib):
 
 
 def test_struct_sizes_match_header():
-    # int32 x 6 + uint64 = 32 bytes; int32 x 10 + char[48] = 88 bytes
-    assert ctypes.sizeof(binding.rmsnorm_options_t) == 32
-    assert ctypes.sizeof(binding.rmsnorm_plan_t) == 88
+    # int32 x 10 + uint64 = 48 bytes; int32 x 12 + char[48] = 96 bytes
+    assert ctypes.sizeof(binding.rmsnorm_options_t) == 48
+    assert ctypes.sizeof(binding.rmsnorm_plan_t) == 96
 
 
 A = 0x10000000     # fake, 256-byte aligned "device" addresses: never dereferenced

@@ -116,7 +116,9 @@ def test_wide_rows(dtype, rows, hidden):
 
 FORCED = [
     ("rowreg", {}), ("twopass", {}), ("staged", {}), ("staged", {"chunk_bytes": 4096}),
-    ("staged", {"cluster": 2}), ("staged", {"cluster": 4}),
+    ("staged", {"cluster": 2}), ("staged", {"cluster": 4}), ("staged", {"threads": 128}),
+    ("staged", {"weights": 1}), ("staged", {"weights": 2, "chunk_bytes": 2048}),
+    ("staged", {"stages": 32, "chunk_bytes": 1024}), ("staged", {"cluster": 2, "weights": 1}),
     ("cluster", {"cluster": 2}), ("cluster", {"cluster": 4}), ("cluster", {"cluster": 8}),
     ("cluster", {"cluster": 16}),
 ]
