@@ -373,8 +373,10 @@ def run_ours(args, wl):
 
 def measure_e2e(args, wl, x_dev, w_dev, y_dev, fwd, binding, world):
     """Same metric end to end: pinned host x,w -> device, the C-ABI call, device
-    y -> pinned host, every step.  The row range is split into chunks run on
-    two streams so that copies in both directions overlap the kernel."""
+    y -> pinned host, every step.  The row range is split into 32 chunks run
+    on four streams so that copies in both directions overlap the kernel
+    (measured on GB300: host<->device copies run at about 200 GB/s each way,
+    so this number is bound by the host link, not by the kernel)."""
     import torch
 
     dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
@@ -385,9 +387,9 @@ def measure_e2e(args, wl, x_dev, w_dev, y_dev, fwd, binding, world):
     rows, hidden = wl.rows, wl.hidden
     xh2, yh2 = x_h.view(rows, hidden), y_h.view(rows, hidden)
     xd2, yd2 = x_dev.view(rows, hidden), y_dev.view(rows, hidden)
-    nchunks = 16 if rows >= 16 else 1
+    nchunks = 32 if rows >= 32 else 1
     bounds = [rows * i // nchunks for i in range(nchunks + 1)]
-    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    streams = [torch.cuda.Stream() for _ in range(4)]
     launches = [0]
 
     def step():
@@ -397,7 +399,7 @@ def measure_e2e(args, wl, x_dev, w_dev, y_dev, fwd, binding, world):
             w_dev.copy_(w_h, non_blocking=True)
             ev_w.record(s0)
         for i in range(nchunks):
-            s = streams[i % 2]
+            s = streams[i % len(streams)]
             a, b = bounds[i], bounds[i + 1]
             with torch.cuda.stream(s):
                 s.wait_event(ev_w)
@@ -432,7 +434,7 @@ def measure_e2e(args, wl, x_dev, w_dev, y_dev, fwd, binding, world):
             "h2d_bytes_per_step": (rows * hidden + hidden) * wl.elem_bytes,
             "d2h_bytes_per_step": rows * hidden * wl.elem_bytes,
             "steps": n, "ms_per_step": 1e3 * dt_s / n, "chunks_per_step": nchunks,
-            "streams": 2, "gpu_launches": launches[0], "timing": "host wall clock"}
+            "streams": len(streams), "gpu_launches": launches[0], "timing": "host wall clock"}
 
 
 def main():
@@ -445,7 +447,7 @@ def main():
     ap.add_argument("--rows", type=int, default=0,
                     help="use only this many rows of the workload (small profiling cases)")
     ap.add_argument("--path", default="auto",
-                    choices=["auto", "rowreg", "staged", "cluster", "twopass"],
+                    choices=["auto", "rowreg", "staged", "cluster", "twopass", "page"],
                     help="force a kernel family through rmsnorm_fwd_ex (evidence runs)")
     ap.add_argument("--cluster", type=int, default=0)
     ap.add_argument("--grid", type=int, default=0, help="force the CTA count")

@@ -67,7 +67,11 @@ typedef enum {
                                   (cp.async.bulk + mbarrier), multi-stage prefetch    */
     RMSNORM_PATH_CLUSTER = 3,  /* split row: a thread-block cluster per row, slices in
                                   registers, partial sums exchanged through DSMEM     */
-    RMSNORM_PATH_TWOPASS = 4   /* generic fallback: read x twice (any width/alignment) */
+    RMSNORM_PATH_TWOPASS = 4,  /* generic fallback: read x twice (any width/alignment) */
+    RMSNORM_PATH_PAGE = 5      /* comparison only, never automatic: the compiler write-up's
+                                  schedule (one 256-thread CTA per row, whole row staged
+                                  in shared memory, 4-byte accesses, 3-level tree); rows
+                                  up to the shared-memory limit (about 56K elements) */
 } rmsnorm_path_t;
 
 /* Options for rmsnorm_fwd_ex / rmsnorm_plan.  Zero-initialise, then set what you

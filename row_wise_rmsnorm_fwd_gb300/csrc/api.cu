@@ -367,6 +367,35 @@ rmsnorm_status_t plan_twopass(const Call& c, Plan* P) {
     return RMSNORM_OK;
 }
 
+// The write-up's own schedule (comparison only): one CTA of 256 threads per
+// row, the whole row staged in shared memory as fp32.
+rmsnorm_status_t plan_page(const Call& c, Plan* P) {
+    if (c.opt.cluster > 1 || c.opt.threads != 0 || c.opt.vec_bytes > c.sz)
+        return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t smem = c.hidden * 4;
+    if (smem + 1024 > c.info->smem_optin) return RMSNORM_ERR_UNSUPPORTED;
+    if (c.rows > 0x7FFFFFFFll) return RMSNORM_ERR_UNSUPPORTED;
+    KernelFn fn = page_kernel_ptr(c.dtype);
+    int occ = 0;
+    if (cached_occupancy(c.dev, fn, page_block(), static_cast<int>(smem), 1, &occ) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
+    P->path = RMSNORM_PATH_PAGE;
+    P->cluster = 1;
+    P->group = page_block();
+    P->block = page_block();
+    P->rpc = 1;
+    P->grid = static_cast<int>(c.rows);
+    P->vb = c.sz;
+    P->nv = 0;
+    P->smem = static_cast<int>(smem);
+    P->nvec = static_cast<int>(c.hidden);
+    P->slice_vecs = static_cast<int>(c.hidden);
+    P->fn = fn;
+    P->name = "page_schedule";
+    return RMSNORM_OK;
+}
+
 // The launch heuristics, from measurements on GB300 (profiles/kernel_choices.md):
 //  - few rows (fewer than SMs): split each row over a cluster so that about one
 //    CTA per SM works, keeping slices of at least 4 KB;
@@ -427,6 +456,8 @@ rmsnorm_status_t make_plan(const Call& c, Plan* P) {
         case RMSNORM_PATH_TWOPASS:
             if (cl > 1) return RMSNORM_ERR_INVALID_ARG;
             return plan_twopass(c, P);
+        case RMSNORM_PATH_PAGE:
+            return plan_page(c, P);
         default:
             return RMSNORM_ERR_INVALID_ARG;
     }

@@ -24,6 +24,10 @@ KernelFn rowreg_kernel_ptr(int dtype, int vb, int nv, bool pf);
 int rowreg_max_block(int nv);
 KernelFn twopass_kernel_ptr(int dtype, int vb);
 int twopass_block();
+// Comparison kernel with the compiler write-up's schedule (one CTA per row).
+KernelFn page_kernel_ptr(int dtype);
+int page_block();
+
 // Staged kernel: one producer warp plus 4 or 8 consumer warps.
 KernelFn staged_kernel_ptr(int dtype, int consumer_warps);
 constexpr int kStagedMaxSlotsHost = 32;

@@ -63,6 +63,15 @@ def test_workload_full(name):
     check_case(x, w, wl.eps, name)
 
 
+@pytest.mark.parametrize("name", ["c1", "c2", "c2t", "c3"])
+def test_workload_page_schedule(name):
+    """The write-up's own schedule, rebuilt as a comparison kernel, on the
+    workloads it fits (the page's example is c1)."""
+    wl = workloads.WORKLOADS[name]
+    x, w = workloads.make_x(wl), workloads.make_w(wl)
+    check_case(x.reshape(-1, wl.hidden), w, wl.eps, f"page schedule {name}", path="page")
+
+
 @pytest.mark.parametrize("name", ["c4", "c5a"])
 def test_workload_full_size_sampled_rows(name):
     """Full-size workload in the bench's launch configuration (automatic
@@ -120,7 +129,7 @@ FORCED = [
     ("staged", {"weights": 1}), ("staged", {"weights": 2, "chunk_bytes": 2048}),
     ("staged", {"stages": 32, "chunk_bytes": 1024}), ("staged", {"cluster": 2, "weights": 1}),
     ("cluster", {"cluster": 2}), ("cluster", {"cluster": 4}), ("cluster", {"cluster": 8}),
-    ("cluster", {"cluster": 16}),
+    ("cluster", {"cluster": 16}), ("page", {}),
 ]
 
 
@@ -186,7 +195,7 @@ def test_in_place(dtype, rows, hidden):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("path", ["auto", "rowreg", "staged", "cluster", "twopass"])
+@pytest.mark.parametrize("path", ["auto", "rowreg", "staged", "cluster", "twopass", "page"])
 def test_guard_regions_untouched(dtype, path):
     """Sentinels before and after y stay intact (no out-of-bounds stores)."""
     rows, hidden = 21, 4104
@@ -237,7 +246,7 @@ def test_eps_zero_zero_row_is_nan():
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("path", ["auto", "rowreg", "staged", "cluster", "twopass"])
+@pytest.mark.parametrize("path", ["auto", "rowreg", "staged", "cluster", "twopass", "page"])
 def test_deterministic(dtype, path):
     x, w = rand_case(64, 8192, dtype, seed=123)
     xc, wc = x.cuda(), w.cuda()
