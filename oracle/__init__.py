@@ -60,8 +60,11 @@ def _load():
         lib.oracle_rmsnorm_f32.argtypes = [vp, vp, vp, i64, i64, dbl]
         lib.oracle_rmsnorm_bf16.argtypes = [vp, vp, vp, vp, i64, i64, dbl]
         lib.oracle_rmsnorm_stats_f64.argtypes = [vp, vp, vp, i64, i64, dbl]
+        lib.oracle_apply_epilogue_f64.argtypes = [vp, i64, ctypes.c_int, dbl]
+        lib.oracle_f64_to_bf16_array.argtypes = [vp, vp, i64]
         for f in ("oracle_rmsnorm_f64", "oracle_rmsnorm_f32",
-                  "oracle_rmsnorm_bf16", "oracle_rmsnorm_stats_f64"):
+                  "oracle_rmsnorm_bf16", "oracle_rmsnorm_stats_f64",
+                  "oracle_apply_epilogue_f64", "oracle_f64_to_bf16_array"):
             getattr(lib, f).restype = ctypes.c_int
         lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_to_f64.restype = ctypes.c_double
@@ -142,6 +145,39 @@ def rmsnorm_stats_f64(x: np.ndarray, eps: float):
     _check(_load().oracle_rmsnorm_stats_f64(_ptr(x), _ptr(ms), _ptr(rstd),
                                             rows, hidden, float(eps)))
     return ms, rstd
+
+
+EPILOGUES = {"none": 0, "scale": 1, "relu": 2}
+
+
+def apply_epilogue(y: np.ndarray, kind, alpha: float = 1.0) -> np.ndarray:
+    """The fused epilogue on binary64 outputs (copy): none, scale by alpha, or
+    ReLU (NaN kept, non-positive values become +0)."""
+    k = EPILOGUES[kind] if isinstance(kind, str) else int(kind)
+    out = np.array(y, dtype=np.float64, copy=True, order="C")
+    _check(_load().oracle_apply_epilogue_f64(_ptr(out), out.size, k, float(alpha)))
+    return out
+
+
+def f64_to_bf16_fast(values) -> np.ndarray:
+    """Vectorised binary64 -> bfloat16 bits (one RNE rounding per element)."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    _check(_load().oracle_f64_to_bf16_array(_ptr(v), _ptr(out), v.size))
+    return out
+
+
+def rmsnorm_epilogue_f32(x: np.ndarray, w: np.ndarray, eps: float, kind, alpha=1.0):
+    """fp32 inputs; RMSNorm then the epilogue, all in binary64."""
+    return apply_epilogue(rmsnorm_f32(x, w, eps), kind, alpha)
+
+
+def rmsnorm_epilogue_bf16(x_bits, w_bits, eps: float, kind, alpha=1.0):
+    """bf16 inputs; RMSNorm and the epilogue in binary64, then ONE rounding.
+    Returns (y64, y16)."""
+    y64, _ = rmsnorm_bf16(x_bits, w_bits, eps)
+    e64 = apply_epilogue(y64, kind, alpha)
+    return e64, f64_to_bf16_fast(e64)
 
 
 def bf16_to_f64(bits) -> np.ndarray:

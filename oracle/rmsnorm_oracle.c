@@ -19,6 +19,14 @@
  * sqrt followed by a true division (no approximate reciprocal square root).
  * No SIMD, no -ffast-math, no reordering beyond the definition above.
  *
+ * Fused epilogue (page "CuTe DSL JIT argument generation", section 2.3, and
+ * the CuTe DSL control-flow page, section 7: a compile-time epilogue_op, e.g.
+ * an optional ReLU, applied to each output value before it is stored):
+ * oracle_apply_epilogue_f64 maps every binary64 output v to
+ *     kind 0: v,   kind 1: alpha * v,   kind 2: ReLU(v) = v if v > 0 or v is
+ *     NaN, else +0,
+ * and the bf16 result is the single rounding of the epilogue's output.
+ *
  * bfloat16 (the pages never mention it; the plain reading used here):
  * inputs are decoded exactly to binary64, the whole computation above runs
  * in binary64, and the result is rounded ONCE to bfloat16 with
@@ -174,6 +182,31 @@ int oracle_rmsnorm_bf16(const uint16_t* x, const uint16_t* w, double* y64,
             if (y16) y16[r * hidden + j] = oracle_f64_to_bf16_rne(v);
         }
     }
+    return ORACLE_OK;
+}
+
+/* ---- epilogue ----------------------------------------------------------- */
+
+int oracle_apply_epilogue_f64(double* y, int64_t n, int kind, double alpha)
+{
+    if (n < 0 || (n > 0 && y == 0) || kind < 0 || kind > 2) return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i) {
+        double v = y[i];
+        if (kind == 1) {
+            v = alpha * v;
+        } else if (kind == 2) {
+            v = (v > 0.0 || isnan(v)) ? v : 0.0;
+        }
+        y[i] = v;
+    }
+    return ORACLE_OK;
+}
+
+/* Round every element once, binary64 -> bfloat16 (round to nearest even). */
+int oracle_f64_to_bf16_array(const double* v, uint16_t* out, int64_t n)
+{
+    if (n < 0 || (n > 0 && (v == 0 || out == 0))) return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f64_to_bf16_rne(v[i]);
     return ORACLE_OK;
 }
 

@@ -39,6 +39,11 @@ MUTANTS = {
                           "double n = ldexp((double)(float)a, -(int)q_exp);"),
     "bf16_ties_away": ("return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;",
                        "return fl + 1.0;"),
+    "epilogue_relu_drops_nan": ("v = (v > 0.0 || isnan(v)) ? v : 0.0;",
+                                "v = (v > 0.0) ? v : 0.0;"),
+    "epilogue_relu_keeps_negative_zero": ("v = (v > 0.0 || isnan(v)) ? v : 0.0;",
+                                          "v = (v >= 0.0 || isnan(v)) ? v : 0.0;"),
+    "epilogue_scale_ignored": ("v = alpha * v;", "v = v;"),
 }
 
 
@@ -59,6 +64,7 @@ def _build(tmp_path, name, mutation):
     lib.oracle_rmsnorm_f64.argtypes = [vp, vp, vp, i64, i64, dbl]
     lib.oracle_f64_to_bf16_rne.argtypes = [dbl]
     lib.oracle_f64_to_bf16_rne.restype = ctypes.c_uint16
+    lib.oracle_apply_epilogue_f64.argtypes = [vp, i64, ctypes.c_int, dbl]
     return lib
 
 
@@ -80,7 +86,16 @@ def _pins_pass(lib) -> bool:
     # (1 + 3*2^-8 -> 0x3F82), and a hair above a tie (must round up)
     probes = {1.0 + 2.0 ** -8: 0x3F80, 1.0 + 3 * 2.0 ** -8: 0x3F82,
               (1.0 + 2.0 ** -8) * (1 + 2.0 ** -40): 0x3F81, 1.0: 0x3F80}
-    return all(lib.oracle_f64_to_bf16_rne(v) == b for v, b in probes.items())
+    if not all(lib.oracle_f64_to_bf16_rne(v) == b for v, b in probes.items()):
+        return False
+    # epilogue definition: ReLU keeps NaN and maps -0 to +0; scale multiplies
+    v = np.array([-2.0, -0.0, 3.0, np.nan])
+    lib.oracle_apply_epilogue_f64(v.ctypes.data, v.size, 2, 0.0)
+    if not (v[0] == 0 and not np.signbit(v[1]) and v[2] == 3.0 and np.isnan(v[3])):
+        return False
+    v = np.array([1.5, -2.0])
+    lib.oracle_apply_epilogue_f64(v.ctypes.data, v.size, 1, 4.0)
+    return bool(v[0] == 6.0 and v[1] == -8.0)
 
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")

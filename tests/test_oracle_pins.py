@@ -369,3 +369,56 @@ def test_rejects_bad_shapes():
 def test_empty_rows_ok():
     y = oracle.rmsnorm_f64(np.ones((0, 5)), np.ones(5), 1e-6)
     assert y.shape == (0, 5)
+
+
+# ------------------------------------------------------------- epilogues --
+# The fused epilogue (CuTe DSL JIT-argument page, section 2.3: a compile-time
+# epilogue_op such as an optional ReLU, applied to each output before the store).
+
+def test_epilogue_scale_power_of_two_is_exact():
+    rng = np.random.default_rng(30)
+    x = rng.normal(0, 1, (4, 65)).astype(np.float32)
+    w = rng.normal(1, 0.1, 65).astype(np.float32)
+    base = oracle.rmsnorm_f32(x, w, 1e-6)
+    for a in (0.25, 2.0, -8.0):
+        np.testing.assert_array_equal(oracle.rmsnorm_epilogue_f32(x, w, 1e-6, "scale", a),
+                                      a * base)
+
+
+def test_epilogue_relu_definition():
+    y = np.array([-2.0, -0.0, 0.0, 1e-300, 3.5, np.nan, -np.inf, np.inf])
+    got = oracle.apply_epilogue(y, "relu")
+    assert got[0] == 0 and got[1] == 0 and np.signbit(got[1]) == False  # noqa: E712
+    assert got[2] == 0 and got[3] == 1e-300 and got[4] == 3.5
+    assert np.isnan(got[5]) and got[6] == 0 and got[7] == np.inf
+
+
+def test_epilogue_relu_matches_torch_float64():
+    g = torch.Generator().manual_seed(31)
+    x = torch.randn(7, 300, generator=g, dtype=torch.float64)
+    w = torch.randn(300, generator=g, dtype=torch.float64) * 0.5 + 0.2
+    ref = torch.relu(torch.nn.functional.rms_norm(x, (300,), w, 1e-5)).numpy()
+    got = oracle.apply_epilogue(oracle.rmsnorm_f64(x.numpy(), w.numpy(), 1e-5), "relu")
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=0)
+    assert (got >= 0).all()
+
+
+def test_epilogue_none_is_identity_and_bf16_rounds_once():
+    g = torch.Generator().manual_seed(32)
+    x = (torch.randn(5, 200, generator=g) * 2).to(torch.bfloat16)
+    w = (torch.randn(200, generator=g) * 0.1 + 1).to(torch.bfloat16)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    wb = w.view(torch.int16).numpy().view(np.uint16)
+    y64, y16 = oracle.rmsnorm_bf16(xb, wb, 1e-6)
+    e64, e16 = oracle.rmsnorm_epilogue_bf16(xb, wb, 1e-6, "none")
+    np.testing.assert_array_equal(e64, y64)
+    np.testing.assert_array_equal(e16, y16)
+    s64, s16 = oracle.rmsnorm_epilogue_bf16(xb, wb, 1e-6, "scale", 3.0)
+    np.testing.assert_array_equal(s64, 3.0 * y64)
+    np.testing.assert_array_equal(s16, oracle.f64_to_bf16(3.0 * y64))
+
+
+def test_vectorised_encoder_matches_scalar_encoder():
+    rng = np.random.default_rng(33)
+    v = rng.normal(0, 1, 5000) * 2.0 ** rng.integers(-130, 128, 5000)
+    np.testing.assert_array_equal(oracle.f64_to_bf16_fast(v), oracle.f64_to_bf16(v))
