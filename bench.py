@@ -221,14 +221,16 @@ def run_reference(args, wl):
 
 
 def forced(args) -> bool:
-    return bool(args.path != "auto" or args.cluster or args.grid or args.threads or args.chunk)
+    return bool(args.path != "auto" or args.cluster or args.grid or args.threads or args.chunk
+                or args.epilogue != "none")
 
 
 def config_block(wl, world, args=None):
     extra = {}
     if args is not None and forced(args):
         extra["forced"] = {"path": args.path, "cluster": args.cluster, "grid": args.grid,
-                           "threads": args.threads, "chunk_bytes": args.chunk}
+                           "threads": args.threads, "chunk_bytes": args.chunk,
+                           "epilogue": args.epilogue}
     return {**extra,
         "workload": f"{wl.name}: {wl.description}",
         "shape": list(wl.shape), "io_dtype": wl.dtype, "eps": wl.eps,
@@ -265,7 +267,8 @@ def run_ours(args, wl):
     options = None
     if forced(args):
         options = binding.make_options(path=args.path, cluster=args.cluster, grid=args.grid,
-                                       threads=args.threads, chunk_bytes=args.chunk)
+                                       threads=args.threads, chunk_bytes=args.chunk,
+                                       epilogue=args.epilogue, alpha=0.5)
         dt_code = binding.RMSNORM_DTYPE_BF16 if wl.dtype == "bf16" else binding.RMSNORM_DTYPE_F32
 
         def fwd(xp, wp, yp, r, h, eps, s):
@@ -453,6 +456,8 @@ def main():
     ap.add_argument("--grid", type=int, default=0, help="force the CTA count")
     ap.add_argument("--threads", type=int, default=0, help="force threads per row group")
     ap.add_argument("--chunk", type=int, default=0, help="staged path: bytes per bulk copy")
+    ap.add_argument("--epilogue", default="none", choices=["none", "scale", "relu"],
+                    help="fused epilogue (measures its cost; default none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()

@@ -95,6 +95,10 @@ typedef struct {
                                 RMSNORM_FAULT_INJECT); the product library returns
                                 RMSNORM_ERR_UNSUPPORTED for any non-zero value. */
     int32_t reserved;        /* must be 0 */
+    int32_t epilogue;        /* fused epilogue applied to each output before the store
+                                (any path but PAGE): 0 none, 1 y*epilogue_alpha,
+                                2 ReLU (y if y > 0 or y is NaN, else +0) */
+    float epilogue_alpha;    /* scale for epilogue 1 (finite) */
     uint64_t wait_timeout_ns;/* limit of every device-side wait; 0 = 2 seconds */
 } rmsnorm_options_t;
 

@@ -38,6 +38,7 @@ class rmsnorm_options_t(ctypes.Structure):
                 ("vec_bytes", ctypes.c_int32), ("chunk_bytes", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("weights", ctypes.c_int32),
                 ("fault_inject", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("epilogue", ctypes.c_int32), ("epilogue_alpha", ctypes.c_float),
                 ("wait_timeout_ns", ctypes.c_uint64)]
 
 
@@ -127,11 +128,12 @@ def declared_functions() -> list[str]:
 
 
 WEIGHTS = {"auto": 0, "smem": 1, "l2": 2}
+EPILOGUES = {"none": 0, "scale": 1, "relu": 2}
 
 
 def make_options(path="auto", cluster=0, threads=0, grid=0, vec_bytes=0,
                  chunk_bytes=0, stages=0, weights=0, wait_timeout_ns=0,
-                 fault_inject=0) -> rmsnorm_options_t:
+                 fault_inject=0, epilogue=0, alpha=1.0) -> rmsnorm_options_t:
     o = rmsnorm_options_t()
     o.path = PATHS[path] if isinstance(path, str) else int(path)
     o.cluster, o.threads, o.grid = int(cluster), int(threads), int(grid)
@@ -139,6 +141,8 @@ def make_options(path="auto", cluster=0, threads=0, grid=0, vec_bytes=0,
     o.stages = int(stages)
     o.weights = WEIGHTS[weights] if isinstance(weights, str) else int(weights)
     o.fault_inject = int(fault_inject)
+    o.epilogue = EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
+    o.epilogue_alpha = float(alpha)
     o.wait_timeout_ns = int(wait_timeout_ns)
     return o
 

@@ -19,8 +19,13 @@ __device__ unsigned g_rmsnorm_status = 0u;
 
 namespace rmsnorm {
 
-KernelFn rowreg_kernel_ptr(int dtype, int vb, int nv, bool pf) {
-    return dtype == 0 ? rowreg_kernel_f32(vb, nv, pf) : rowreg_kernel_bf16(vb, nv, pf);
+KernelFn rowreg_kernel_ptr(int dtype, int vb, int nv, bool pf, int epi) {
+    using Pick = KernelFn (*)(int, int, bool);
+    static const Pick table[2][3] = {
+        {rowreg_kernel_f32_e0, rowreg_kernel_f32_e1, rowreg_kernel_f32_e2},
+        {rowreg_kernel_bf16_e0, rowreg_kernel_bf16_e1, rowreg_kernel_bf16_e2}};
+    if (dtype < 0 || dtype > 1 || epi < 0 || epi > 2) return nullptr;
+    return table[dtype][epi](vb, nv, pf);
 }
 int rowreg_max_block(int nv) { return nv >= 4 ? 512 : 1024; }
 
@@ -204,7 +209,7 @@ rmsnorm_status_t plan_rowreg(const Call& c, int cluster, Plan* P) {
         G = static_cast<int>(g);
     }
     if (G > rowreg_max_block(NV)) return RMSNORM_ERR_UNSUPPORTED;
-    KernelFn fn = rowreg_kernel_ptr(c.dtype, vb, NV, cluster > 1);
+    KernelFn fn = rowreg_kernel_ptr(c.dtype, vb, NV, cluster > 1, c.opt.epilogue);
     if (!fn) return RMSNORM_ERR_UNSUPPORTED;
     const int rpc = cluster == 1 ? (G >= 256 ? 1 : 256 / G) : 1;
     const int block = G * rpc;
@@ -298,7 +303,7 @@ rmsnorm_status_t plan_staged(const Call& c, int cluster, Plan* P) {
         ncw = c.opt.threads / 32;
     }
     const int block = 32 * (ncw + 1);
-    KernelFn fn = staged_kernel_ptr(c.dtype, ncw);
+    KernelFn fn = staged_kernel_ptr(c.dtype, ncw, c.opt.epilogue);
     if (!fn) return RMSNORM_ERR_UNSUPPORTED;
     int occ = 0;
     if (cached_occupancy(c.dev, fn, block, static_cast<int>(smem), cluster, &occ) !=
@@ -340,7 +345,7 @@ rmsnorm_status_t plan_twopass(const Call& c, Plan* P) {
     int vb;
     rmsnorm_status_t st = pick_vb(c, &vb);
     if (st != RMSNORM_OK) return st;
-    KernelFn fn = twopass_kernel_ptr(c.dtype, vb);
+    KernelFn fn = twopass_kernel_ptr(c.dtype, vb, c.opt.epilogue);
     if (!fn) return RMSNORM_ERR_UNSUPPORTED;
     const int64_t nvec = c.hidden / (vb / c.sz);
     int block = c.opt.threads > 0 ? c.opt.threads
@@ -370,7 +375,8 @@ rmsnorm_status_t plan_twopass(const Call& c, Plan* P) {
 // The write-up's own schedule (comparison only): one CTA of 256 threads per
 // row, the whole row staged in shared memory as fp32.
 rmsnorm_status_t plan_page(const Call& c, Plan* P) {
-    if (c.opt.cluster > 1 || c.opt.threads != 0 || c.opt.vec_bytes > c.sz)
+    if (c.opt.cluster > 1 || c.opt.threads != 0 || c.opt.vec_bytes > c.sz ||
+        c.opt.epilogue != 0)
         return RMSNORM_ERR_UNSUPPORTED;
     const int64_t smem = c.hidden * 4;
     if (smem + 1024 > c.info->smem_optin) return RMSNORM_ERR_UNSUPPORTED;
@@ -437,13 +443,15 @@ rmsnorm_status_t make_plan(const Call& c, Plan* P) {
     const int cl = c.opt.cluster;
     if (c.opt.reserved != 0) return RMSNORM_ERR_INVALID_ARG;
     if (c.opt.fault_inject < 0 || c.opt.fault_inject > 2) return RMSNORM_ERR_INVALID_ARG;
+    if (c.opt.epilogue < 0 || c.opt.epilogue > 2) return RMSNORM_ERR_INVALID_ARG;
+    if (c.opt.epilogue == 1 && !std::isfinite(c.opt.epilogue_alpha)) return RMSNORM_ERR_INVALID_ARG;
     if (c.opt.fault_inject != 0 && !RMSNORM_FAULT_INJECT) return RMSNORM_ERR_UNSUPPORTED;
     if (cl < 0 || cl > 16) return RMSNORM_ERR_INVALID_ARG;
     switch (c.opt.path) {
         case RMSNORM_PATH_AUTO:
             if (cl != 0 || c.opt.threads != 0 || c.opt.chunk_bytes != 0 || c.opt.stages != 0 ||
                 c.opt.weights != 0)
-                return RMSNORM_ERR_INVALID_ARG;
+                return RMSNORM_ERR_INVALID_ARG;   // launch-shape options need a forced path
             return plan_auto(c, P);
         case RMSNORM_PATH_ROWREG:
             if (cl > 1) return RMSNORM_ERR_INVALID_ARG;
@@ -528,6 +536,7 @@ rmsnorm_status_t run(int32_t dtype, const void* x, const void* w, void* y, int64
     p.nslots = P.nslots;
     p.w_staged = P.w_staged;
     p.fault = c.opt.fault_inject;
+    p.alpha = c.opt.epilogue == 1 ? c.opt.epilogue_alpha : 1.0f;
     p.status = c.info->status;
     p.timeout_ns = c.opt.wait_timeout_ns ? c.opt.wait_timeout_ns : kDefaultTimeoutNs;
 

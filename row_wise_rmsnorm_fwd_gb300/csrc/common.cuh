@@ -22,6 +22,25 @@ enum : int {
     kFaultClusterWithholdPartial = 2,  // one cluster CTA never sends its partial
 };
 
+// Fused epilogues, applied to each fp32 output value before the store
+// (compile-time choice; the CuTe DSL pages' Constexpr epilogue_op idea).
+enum : int {
+    kEpiNone = 0,     // y
+    kEpiScale = 1,    // y * alpha
+    kEpiRelu = 2,     // y if y > 0 or y is NaN, else +0
+};
+
+template <int EPI>
+__device__ __forceinline__ float epilogue(float v, float alpha) {
+    if constexpr (EPI == kEpiScale) {
+        return v * alpha;
+    } else if constexpr (EPI == kEpiRelu) {
+        return (v > 0.f || v != v) ? v : 0.f;
+    } else {
+        return v;
+    }
+}
+
 // Device status word codes (low byte = rmsnorm_status_t, next byte = site).
 enum : unsigned {
     kStatusTimeout = 4u,
@@ -49,6 +68,7 @@ struct Params {
     int32_t nslots;        // staged path: chunk slots in the shared-memory ring
     int32_t w_staged;      // staged path: weight slice held in shared memory
     int32_t fault;         // failure-detection test builds only (else always 0)
+    float alpha;           // epilogue scale (kEpiScale)
     unsigned* status;      // per-device status word
     uint64_t timeout_ns;   // limit for every bounded wait
 };

@@ -24,7 +24,8 @@
 //
 // Compile-time choices: PF (register prefetch of the next row), WREG (weights
 // held in registers across rows, packed; otherwise re-read from L1 per row),
-// LD / ST (cache policies of the x loads and y stores, see common.cuh).
+// LD / ST (cache policies of the x loads and y stores, see common.cuh), EPI
+// (fused epilogue applied before the store).
 #pragma once
 #include "common.cuh"
 
@@ -33,7 +34,7 @@ namespace rmsnorm {
 template <int NV>
 constexpr int rowreg_max_threads() { return NV >= 4 ? 512 : 1024; }
 
-template <typename T, int VB, int NV, bool PF, bool WREG, int LD, int ST>
+template <typename T, int VB, int NV, bool PF, bool WREG, int LD, int ST, int EPI>
 __global__ void __launch_bounds__(rowreg_max_threads<NV>())
 rowreg_kernel(const Params p) {
     constexpr int EPV = VecTraits<T, VB>::kElems;
@@ -158,7 +159,8 @@ rowreg_kernel(const Params p) {
                     float o[EPV];
 #pragma unroll
                     for (int k = 0; k < EPV; ++k)
-                        o[k] = (get<T, VB>(cur[i], k) * rstd) * get<T, VB>(wi, k);
+                        o[k] = epilogue<EPI>((get<T, VB>(cur[i], k) * rstd) * get<T, VB>(wi, k),
+                                             p.alpha);
                     st_stream<VB, ST>(dst + static_cast<int64_t>(vidx[i]) * VB,
                                       pack<T, VB>(o));
                 }

@@ -64,7 +64,7 @@ __device__ __forceinline__ Vec<16> as_vec(const uint4& q) {
 
 // NCW consumer warps (plus the producer warp).  Registers are capped at 96 so
 // that two 9-warp CTAs fit the register file of every SM sub-partition.
-template <typename T, int NCW>
+template <typename T, int NCW, int EPI>
 __global__ void __maxnreg__(96) staged_kernel(const Params p) {
     constexpr int EPV = 16 / static_cast<int>(sizeof(T));
     constexpr int NC = 32 * NCW;
@@ -265,7 +265,8 @@ __global__ void __maxnreg__(96) staged_kernel(const Params p) {
                             float o[EPV];
 #pragma unroll
                             for (int e = 0; e < EPV; ++e)
-                                o[e] = (get<T, 16>(xv, e) * rstd) * get<T, 16>(wv[u], e);
+                                o[e] = epilogue<EPI>(
+                                    (get<T, 16>(xv, e) * rstd) * get<T, 16>(wv[u], e), p.alpha);
                             st_stream<16>(dst + koff + static_cast<int64_t>(v) * 16,
                                           pack<T, 16>(o));
                         }

@@ -13,7 +13,7 @@ namespace rmsnorm {
 
 constexpr int kTwoPassThreads = 1024;
 
-template <typename T, int VB>
+template <typename T, int VB, int EPI>
 __global__ void __launch_bounds__(kTwoPassThreads) twopass_kernel(const Params p) {
     constexpr int EPV = VecTraits<T, VB>::kElems;
     __shared__ float red[2][32];
@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kTwoPassThreads) twopass_kernel(const Params p
             float o[EPV];
 #pragma unroll
             for (int k = 0; k < EPV; ++k)
-                o[k] = (get<T, VB>(xv, k) * rstd) * get<T, VB>(wv, k);
+                o[k] = epilogue<EPI>((get<T, VB>(xv, k) * rstd) * get<T, VB>(wv, k), p.alpha);
             st_stream<VB>(dst + off, pack<T, VB>(o));
         }
     }

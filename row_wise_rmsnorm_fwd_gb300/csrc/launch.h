@@ -17,19 +17,24 @@ struct LaunchShape {
 
 // Kernel instances; nullptr when the combination is not compiled.
 // dtype: 0 = fp32, 1 = bf16.  vb = bytes per vector, nv = vectors per thread.
-// pf = register prefetch of the next row (used by the cluster split-row path).
-KernelFn rowreg_kernel_f32(int vb, int nv, bool pf);
-KernelFn rowreg_kernel_bf16(int vb, int nv, bool pf);
-KernelFn rowreg_kernel_ptr(int dtype, int vb, int nv, bool pf);
+// pf = register prefetch of the next row (used by the cluster split-row path);
+// epi = fused epilogue (kEpiNone / kEpiScale / kEpiRelu).
+KernelFn rowreg_kernel_f32_e0(int vb, int nv, bool pf);
+KernelFn rowreg_kernel_f32_e1(int vb, int nv, bool pf);
+KernelFn rowreg_kernel_f32_e2(int vb, int nv, bool pf);
+KernelFn rowreg_kernel_bf16_e0(int vb, int nv, bool pf);
+KernelFn rowreg_kernel_bf16_e1(int vb, int nv, bool pf);
+KernelFn rowreg_kernel_bf16_e2(int vb, int nv, bool pf);
+KernelFn rowreg_kernel_ptr(int dtype, int vb, int nv, bool pf, int epi);
 int rowreg_max_block(int nv);
-KernelFn twopass_kernel_ptr(int dtype, int vb);
+KernelFn twopass_kernel_ptr(int dtype, int vb, int epi);
 int twopass_block();
 // Comparison kernel with the compiler write-up's schedule (one CTA per row).
 KernelFn page_kernel_ptr(int dtype);
 int page_block();
 
 // Staged kernel: one producer warp plus 4 or 8 consumer warps.
-KernelFn staged_kernel_ptr(int dtype, int consumer_warps);
+KernelFn staged_kernel_ptr(int dtype, int consumer_warps, int epi);
 constexpr int kStagedMaxSlotsHost = 32;
 constexpr int kStagedHeaderHost = 1024;
 // Dynamic shared memory of the staged kernel: header + weight slice (0 if the

@@ -22,11 +22,19 @@ F32_ATOL = 1e-6
 BF16_MAX_ULP = 1
 
 
-def oracle_for(x_cpu: torch.Tensor, w_cpu: torch.Tensor, eps: float):
-    """Oracle output for host tensors: float64 array (fp32) or uint16 bits (bf16)."""
+def oracle_for(x_cpu: torch.Tensor, w_cpu: torch.Tensor, eps: float,
+               epilogue: str = "none", alpha: float = 1.0):
+    """Oracle output for host tensors: float64 array (fp32) or uint16 bits (bf16),
+    with the fused epilogue applied before the (single) bf16 rounding."""
     if x_cpu.dtype == torch.float32:
-        return oracle.rmsnorm_f32(x_cpu.numpy(), w_cpu.numpy(), eps)
-    _, y16 = oracle.rmsnorm_bf16(workloads.bf16_bits(x_cpu), workloads.bf16_bits(w_cpu), eps)
+        y = oracle.rmsnorm_f32(x_cpu.numpy(), w_cpu.numpy(), eps)
+        return y if epilogue == "none" else oracle.apply_epilogue(y, epilogue, alpha)
+    if epilogue == "none":
+        _, y16 = oracle.rmsnorm_bf16(workloads.bf16_bits(x_cpu), workloads.bf16_bits(w_cpu),
+                                     eps)
+        return y16
+    _, y16 = oracle.rmsnorm_epilogue_bf16(workloads.bf16_bits(x_cpu),
+                                          workloads.bf16_bits(w_cpu), eps, epilogue, alpha)
     return y16
 
 

@@ -43,8 +43,8 @@ def test_status_strings(lib):
 
 
 def test_struct_sizes_match_header():
-    # int32 x 10 + uint64 = 48 bytes; int32 x 12 + char[48] = 96 bytes
-    assert ctypes.sizeof(binding.rmsnorm_options_t) == 48
+    # int32 x 11 + float + uint64 = 56 bytes; int32 x 12 + char[48] = 96 bytes
+    assert ctypes.sizeof(binding.rmsnorm_options_t) == 56
     assert ctypes.sizeof(binding.rmsnorm_plan_t) == 96
 
 

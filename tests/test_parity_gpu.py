@@ -2,6 +2,8 @@
 element, through the C ABI (ctypes binding).  Needs a GB300 (sm_103a)."""
 from __future__ import annotations
 
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -291,3 +293,42 @@ def test_unsupported_forced_option_launches_nothing():
     assert ei.value.status == binding.RMSNORM_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert bool((y == 7.0).all())
+
+
+# --------------------------------------------------------- fused epilogue --
+
+EPI_PATHS = [("auto", {}), ("rowreg", {}), ("staged", {}), ("cluster", {"cluster": 2}),
+             ("cluster", {"cluster": 8}), ("twopass", {}), ("rowreg", {"vec_bytes": 4})]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("epi,alpha", [("scale", 0.37), ("scale", -4.0), ("relu", 1.0)])
+@pytest.mark.parametrize("path,extra", EPI_PATHS, ids=lambda v: str(v))
+def test_fused_epilogue(dtype, epi, alpha, path, extra):
+    """y = epilogue(RMSNorm(x) * w) in every kernel family, against the oracle's
+    epilogue in binary64 (bf16 rounded once, after the epilogue)."""
+    rows, hidden = (23, 4096) if path != "cluster" else (5, 16384)
+    x, w = rand_case(rows, hidden, dtype, seed=zlib.crc32(f"{epi}{path}".encode()) % 1000)
+    opts = {} if path == "auto" else {"path": path, **extra}
+    y = torch.empty(rows, hidden, dtype=DT[dtype], device="cuda")
+    binding.rmsnorm_fwd_ex(x.cuda(), w.cuda(), y, 1e-6,
+                           options={**opts, "epilogue": epi, "alpha": alpha})
+    torch.cuda.synchronize()
+    compare(y, oracle_for(x, w, 1e-6, epi, alpha), f"{epi} {path} {extra} {dtype}")
+    if epi == "relu":
+        assert bool((y >= 0).all())
+
+
+def test_epilogue_rejected_where_unsupported():
+    x = torch.ones(4, 512, device="cuda")
+    w = torch.ones(512, device="cuda")
+    with pytest.raises(binding.RmsnormError) as ei:
+        binding.rmsnorm_fwd_ex(x, w, eps=1e-6, options={"path": "page", "epilogue": "relu"})
+    assert ei.value.status == binding.RMSNORM_ERR_UNSUPPORTED
+    with pytest.raises(binding.RmsnormError) as ei:
+        binding.rmsnorm_fwd_ex(x, w, eps=1e-6, options={"epilogue": 9})
+    assert ei.value.status == binding.RMSNORM_ERR_INVALID_ARG
+    with pytest.raises(binding.RmsnormError) as ei:
+        binding.rmsnorm_fwd_ex(x, w, eps=1e-6,
+                               options={"epilogue": "scale", "alpha": float("inf")})
+    assert ei.value.status == binding.RMSNORM_ERR_INVALID_ARG
