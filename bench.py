@@ -237,7 +237,7 @@ def config_block(wl, world, args=None):
         "bytes_per_step_per_gpu": wl.bytes_per_call,
         "rows_per_step_per_gpu": wl.rows,
         "l2": "inputs larger than L2 (no flush needed)" if wl.bytes_per_call > 4 * 129e6
-              else "L2 flushed between steps",
+              else "L2 flushed between steps (read of a 258 MB buffer)",
         "parallelism": f"rows replicated per GPU x{world} (independent rows, no collective)",
     }
 
@@ -278,7 +278,10 @@ def run_ours(args, wl):
     plan = binding.rmsnorm_plan(x, w, y, options=options)
     flush = None
     if wl.bytes_per_call <= 4 * 129e6:
-        flush = torch.empty(int(2 * 129e6) // 4 + 1024, dtype=torch.float32, device=dev)
+        # read-only flush: summing a 258 MB buffer evicts x and y from L2 and
+        # leaves only clean lines (a write-based flush would leave ~129 MB of
+        # dirty lines whose write-back then competes with the next launch)
+        flush = torch.ones(int(2 * 129e6) // 4 + 1024, dtype=torch.float32, device=dev)
 
     def step():
         st = fwd(x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, hidden, wl.eps, handle)
@@ -294,7 +297,7 @@ def run_ours(args, wl):
 
     for _ in range(args.warmup):
         if flush is not None:
-            flush.fill_(1.0)
+            flush.sum()
         step()
     barrier()
 
@@ -308,7 +311,7 @@ def run_ours(args, wl):
         t_begin.record(stream)
         for i in range(args.steps):
             if flush is not None:
-                flush.fill_(1.0)   # outside the per-launch event pair
+                flush.sum()        # outside the per-launch event pair
             starts[i].record(stream)
             step()
             ends[i].record(stream)
@@ -376,8 +379,8 @@ def run_ours(args, wl):
 
 def measure_e2e(args, wl, x_dev, w_dev, y_dev, fwd, binding, world):
     """Same metric end to end: pinned host x,w -> device, the C-ABI call, device
-    y -> pinned host, every step.  The row range is split into 32 chunks run
-    on four streams so that copies in both directions overlap the kernel
+    y -> pinned host, every step.  The row range is split into 16 chunks run
+    on two streams so that copies in both directions overlap the kernel
     (measured on GB300: host<->device copies run at about 200 GB/s each way,
     so this number is bound by the host link, not by the kernel)."""
     import torch
@@ -390,9 +393,9 @@ def measure_e2e(args, wl, x_dev, w_dev, y_dev, fwd, binding, world):
     rows, hidden = wl.rows, wl.hidden
     xh2, yh2 = x_h.view(rows, hidden), y_h.view(rows, hidden)
     xd2, yd2 = x_dev.view(rows, hidden), y_dev.view(rows, hidden)
-    nchunks = 32 if rows >= 32 else 1
+    nchunks = 16 if rows >= 16 else 1
     bounds = [rows * i // nchunks for i in range(nchunks + 1)]
-    streams = [torch.cuda.Stream() for _ in range(4)]
+    streams = [torch.cuda.Stream() for _ in range(2)]
     launches = [0]
 
     def step():

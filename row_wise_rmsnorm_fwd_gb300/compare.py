@@ -11,8 +11,9 @@ torch.compile.  This runs, on the same GPU and inputs, for each workload:
   - ``eager``: torch.nn.functional.rms_norm,
   - ``compile``: torch.compile of the same call (if it compiles here).
 Timing: CUDA events around each call on the current stream after warm-up;
-workloads smaller than 4x L2 are preceded by a 258 MB write (outside the
-events) so every call reads from HBM.  GB/s counts algorithmic bytes (x read,
+workloads smaller than 4x L2 are preceded by a read of a 258 MB buffer
+(outside the events) so every call reads its inputs from HBM with no dirty
+lines left in L2.  GB/s counts algorithmic bytes (x read,
 y written, w read once).  One JSON line per (workload, implementation).
 """
 from __future__ import annotations
@@ -41,7 +42,7 @@ def _timed(fn, iters: int, flush):
     s = torch.cuda.current_stream()
     for _ in range(iters):
         if flush is not None:
-            flush.fill_(1.0)
+            flush.sum()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(s)
@@ -65,7 +66,7 @@ def run(names, iters: int):
         y = torch.empty_like(x)
         flush = None
         if wl.bytes_per_call <= 4 * L2_BYTES:
-            flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+            flush = torch.ones(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
         eps = wl.eps
         H = wl.hidden
 

@@ -44,10 +44,11 @@ cudaError_t note(cudaError_t e) {
 constexpr int kMaxDevices = 64;
 constexpr int kRowregWaves = 4;   // row-block CTAs per resident CTA slot
 constexpr int64_t kStagedChunk = 16384;   // bytes per bulk copy
-constexpr int64_t kStagedLookahead = 6;   // ring slots beyond one row slice
+constexpr int64_t kStagedLookahead = 2;   // ring slots beyond one row slice
 constexpr int kStagedConsumerWarps = 8;   // default consumer warps per CTA
 constexpr int64_t kRowregMaxRowBytes = 32768;   // auto: register-resident up to here
 constexpr int64_t kStagedMaxRowBytes = 65536;   // auto: fp32 staged up to here
+constexpr int kAutoMaxCluster = 8;              // auto: portable cluster sizes only
 
 struct DeviceInfo {
     std::once_flag once;
@@ -248,9 +249,10 @@ rmsnorm_status_t plan_rowreg(const Call& c, int cluster, Plan* P) {
 }
 
 // Bulk-copy staged kernel; needs 16-byte aligned pointers and row pitch.
-// Geometry: chunks of at most 16 KB, a ring of chunks-per-slice + 6 slots
-// (about 96 KB of copies in flight beyond the row being consumed), and the
-// weight slice in shared memory when that still fits next to the ring.
+// Geometry (measured on GB300): chunks of 16 KB (32 KB for slices of 64 KB
+// and more), a ring of chunks-per-slice + 2 slots, and the weight slice in
+// shared memory when it fits next to the ring.  Deeper rings cost occupancy
+// and measured slower.
 rmsnorm_status_t plan_staged(const Call& c, int cluster, Plan* P) {
     if (c.opt.vec_bytes != 0 && c.opt.vec_bytes != 16) return RMSNORM_ERR_UNSUPPORTED;
     if (widest_vb(c) != 16) return RMSNORM_ERR_UNSUPPORTED;
@@ -264,7 +266,8 @@ rmsnorm_status_t plan_staged(const Call& c, int cluster, Plan* P) {
     if (chunk != 0) {
         if (chunk % 16 != 0 || chunk <= 0) return RMSNORM_ERR_INVALID_ARG;
     } else {
-        chunk = slice_bytes < kStagedChunk ? slice_bytes : kStagedChunk;
+        const int64_t pref = slice_bytes >= 4 * kStagedChunk ? 2 * kStagedChunk : kStagedChunk;
+        chunk = slice_bytes < pref ? slice_bytes : pref;
     }
     int64_t nchunks = (slice_bytes + chunk - 1) / chunk;
     if (nchunks > kStagedMaxSlotsHost) {
@@ -403,8 +406,9 @@ rmsnorm_status_t plan_page(const Call& c, Plan* P) {
 }
 
 // The launch heuristics, from measurements on GB300 (profiles/kernel_choices.md):
-//  - few rows (fewer than SMs): split each row over a cluster so that about one
-//    CTA per SM works, keeping slices of at least 4 KB;
+//  - few rows (fewer than SMs): split each row over a cluster (up to the
+//    portable 8 CTAs; 16 measured no faster) so that about one CTA per SM
+//    works, keeping slices of at least 4 KB;
 //  - rows up to 32 KB: register-resident, one CTA (or warp) per row (93-101% of
 //    the measured HBM copy peak);
 //  - fp32 rows up to 64 KB: shared-memory staged by bulk copies (96%);
@@ -416,7 +420,7 @@ rmsnorm_status_t plan_auto(const Call& c, Plan* P) {
     rmsnorm_status_t st;
     if (c.rows < c.info->sms) {
         int want = pow2_floor(c.info->sms / (c.rows > 0 ? c.rows : 1));
-        if (want > 16) want = 16;
+        if (want > kAutoMaxCluster) want = kAutoMaxCluster;
         while (want > 1 && row_bytes / want < 4096) want >>= 1;
         for (int cl = want; cl <= 16; cl <<= 1) {
             st = plan_rowreg(c, cl, P);

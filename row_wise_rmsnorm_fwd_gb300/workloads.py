@@ -20,13 +20,16 @@ c3         (4, 512, 3584)           f32    N(0,1), 36 outlier columns x50     1e
 c4         (65536, 4096)            f32    N(0,1)            U(0.5,1.5)       1e-6
 c5a        (262144, 8192)           bf16   N(0,2) (std 2)    N(1,0.1)         1e-6
 c5b        (8, 262144)              bf16   N(0,2)            N(1,0.1)         1e-6
+w16k       (16384, 16384)           f32    N(0,1)            N(1,0.1)         1e-6
 w32k       (8192, 32768)            f32    N(0,1)            N(1,0.1)         1e-6
 w64k       (16384, 65536)           bf16   N(0,2)            N(1,0.1)         1e-6
 =========  =======================  =====  ================  ===============  ======
 
-c1..c5b are the measured workloads; w32k and w64k are extra wide-row cases
-(128 KiB rows, too wide to hold in one CTA's registers) used to measure the
-shared-memory staged and cluster kernels on HBM-sized inputs.
+c1..c5b are the measured workloads; w16k (64 KiB rows) and w32k, w64k
+(128 KiB rows) are extra wide-row cases, too wide for the register-resident
+kernel's sweet spot, used to measure the shared-memory staged, cluster and
+two-pass kernels on HBM-sized inputs.  MODEL_SWEEP
+adds the model-shaped batch x seq grid (see below).
 
 Readings: "N(0,2)" is mean 0, standard deviation 2; the Qwen-shaped case's
 "1% outlier channels" are round(0.01*3584) = 36 whole columns, picked by a
@@ -104,6 +107,9 @@ WORKLOADS = {
         Workload("c5b", 4, (8, 262144), "bf16", ("normal", 0.0, 2.0),
                  ("normal", 1.0, 0.1), 1e-6,
                  description="few rows, wide bf16 (8,262144)"),
+        Workload("w16k", 7, (16384, 16384), "f32", ("normal", 0.0, 1.0),
+                 ("normal", 1.0, 0.1), 1e-6,
+                 description="wide fp32 rows (16384,16384), 64 KiB per row"),
         Workload("w32k", 5, (8192, 32768), "f32", ("normal", 0.0, 1.0),
                  ("normal", 1.0, 0.1), 1e-6,
                  description="wide fp32 rows (8192,32768), 128 KiB per row"),
@@ -112,6 +118,22 @@ WORKLOADS = {
                  description="wide bf16 rows (16384,65536), 128 KiB per row"),
     ]
 }
+
+
+# Model-shaped sweep: the write-up's model blocks (TinyLlama, hidden 2048;
+# Qwen2.5-7B, hidden 3584) at its two sequence lengths (128 and 512) over a
+# range of batch sizes; rows = batch * seq.  fp32 as on the page, N(0,1)
+# activations, N(1,0.1) weights, eps 1e-5 (TinyLlama) / 1e-6 (Qwen).
+MODEL_SWEEP = {}
+for _model, _hidden, _eps in (("tinyllama", 2048, 1e-5), ("qwen7b", 3584, 1e-6)):
+    for _seq in (128, 512):
+        for _batch in (1, 4, 16, 64):
+            _name = f"{_model}_b{_batch}_s{_seq}"
+            MODEL_SWEEP[_name] = Workload(
+                _name, 10 + len(MODEL_SWEEP), (_batch, _seq, _hidden), "f32",
+                ("normal", 0.0, 1.0), ("normal", 1.0, 0.1), _eps,
+                description=f"{_model}-shaped (batch {_batch}, seq {_seq}, hidden {_hidden})")
+WORKLOADS.update(MODEL_SWEEP)
 
 
 def _torch_dtype(dtype: str):
