@@ -45,7 +45,8 @@ constexpr int kMaxDevices = 64;
 constexpr int kRowregWaves = 4;   // row-block CTAs per resident CTA slot
 constexpr int64_t kStagedChunk = 16384;   // bytes per bulk copy
 constexpr int64_t kStagedLookahead = 2;   // ring slots beyond one row slice
-constexpr int kStagedConsumerWarps = 8;   // default consumer warps per CTA
+constexpr int kStagedConsumerWarps = 8;       // default consumer warps per CTA (fp32)
+constexpr int kStagedConsumerWarpsBf16 = 4;   // default consumer warps per CTA (bf16)
 constexpr int64_t kRowregMaxRowBytes = 32768;   // auto: register-resident up to here
 constexpr int64_t kStagedMaxRowBytes = 65536;   // auto: fp32 staged up to here
 constexpr int kAutoMaxCluster = 8;              // auto: portable cluster sizes only
@@ -299,8 +300,9 @@ rmsnorm_status_t plan_staged(const Call& c, int cluster, Plan* P) {
     if (c.opt.stages > 0 && slots != c.opt.stages) return RMSNORM_ERR_UNSUPPORTED;
     const int64_t smem = staged_smem_bytes(chunk, static_cast<int>(slots), wres);
     if (smem <= 0 || smem > budget) return RMSNORM_ERR_UNSUPPORTED;
-    // Consumer warps: forced through `threads` (128 or 256), else 8.
-    int ncw = kStagedConsumerWarps;
+    // Consumer warps: forced through `threads` (128 or 256), else 8 for fp32
+    // and 4 for bf16 (measured: bf16 CTAs of 9 warps lose occupancy).
+    int ncw = c.dtype == RMSNORM_DTYPE_BF16 ? kStagedConsumerWarpsBf16 : kStagedConsumerWarps;
     if (c.opt.threads != 0) {
         if (c.opt.threads != 128 && c.opt.threads != 256) return RMSNORM_ERR_UNSUPPORTED;
         ncw = c.opt.threads / 32;
