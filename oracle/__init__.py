@@ -1,4 +1,4 @@
-"""CPU oracle for the row-wise RMSNorm forward pass.
+"""CPU oracle for the row-wise RMSNorm forward pass (and row-wise softmax).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline legs of ``bench.py`` may import this package.  The CUDA library
@@ -27,6 +27,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "rmsnorm_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "rowsoftmax_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle_rmsnorm.so")
 
@@ -38,11 +39,11 @@ def build(force: bool = False) -> str:
     """Compile the C oracle into ``oracle/_build/liboracle_rmsnorm.so``."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(s) for s in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
-           "-ffp-contract=off", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+           "-ffp-contract=off", "-Wall", "-Wextra", "-o", tmp, *_SRCS, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -61,6 +62,11 @@ def _load():
         lib.oracle_rmsnorm_bf16.argtypes = [vp, vp, vp, vp, i64, i64, dbl]
         lib.oracle_rmsnorm_stats_f64.argtypes = [vp, vp, vp, i64, i64, dbl]
         lib.oracle_apply_epilogue_f64.argtypes = [vp, i64, ctypes.c_int, dbl]
+        lib.oracle_rowsoftmax_f64.argtypes = [vp, vp, i64, i64]
+        lib.oracle_rowsoftmax_f32.argtypes = [vp, vp, i64, i64]
+        lib.oracle_rowsoftmax_bf16.argtypes = [vp, vp, vp, i64, i64]
+        for f in ("oracle_rowsoftmax_f64", "oracle_rowsoftmax_f32", "oracle_rowsoftmax_bf16"):
+            getattr(lib, f).restype = ctypes.c_int
         lib.oracle_f64_to_bf16_array.argtypes = [vp, vp, i64]
         for f in ("oracle_rmsnorm_f64", "oracle_rmsnorm_f32",
                   "oracle_rmsnorm_bf16", "oracle_rmsnorm_stats_f64",
@@ -178,6 +184,49 @@ def rmsnorm_epilogue_bf16(x_bits, w_bits, eps: float, kind, alpha=1.0):
     y64, _ = rmsnorm_bf16(x_bits, w_bits, eps)
     e64 = apply_epilogue(y64, kind, alpha)
     return e64, f64_to_bf16_fast(e64)
+
+
+# ------------------------------------------------------------ row softmax --
+# Plain definition (the write-up names softmax-style small reductions but
+# prints no formula): y = exp(x - max) / sum exp(x - max) per row, binary64.
+
+def _rows_cols(x: np.ndarray):
+    if x.ndim < 1 or x.shape[-1] == 0:
+        raise ValueError("x needs a non-empty last dimension")
+    cols = x.shape[-1]
+    rows = int(np.prod(x.shape[:-1], dtype=np.int64)) if x.ndim > 1 else 1
+    return rows, cols
+
+
+def rowsoftmax_f64(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    rows, cols = _rows_cols(x)
+    y = np.empty_like(x)
+    _check(_load().oracle_rowsoftmax_f64(_ptr(x), _ptr(y), rows, cols))
+    return y
+
+
+def rowsoftmax_f32(x: np.ndarray) -> np.ndarray:
+    """binary32 input (widened exactly), binary64 result."""
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.float32:
+        raise TypeError("rowsoftmax_f32 takes float32")
+    rows, cols = _rows_cols(x)
+    y = np.empty(x.shape, dtype=np.float64)
+    _check(_load().oracle_rowsoftmax_f32(_ptr(x), _ptr(y), rows, cols))
+    return y
+
+
+def rowsoftmax_bf16(x_bits: np.ndarray):
+    """bfloat16 bits in; returns (y64, y16) with y16 the single RNE rounding."""
+    x_bits = np.ascontiguousarray(x_bits)
+    if x_bits.dtype != np.uint16:
+        raise TypeError("rowsoftmax_bf16 takes uint16 bit patterns")
+    rows, cols = _rows_cols(x_bits)
+    y64 = np.empty(x_bits.shape, dtype=np.float64)
+    y16 = np.empty(x_bits.shape, dtype=np.uint16)
+    _check(_load().oracle_rowsoftmax_bf16(_ptr(x_bits), _ptr(y64), _ptr(y16), rows, cols))
+    return y64, y16
 
 
 def bf16_to_f64(bits) -> np.ndarray:

@@ -18,6 +18,7 @@ from test_oracle_pins import GOLDEN, _eval_closed_form
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                    "oracle", "rmsnorm_oracle.c")
+SOFTMAX_SRC = os.path.join(os.path.dirname(SRC), "rowsoftmax_oracle.c")
 
 MUTANTS = {
     "unmodified": None,
@@ -106,3 +107,63 @@ def test_pins_reject_mutant(tmp_path, name):
         assert _pins_pass(lib)
     else:
         assert not _pins_pass(lib), f"pins did not catch mutant {name}"
+
+
+# ---------------------------------------------------------- row softmax --
+
+SOFTMAX_MUTANTS = {
+    "unmodified": None,
+    "no_max_shift": ("y[j] = exp(x[j] - m);", "y[j] = exp(x[j]);"),
+    "min_not_max": ("if (x[j] > m) m = x[j];", "if (x[j] < m) m = x[j];"),
+    "divide_by_count": ("for (int64_t j = 0; j < cols; ++j) y[j] = y[j] / s;",
+                        "for (int64_t j = 0; j < cols; ++j) y[j] = y[j] / (double)cols;"),
+    "first_element_skipped": ("    double s = 0.0;\n    for (int64_t j = 0; j < cols; ++j) {",
+                              "    double s = 0.0;\n    for (int64_t j = 1; j < cols; ++j) {"),
+}
+
+
+def _build_softmax(tmp_path, name, mutation):
+    src = open(SOFTMAX_SRC).read()
+    if mutation is not None:
+        old, new = mutation
+        assert src.count(old) >= 1, f"mutation site for {name} not found"
+        src = src.replace(old, new)
+    c = tmp_path / f"sm_{name}.c"
+    c.write_text(src)
+    so = tmp_path / f"libsm_{name}.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-o", str(so), SRC, str(c), "-lm"], check=True)
+    lib = ctypes.CDLL(str(so))
+    lib.oracle_rowsoftmax_f64.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_int64, ctypes.c_int64]
+    return lib
+
+
+def _softmax_pins_pass(lib) -> bool:
+    import math
+
+    def sm(rows):
+        x = np.ascontiguousarray(rows, dtype=np.float64)
+        y = np.empty_like(x)
+        lib.oracle_rowsoftmax_f64(x.ctypes.data, y.ctypes.data, x.shape[0], x.shape[1])
+        return y
+    with np.errstate(all="ignore"):
+        y = sm([[0.0, math.log(3.0), math.log(6.0)]])
+        if not np.allclose(y[0], [0.1, 0.3, 0.6], rtol=4e-16, atol=0):
+            return False
+        y = sm([[1000.0, 1001.0]])
+        e = math.e
+        if not np.allclose(y[0], [1 / (1 + e), e / (1 + e)], rtol=1e-15, atol=0):
+            return False
+        y = sm([[0.0, 800.0]])
+        return bool(y[0, 0] == 0.0 and y[0, 1] == 1.0)
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+@pytest.mark.parametrize("name", sorted(SOFTMAX_MUTANTS))
+def test_softmax_pins_reject_mutant(tmp_path, name):
+    lib = _build_softmax(tmp_path, name, SOFTMAX_MUTANTS[name])
+    if name == "unmodified":
+        assert _softmax_pins_pass(lib)
+    else:
+        assert not _softmax_pins_pass(lib), f"pins did not catch mutant {name}"
