@@ -29,6 +29,7 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "RMSNorm GB/s and rows/s on 1 GB300; % of HBM roofline"
+METRIC_SOFTMAX = "row softmax GB/s and rows/s on 1 GB300; % of HBM roofline"
 
 
 # ------------------------------------------------------------------ helpers --
@@ -157,25 +158,33 @@ def cpu_oracle_sample(wl, budget_s: float = 10.0, chunk_rows: int = 2048, max_ch
     from row_wise_rmsnorm_fwd_gb300 import workloads
 
     oracle.build()
-    w = workloads.make_w(wl)
+    softmax = wl.op == "softmax"
+    w = None if softmax else workloads.make_w(wl)
     chunk_rows = min(chunk_rows, wl.rows)
     done_rows, elapsed, k = 0, 0.0, 0
-    if wl.dtype == "bf16":
+    if wl.dtype == "bf16" and not softmax:
         wb = workloads.bf16_bits(w)
     while elapsed < budget_s and k < max_chunks:
         x = workloads.make_x(wl, rows=chunk_rows, seed_offset=k)
         if wl.dtype == "bf16":
             xb = workloads.bf16_bits(x)
             t0 = time.perf_counter()
-            oracle.rmsnorm_bf16(xb, wb, wl.eps)
+            if softmax:
+                oracle.rowsoftmax_bf16(xb)
+            else:
+                oracle.rmsnorm_bf16(xb, wb, wl.eps)
         else:
-            xn, wn = x.numpy(), w.numpy()
+            xn = x.numpy()
             t0 = time.perf_counter()
-            oracle.rmsnorm_f32(xn, wn, wl.eps)
+            if softmax:
+                oracle.rowsoftmax_f32(xn)
+            else:
+                oracle.rmsnorm_f32(xn, w.numpy(), wl.eps)
         elapsed += time.perf_counter() - t0
         done_rows += chunk_rows
         k += 1
-    bytes_done = (2 * done_rows * wl.hidden) * wl.elem_bytes + wl.hidden * wl.elem_bytes
+    bytes_done = (2 * done_rows * wl.hidden) * wl.elem_bytes + \
+        (0 if softmax else wl.hidden * wl.elem_bytes)
     return {
         "value": bytes_done / elapsed / 1e9,
         "unit": "GB/s",
@@ -205,7 +214,8 @@ def run_reference(args, wl):
     value = total_bytes / total_s
     line = {
         "impl": "reference",
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "metric": METRIC_SOFTMAX if wl.op == "softmax" else METRIC, "value": value,
+        "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -259,13 +269,21 @@ def run_ours(args, wl):
     from row_wise_rmsnorm_fwd_gb300 import binding, workloads
 
     x = workloads.make_x(wl, device="cuda")
-    w = workloads.make_w(wl, device="cuda")
+    softmax = wl.op == "softmax"
+    w = torch.empty(0, device="cuda") if softmax else workloads.make_w(wl, device="cuda")
     y = torch.empty_like(x)
     rows, hidden = wl.rows, wl.hidden
     stream = torch.cuda.current_stream()
     handle = stream.cuda_stream
     options = None
-    if forced(args):
+    if softmax:
+        options = binding.make_options(path=args.path if args.path in ("rowreg", "twopass")
+                                       else "auto", grid=args.grid, threads=args.threads)
+        dt_code = binding.RMSNORM_DTYPE_BF16 if wl.dtype == "bf16" else binding.RMSNORM_DTYPE_F32
+
+        def fwd(xp, wp, yp, r, h, eps, s):
+            return binding.raw.rowsoftmax_fwd_ex(dt_code, xp, yp, r, h, options, s)
+    elif forced(args):
         options = binding.make_options(path=args.path, cluster=args.cluster, grid=args.grid,
                                        threads=args.threads, chunk_bytes=args.chunk,
                                        epilogue=args.epilogue, alpha=0.5)
@@ -275,7 +293,8 @@ def run_ours(args, wl):
             return binding.raw.rmsnorm_fwd_ex(dt_code, xp, wp, yp, r, h, eps, options, s)
     else:
         fwd = binding.raw.rmsnorm_fwd_bf16 if wl.dtype == "bf16" else binding.raw.rmsnorm_fwd_f32
-    plan = binding.rmsnorm_plan(x, w, y, options=options)
+    plan = (binding.rowsoftmax_plan(x, y, options=options) if softmax
+            else binding.rmsnorm_plan(x, w, y, options=options))
     flush = None
     if wl.bytes_per_call <= 4 * 129e6:
         # read-only flush: summing a 258 MB buffer evicts x and y from L2 and
@@ -349,7 +368,8 @@ def run_ours(args, wl):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "metric": METRIC_SOFTMAX if softmax else METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic", "config": config_block(wl, world, args),
@@ -389,6 +409,7 @@ def measure_e2e(args, wl, x_dev, w_dev, y_dev, fwd, binding, world):
     x_h = torch.empty(wl.shape, dtype=dt, pin_memory=True)
     x_h.copy_(x_dev.cpu())
     w_h = w_dev.cpu().pin_memory()
+    w_bytes = w_dev.numel() * wl.elem_bytes
     y_h = torch.empty(wl.shape, dtype=dt, pin_memory=True)
     rows, hidden = wl.rows, wl.hidden
     xh2, yh2 = x_h.view(rows, hidden), y_h.view(rows, hidden)
@@ -402,7 +423,8 @@ def measure_e2e(args, wl, x_dev, w_dev, y_dev, fwd, binding, world):
         ev_w = torch.cuda.Event()
         s0 = streams[0]
         with torch.cuda.stream(s0):
-            w_dev.copy_(w_h, non_blocking=True)
+            if w_dev.numel():
+                w_dev.copy_(w_h, non_blocking=True)
             ev_w.record(s0)
         for i in range(nchunks):
             s = streams[i % len(streams)]
@@ -437,7 +459,7 @@ def measure_e2e(args, wl, x_dev, w_dev, y_dev, fwd, binding, world):
     if not torch.equal(yh2[-1].to(y_dev.device), yd2[-1]):
         raise RuntimeError("end-to-end copy-back mismatch")
     return {"value": world * wl.bytes_per_call * n / dt_s / 1e9, "unit": "GB/s",
-            "h2d_bytes_per_step": (rows * hidden + hidden) * wl.elem_bytes,
+            "h2d_bytes_per_step": rows * hidden * wl.elem_bytes + w_bytes,
             "d2h_bytes_per_step": rows * hidden * wl.elem_bytes,
             "steps": n, "ms_per_step": 1e3 * dt_s / n, "chunks_per_step": nchunks,
             "streams": len(streams), "gpu_launches": launches[0], "timing": "host wall clock"}

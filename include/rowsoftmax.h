@@ -1,0 +1,61 @@
+/*
+ * rowsoftmax.h -- C ABI of librmsnorm's row-wise softmax (same library,
+ * same status codes and conventions as rmsnorm.h).
+ *
+ * For every row r of a row-major matrix x with `cols` columns:
+ *
+ *     m[r]   = max_j x[r,j]
+ *     y[r,j] = exp(x[r,j] - m[r]) / sum_k exp(x[r,k] - m[r])
+ *
+ * The compiler write-up "A hackable Python ML compiler, part 2" lists such
+ * small reductions (softmax inside SDPA) among the ops its generated kernels
+ * win on, without printing a formula; this is the plain definition in the
+ * stable form.  fp32 arithmetic (CUDA expf); bf16 inputs are widened exactly
+ * and each output is rounded once.  IEEE semantics for special values: -inf
+ * entries give 0; a row of -inf, or any NaN or +inf in a row, gives a NaN row.
+ *
+ *  - x, y: DEVICE pointers owned by the caller, rows*cols elements, contiguous
+ *    row-major; y == x (in place) is allowed, any other overlap is rejected.
+ *  - rows >= 0 (0: OK, no launch); 1 <= cols <= 2^31-1.
+ *  - Asynchronous on `stream`; allocates nothing; argument errors are found on
+ *    the host before any launch (RMSNORM_ERR_INVALID_ARG); a failed CUDA call
+ *    returns RMSNORM_ERR_CUDA (see rmsnorm_last_cuda_error).
+ */
+#ifndef ROWSOFTMAX_H_
+#define ROWSOFTMAX_H_
+
+#include "rmsnorm.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* y = softmax(x) along the last axis, fp32 tensors. */
+rmsnorm_status_t rowsoftmax_fwd_f32(const float* x, float* y, int64_t rows, int64_t cols,
+                                    rmsnorm_stream_t stream);
+
+/* The same for bfloat16 tensors (raw 16-bit patterns), fp32 arithmetic. */
+rmsnorm_status_t rowsoftmax_fwd_bf16(const uint16_t* x, uint16_t* y, int64_t rows,
+                                     int64_t cols, rmsnorm_stream_t stream);
+
+/*
+ * Either dtype with options: opt->path may be RMSNORM_PATH_AUTO,
+ * RMSNORM_PATH_ROWREG (row held in registers; rows up to 64 KiB) or
+ * RMSNORM_PATH_TWOPASS (the wide-row kernel: reads each row three times, the
+ * repeats normally from L2); opt->threads, opt->grid and opt->vec_bytes as
+ * for rmsnorm_fwd_ex.  Other option fields must be zero.  `opt` may be NULL.
+ */
+rmsnorm_status_t rowsoftmax_fwd_ex(int32_t dtype, const void* x, void* y, int64_t rows,
+                                   int64_t cols, const rmsnorm_options_t* opt,
+                                   rmsnorm_stream_t stream);
+
+/* What rowsoftmax_fwd_ex would launch (no launch); see rmsnorm_plan. */
+rmsnorm_status_t rowsoftmax_plan(int32_t dtype, const void* x, const void* y, int64_t rows,
+                                 int64_t cols, const rmsnorm_options_t* opt,
+                                 rmsnorm_plan_t* plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROWSOFTMAX_H_ */

@@ -1,4 +1,4 @@
-"""librmsnorm: fused row-wise RMSNorm forward for NVIDIA GB300 (sm_103a).
+"""librmsnorm: fused row-wise RMSNorm forward (and row softmax) for NVIDIA GB300.
 
 ``y[r, j] = (x[r, j] * rsqrt(mean_j x[r, j]^2 + eps)) * w[j]`` computed by
 hand-written CUDA kernels behind a C ABI (``include/rmsnorm.h``).  This package
@@ -11,7 +11,8 @@ can be used without the compiled library.
 _BINDING_NAMES = {
     "rmsnorm_fwd_f32", "rmsnorm_fwd_bf16", "rmsnorm_fwd_ex", "rmsnorm_plan",
     "rmsnorm_last_device_status", "rmsnorm_status_string", "rmsnorm_abi_version",
-    "rmsnorm_last_cuda_error",
+    "rmsnorm_last_cuda_error", "rowsoftmax_fwd_f32", "rowsoftmax_fwd_bf16",
+    "rowsoftmax_fwd_ex", "rowsoftmax_plan",
     "make_options", "RmsnormError", "raw", "load",
 }
 

@@ -99,6 +99,16 @@ def open_library(path: str):
     lib.rmsnorm_fault_injection_enabled.restype = ctypes.c_int32
     lib.rmsnorm_abi_version.argtypes = []
     lib.rmsnorm_abi_version.restype = ctypes.c_int32
+    for name in ("rowsoftmax_fwd_f32", "rowsoftmax_fwd_bf16"):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, vp, i64, i64, vp]
+        fn.restype = ctypes.c_int
+    lib.rowsoftmax_fwd_ex.argtypes = [i32, vp, vp, i64, i64, ctypes.POINTER(rmsnorm_options_t),
+                                      vp]
+    lib.rowsoftmax_fwd_ex.restype = ctypes.c_int
+    lib.rowsoftmax_plan.argtypes = [i32, vp, vp, i64, i64, ctypes.POINTER(rmsnorm_options_t),
+                                    ctypes.POINTER(rmsnorm_plan_t)]
+    lib.rowsoftmax_plan.restype = ctypes.c_int
     return lib
 
 
@@ -121,7 +131,7 @@ def declared_functions() -> list[str]:
         text = open(os.path.join(inc, fname)).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
-        for m in re.finditer(r"\b(rmsnorm_[a-z0-9_]+)\s*\(", text):
+        for m in re.finditer(r"\b((?:rmsnorm|rowsoftmax)_[a-z0-9_]+)\s*\(", text):
             if m.group(1) not in names:
                 names.append(m.group(1))
     return names
@@ -169,8 +179,23 @@ def _raw_plan(dtype, x, w, y, rows, hidden, options=None):
     return st, plan
 
 
+def _raw_sm_f32(x, y, rows, cols, stream=0) -> int:
+    return load().rowsoftmax_fwd_f32(x, y, rows, cols, stream or None)
+
+
+def _raw_sm_bf16(x, y, rows, cols, stream=0) -> int:
+    return load().rowsoftmax_fwd_bf16(x, y, rows, cols, stream or None)
+
+
+def _raw_sm_ex(dtype, x, y, rows, cols, options=None, stream=0) -> int:
+    opt = ctypes.byref(options) if options is not None else None
+    return load().rowsoftmax_fwd_ex(dtype, x, y, rows, cols, opt, stream or None)
+
+
 raw = SimpleNamespace(rmsnorm_fwd_f32=_raw_fwd_f32, rmsnorm_fwd_bf16=_raw_fwd_bf16,
-                      rmsnorm_fwd_ex=_raw_fwd_ex, rmsnorm_plan=_raw_plan)
+                      rmsnorm_fwd_ex=_raw_fwd_ex, rmsnorm_plan=_raw_plan,
+                      rowsoftmax_fwd_f32=_raw_sm_f32, rowsoftmax_fwd_bf16=_raw_sm_bf16,
+                      rowsoftmax_fwd_ex=_raw_sm_ex)
 
 
 # ------------------------------------------------------------------ tensors --
@@ -264,6 +289,77 @@ def rmsnorm_plan(x, w, y=None, options=None) -> dict:
     st, plan = _raw_plan(dtype, x.data_ptr(), w.data_ptr(), y_ptr, rows, hidden, options)
     if st != RMSNORM_OK:
         raise RmsnormError(st, "rmsnorm_plan")
+    d = {f: getattr(plan, f) for f, _ in rmsnorm_plan_t._fields_ if f != "kernel"}
+    d["kernel"] = plan.kernel.decode()
+    d["path_name"] = PATH_NAMES.get(plan.path, "?")
+    return d
+
+
+# -------------------------------------------------------------- row softmax --
+
+def _check_sm(x, y):
+    torch = _torch()
+    if x.dtype not in (torch.float32, torch.bfloat16) or y.dtype != x.dtype:
+        raise TypeError("x and y must both be float32 or both bfloat16")
+    for name, t in (("x", x), ("y", y)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if y.shape != x.shape or x.dim() == 0 or x.shape[-1] == 0:
+        raise ValueError("x and y must share a shape with a non-empty last dim")
+    cols = x.shape[-1]
+    return x.numel() // cols, cols
+
+
+def rowsoftmax_fwd_f32(x, y=None, stream=None):
+    """y = softmax(x) along the last dim, float32 CUDA tensors."""
+    if y is None:
+        y = _torch().empty_like(x)
+    rows, cols = _check_sm(x, y)
+    st = _raw_sm_f32(x.data_ptr(), y.data_ptr(), rows, cols, _stream_handle(stream))
+    if st != RMSNORM_OK:
+        raise RmsnormError(st, "rowsoftmax_fwd_f32")
+    return y
+
+
+def rowsoftmax_fwd_bf16(x, y=None, stream=None):
+    """y = softmax(x) along the last dim, bfloat16 CUDA tensors (fp32 math)."""
+    if y is None:
+        y = _torch().empty_like(x)
+    rows, cols = _check_sm(x, y)
+    st = _raw_sm_bf16(x.data_ptr(), y.data_ptr(), rows, cols, _stream_handle(stream))
+    if st != RMSNORM_OK:
+        raise RmsnormError(st, "rowsoftmax_fwd_bf16")
+    return y
+
+
+def rowsoftmax_fwd_ex(x, y=None, options=None, stream=None):
+    """Either dtype with options (path auto / rowreg / twopass, threads, grid)."""
+    torch = _torch()
+    if y is None:
+        y = torch.empty_like(x)
+    rows, cols = _check_sm(x, y)
+    if isinstance(options, dict):
+        options = make_options(**options)
+    dt = RMSNORM_DTYPE_F32 if x.dtype == torch.float32 else RMSNORM_DTYPE_BF16
+    st = _raw_sm_ex(dt, x.data_ptr(), y.data_ptr(), rows, cols, options, _stream_handle(stream))
+    if st != RMSNORM_OK:
+        raise RmsnormError(st, "rowsoftmax_fwd_ex")
+    return y
+
+
+def rowsoftmax_plan(x, y=None, options=None) -> dict:
+    torch = _torch()
+    if isinstance(options, dict):
+        options = make_options(**options)
+    cols = x.shape[-1]
+    rows = x.numel() // cols
+    dt = RMSNORM_DTYPE_F32 if x.dtype == torch.float32 else RMSNORM_DTYPE_BF16
+    plan = rmsnorm_plan_t()
+    opt = ctypes.byref(options) if options is not None else None
+    st = load().rowsoftmax_plan(dt, x.data_ptr(), (y if y is not None else x).data_ptr(),
+                                rows, cols, opt, ctypes.byref(plan))
+    if st != RMSNORM_OK:
+        raise RmsnormError(st, "rowsoftmax_plan")
     d = {f: getattr(plan, f) for f, _ in rmsnorm_plan_t._fields_ if f != "kernel"}
     d["kernel"] = plan.kernel.decode()
     d["path_name"] = PATH_NAMES.get(plan.path, "?")

@@ -4,7 +4,8 @@
                                                  [--iters 50] [--out FILE]
 
 The compiler write-up measures its generated kernels against PyTorch eager and
-torch.compile.  This runs, on the same GPU and inputs, for each workload:
+torch.compile.  This runs, on the same GPU and inputs, for each workload
+(row-softmax workloads compare ours with torch.softmax eager and compiled):
   - ``ours``: librmsnorm's automatic choice (rmsnorm_fwd_f32 / _bf16),
   - ``page``: librmsnorm's rebuild of the write-up's own kernel schedule
     (RMSNORM_PATH_PAGE: one CTA per row, smem staging, scalar accesses),
@@ -62,7 +63,8 @@ def run(names, iters: int):
         wl = workloads.WORKLOADS[name]
         dev = "cuda"
         x = workloads.make_x(wl, device=dev).reshape(-1, wl.hidden)
-        w = workloads.make_w(wl, device=dev)
+        softmax = wl.op == "softmax"
+        w = None if softmax else workloads.make_w(wl, device=dev)
         y = torch.empty_like(x)
         flush = None
         if wl.bytes_per_call <= 4 * L2_BYTES:
@@ -71,17 +73,25 @@ def run(names, iters: int):
         H = wl.hidden
 
         def ours():
-            binding.rmsnorm_fwd_ex(x, w, y, eps)
+            if softmax:
+                binding.rowsoftmax_fwd_ex(x, y)
+            else:
+                binding.rmsnorm_fwd_ex(x, w, y, eps)
 
         def page():
             binding.rmsnorm_fwd_ex(x, w, y, eps, options={"path": "page"})
 
         def eager():
+            if softmax:
+                return torch.softmax(x, -1)
             return torch.nn.functional.rms_norm(x, (H,), w, eps)
 
-        impls = [("ours", ours), ("page", page), ("eager", eager)]
+        impls = [("ours", ours), ("eager", eager)] if softmax else \
+            [("ours", ours), ("page", page), ("eager", eager)]
         try:
-            compiled = torch.compile(lambda t: torch.nn.functional.rms_norm(t, (H,), w, eps))
+            compiled = torch.compile(
+                (lambda t: torch.softmax(t, -1)) if softmax
+                else (lambda t: torch.nn.functional.rms_norm(t, (H,), w, eps)))
             compiled(x)
             impls.append(("compile", lambda: compiled(x)))
         except Exception as e:  # noqa: BLE001 -- report, do not fail the comparison

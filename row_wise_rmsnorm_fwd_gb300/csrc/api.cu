@@ -5,6 +5,7 @@
 // y[r,j] = (x[r,j] * rsqrt(mean_j x[r,j]^2 + eps)) * w[j].
 #include "rmsnorm.h"
 #include "launch.h"
+#include "device.h"
 
 #include <cmath>
 #include <cstdio>
@@ -12,10 +13,6 @@
 #include <map>
 #include <mutex>
 #include <tuple>
-
-// The device status word: written only by a kernel whose bounded wait
-// expired; read and cleared by rmsnorm_last_device_status.
-__device__ unsigned g_rmsnorm_status = 0u;
 
 namespace rmsnorm {
 
@@ -33,16 +30,7 @@ namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s
 
-// The CUDA runtime is linked statically, so its error state is private to
-// this library; the last failing call's error is kept per host thread.
-thread_local cudaError_t t_last_cuda_error = cudaSuccess;
-
-cudaError_t note(cudaError_t e) {
-    if (e != cudaSuccess) t_last_cuda_error = e;
-    return e;
-}
-constexpr int kMaxDevices = 64;
-constexpr int kRowregWaves = 4;   // row-block CTAs per resident CTA slot
+constexpr int kRowregWaves = 16;   // row-block CTAs per resident CTA slot
 constexpr int64_t kStagedChunk = 16384;   // bytes per bulk copy
 constexpr int64_t kStagedLookahead = 2;   // ring slots beyond one row slice
 constexpr int kStagedConsumerWarps = 8;       // default consumer warps per CTA (fp32)
@@ -50,80 +38,6 @@ constexpr int kStagedConsumerWarpsBf16 = 4;   // default consumer warps per CTA 
 constexpr int64_t kRowregMaxRowBytes = 32768;   // auto: register-resident up to here
 constexpr int64_t kStagedMaxRowBytes = 65536;   // auto: fp32 staged up to here
 constexpr int kAutoMaxCluster = 8;              // auto: portable cluster sizes only
-
-struct DeviceInfo {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
-    int sms = 0;
-    int smem_optin = 0;
-    unsigned* status = nullptr;
-};
-DeviceInfo g_dev[kMaxDevices];
-
-cudaError_t init_device(DeviceInfo& d, int dev) {
-    cudaError_t e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e == cudaSuccess)
-        e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_rmsnorm_status);
-    return e;
-}
-
-cudaError_t current_device(DeviceInfo** out, int* dev_out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return note(e);
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    DeviceInfo& d = g_dev[dev];
-    std::call_once(d.once, [&] { d.err = init_device(d, dev); });
-    *out = &d;
-    if (dev_out) *dev_out = dev;
-    return note(d.err);
-}
-
-// Kernels are prepared once per device; occupancy answers are cached per
-// (device, kernel, block, smem, cluster).
-std::mutex g_occ_mu;
-std::map<std::tuple<int, KernelFn, int, int, int>, int> g_occ;
-std::map<std::pair<int, KernelFn>, cudaError_t> g_prepared;
-
-cudaError_t ensure_prepared(int dev, KernelFn fn, int smem_limit) {
-    std::lock_guard<std::mutex> lk(g_occ_mu);
-    const auto key = std::make_pair(dev, fn);
-    auto it = g_prepared.find(key);
-    if (it != g_prepared.end()) return it->second;
-    const cudaError_t e = prepare_kernel(fn, smem_limit);
-    g_prepared[key] = e;
-    return note(e);
-}
-
-cudaError_t cached_occupancy(int dev, KernelFn fn, int block, int smem, int cluster, int* out) {
-    const auto key = std::make_tuple(dev, fn, block, smem, cluster);
-    {
-        std::lock_guard<std::mutex> lk(g_occ_mu);
-        auto it = g_occ.find(key);
-        if (it != g_occ.end()) { *out = it->second; return cudaSuccess; }
-    }
-    int v = 0;
-    cudaError_t e = ensure_prepared(dev, fn, g_dev[dev].smem_optin);
-    if (e == cudaSuccess) {
-        if (cluster > 1) {
-            e = max_active_clusters(fn, block, smem, cluster, &v);
-        } else {
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &v, reinterpret_cast<const void*>(fn), block, static_cast<size_t>(smem));
-        }
-    }
-    if (e != cudaSuccess) {
-        // A cluster shape the device cannot run is "zero clusters", not an error.
-        if (cluster > 1) { cudaGetLastError(); v = 0; e = cudaSuccess; }
-        else return note(e);
-    }
-    std::lock_guard<std::mutex> lk(g_occ_mu);
-    g_occ[key] = v;
-    *out = v;
-    return cudaSuccess;
-}
 
 struct Call {
     int dtype;
@@ -133,7 +47,8 @@ struct Call {
     int64_t hidden;
     rmsnorm_options_t opt;
     int dev;
-    DeviceInfo* info;
+    const DeviceView* info;
+    DeviceView view;
 };
 
 struct Plan {
@@ -216,14 +131,16 @@ rmsnorm_status_t plan_rowreg(const Call& c, int cluster, Plan* P) {
     const int rpc = cluster == 1 ? (G >= 256 ? 1 : 256 / G) : 1;
     const int block = G * rpc;
     int occ = 0;
-    if (cached_occupancy(c.dev, fn, block, 0, cluster, &occ) != cudaSuccess)
+    if (cached_occupancy(c.dev, c.info->smem_optin, fn, block, 0, cluster, &occ) != cudaSuccess)
         return RMSNORM_ERR_CUDA;
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
     int grid;
     if (cluster == 1) {
-        // Grid-stride over row blocks with about four waves of resident CTAs:
-        // measured on GB300 to keep HBM busier than exactly one resident wave
-        // (CTAs fall out of phase, so loads, reductions and stores overlap).
+        // Grid-stride over row blocks with about sixteen waves of resident CTAs:
+        // measured on GB300 to keep HBM busier than one resident wave (CTAs
+        // fall out of phase, so loads, reductions and stores overlap): on c4
+        // and c5a 1 wave gives 98%, 4 waves 98.5-100%, 16 waves 99-102% of
+        // the measured copy peak.
         const int64_t nblocks = (c.rows + rpc - 1) / rpc;
         const int64_t target = static_cast<int64_t>(c.info->sms) * occ * kRowregWaves;
         grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
@@ -311,7 +228,7 @@ rmsnorm_status_t plan_staged(const Call& c, int cluster, Plan* P) {
     KernelFn fn = staged_kernel_ptr(c.dtype, ncw, c.opt.epilogue);
     if (!fn) return RMSNORM_ERR_UNSUPPORTED;
     int occ = 0;
-    if (cached_occupancy(c.dev, fn, block, static_cast<int>(smem), cluster, &occ) !=
+    if (cached_occupancy(c.dev, c.info->smem_optin, fn, block, static_cast<int>(smem), cluster, &occ) !=
         cudaSuccess)
         return RMSNORM_ERR_CUDA;
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
@@ -358,7 +275,7 @@ rmsnorm_status_t plan_twopass(const Call& c, Plan* P) {
                                                              : round_up(nvec, 32));
     if (block % 32 != 0 || block > twopass_block()) return RMSNORM_ERR_INVALID_ARG;
     int occ = 0;
-    if (cached_occupancy(c.dev, fn, block, 0, 1, &occ) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (cached_occupancy(c.dev, c.info->smem_optin, fn, block, 0, 1, &occ) != cudaSuccess) return RMSNORM_ERR_CUDA;
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
     const int64_t resident = static_cast<int64_t>(c.info->sms) * occ;
     P->path = RMSNORM_PATH_TWOPASS;
@@ -388,7 +305,7 @@ rmsnorm_status_t plan_page(const Call& c, Plan* P) {
     if (c.rows > 0x7FFFFFFFll) return RMSNORM_ERR_UNSUPPORTED;
     KernelFn fn = page_kernel_ptr(c.dtype);
     int occ = 0;
-    if (cached_occupancy(c.dev, fn, page_block(), static_cast<int>(smem), 1, &occ) != cudaSuccess)
+    if (cached_occupancy(c.dev, c.info->smem_optin, fn, page_block(), static_cast<int>(smem), 1, &occ) != cudaSuccess)
         return RMSNORM_ERR_CUDA;
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
     P->path = RMSNORM_PATH_PAGE;
@@ -518,7 +435,9 @@ rmsnorm_status_t run(int32_t dtype, const void* x, const void* w, void* y, int64
     if (st != RMSNORM_OK) return st;
     if (!std::isfinite(eps) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
     if (rows == 0) return RMSNORM_OK;
-    if (current_device(&c.info, &c.dev) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (current_device(&c.view) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    c.info = &c.view;
+    c.dev = c.view.dev;
     Plan P;
     st = make_plan(c, &P);
     if (st != RMSNORM_OK) return st;
@@ -585,7 +504,9 @@ rmsnorm_status_t rmsnorm_plan(int32_t dtype, const void* x, const void* w, const
     Call c;
     rmsnorm_status_t st = validate(dtype, x, w, y, rows, hidden, opt, &c);
     if (st != RMSNORM_OK) return st;
-    if (current_device(&c.info, &c.dev) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (current_device(&c.view) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    c.info = &c.view;
+    c.dev = c.view.dev;
     if (c.rows == 0) c.rows = 1;   // describe the launch a one-row call would make
     Plan P;
     st = make_plan(c, &P);
@@ -608,8 +529,9 @@ rmsnorm_status_t rmsnorm_plan(int32_t dtype, const void* x, const void* w, const
 }
 
 rmsnorm_status_t rmsnorm_last_device_status(rmsnorm_stream_t stream) {
-    DeviceInfo* info = nullptr;
-    if (current_device(&info, nullptr) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    DeviceView view;
+    if (current_device(&view) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    const DeviceView* info = &view;
     if (note(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
         return RMSNORM_ERR_CUDA;
     unsigned word = 0;
@@ -637,10 +559,9 @@ const char* rmsnorm_status_string(rmsnorm_status_t status) {
 }
 
 int32_t rmsnorm_last_cuda_error(char* msg, size_t len) {
-    const cudaError_t e = t_last_cuda_error;
+    const cudaError_t e = take_last_cuda_error();
     if (msg && len > 0)
         std::snprintf(msg, len, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
-    t_last_cuda_error = cudaSuccess;
     return static_cast<int32_t>(e);
 }
 

@@ -29,6 +29,12 @@ KernelFn rowreg_kernel_ptr(int dtype, int vb, int nv, bool pf, int epi);
 int rowreg_max_block(int nv);
 KernelFn twopass_kernel_ptr(int dtype, int vb, int epi);
 int twopass_block();
+// Row softmax: register-resident kernel and the three-pass wide-row kernel.
+KernelFn softmax_rowreg_ptr(int dtype, int vb, int nv);
+int softmax_rowreg_max_block(int nv);
+KernelFn softmax_threepass_ptr(int dtype, int vb);
+int softmax_threepass_block();
+
 // Comparison kernel with the compiler write-up's schedule (one CTA per row).
 KernelFn page_kernel_ptr(int dtype);
 int page_block();

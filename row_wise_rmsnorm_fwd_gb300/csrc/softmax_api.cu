@@ -1,0 +1,255 @@
+// softmax_api.cu -- C ABI of the row-wise softmax (include/rowsoftmax.h):
+// validation, kernel choice and launch.  Shares the library's per-device
+// state (device.h) and status conventions with the RMSNorm entry points.
+#include "rowsoftmax.h"
+#include "launch.h"
+#include "device.h"
+
+#include <cstdio>
+#include <cstring>
+
+namespace rmsnorm {
+namespace {
+
+constexpr int kSoftmaxWaves = 4;   // row-block CTAs per resident CTA slot
+
+struct SmCall {
+    int dtype;
+    int sz;
+    uintptr_t x, y;
+    int64_t rows, cols;
+    rmsnorm_options_t opt;
+    DeviceView dv;
+};
+
+struct SmPlan {
+    int path = 0;
+    int group = 0;
+    int block = 0;
+    int rpc = 1;
+    int grid = 0;
+    int vb = 0;
+    int nv = 0;
+    int nvec = 0;
+    KernelFn fn = nullptr;
+    const char* name = "";
+};
+
+int sm_round_up(int64_t a, int64_t b) { return static_cast<int>(((a + b - 1) / b) * b); }
+int sm_pow2_ceil(int64_t v) { int p = 1; while (p < v) p <<= 1; return p; }
+
+rmsnorm_status_t sm_validate(int32_t dtype, const void* x, const void* y, int64_t rows,
+                             int64_t cols, const rmsnorm_options_t* opt, SmCall* c) {
+    if (dtype != RMSNORM_DTYPE_F32 && dtype != RMSNORM_DTYPE_BF16) return RMSNORM_ERR_INVALID_ARG;
+    if (!x || !y) return RMSNORM_ERR_INVALID_ARG;
+    if (rows < 0 || cols <= 0 || cols > 0x7FFFFFFFll) return RMSNORM_ERR_INVALID_ARG;
+    const int sz = dtype == RMSNORM_DTYPE_F32 ? 4 : 2;
+    if (rows > 0 && rows > (INT64_MAX / sz) / cols) return RMSNORM_ERR_INVALID_ARG;
+    const uintptr_t ux = reinterpret_cast<uintptr_t>(x), uy = reinterpret_cast<uintptr_t>(y);
+    if (ux % sz || uy % sz) return RMSNORM_ERR_INVALID_ARG;
+    const uint64_t n = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols) * sz;
+    if (ux != uy && ux < uy + n && uy < ux + n) return RMSNORM_ERR_INVALID_ARG;
+    std::memset(c, 0, sizeof(*c));
+    c->dtype = dtype;
+    c->sz = sz;
+    c->x = ux;
+    c->y = uy;
+    c->rows = rows;
+    c->cols = cols;
+    if (opt) {
+        c->opt = *opt;
+        const rmsnorm_options_t& o = *opt;
+        if (o.cluster || o.chunk_bytes || o.stages || o.weights || o.fault_inject ||
+            o.reserved || o.epilogue)
+            return RMSNORM_ERR_INVALID_ARG;
+        if (o.path != RMSNORM_PATH_AUTO && o.path != RMSNORM_PATH_ROWREG &&
+            o.path != RMSNORM_PATH_TWOPASS)
+            return RMSNORM_ERR_INVALID_ARG;
+        if (o.threads < 0 || o.threads % 32 != 0 || o.threads > 1024 || o.grid < 0)
+            return RMSNORM_ERR_INVALID_ARG;
+    }
+    return RMSNORM_OK;
+}
+
+rmsnorm_status_t sm_pick_vb(const SmCall& c, int* vb) {
+    const uintptr_t a = c.x | c.y;
+    const int64_t pitch = c.cols * c.sz;
+    int widest = c.sz;
+    for (int v = 16; v >= c.sz; v >>= 1)
+        if (a % v == 0 && pitch % v == 0) { widest = v; break; }
+    const int f = c.opt.vec_bytes;
+    if (f == 0) { *vb = widest; return RMSNORM_OK; }
+    if (f != 2 && f != 4 && f != 8 && f != 16) return RMSNORM_ERR_INVALID_ARG;
+    if (f < c.sz || f > widest) return RMSNORM_ERR_UNSUPPORTED;
+    *vb = f;
+    return RMSNORM_OK;
+}
+
+rmsnorm_status_t sm_plan_rowreg(const SmCall& c, SmPlan* P) {
+    int vb;
+    rmsnorm_status_t st = sm_pick_vb(c, &vb);
+    if (st != RMSNORM_OK) return st;
+    const int64_t nvec = c.cols / (vb / c.sz);
+    int G, NV;
+    if (c.opt.threads > 0) {
+        G = c.opt.threads;
+        const int64_t need = (nvec + G - 1) / G;
+        if (need > 8) return RMSNORM_ERR_UNSUPPORTED;
+        NV = sm_pow2_ceil(need);
+    } else if (nvec <= 32 * 4) {
+        G = 32;
+        NV = sm_pow2_ceil((nvec + 31) / 32);
+    } else {
+        NV = 4;
+        int64_t g = sm_round_up((nvec + NV - 1) / NV, 32);
+        if (g > softmax_rowreg_max_block(NV)) {
+            NV = 8;
+            g = sm_round_up((nvec + NV - 1) / NV, 32);
+        }
+        if (g > softmax_rowreg_max_block(NV)) return RMSNORM_ERR_UNSUPPORTED;
+        G = static_cast<int>(g);
+    }
+    if (G > softmax_rowreg_max_block(NV)) return RMSNORM_ERR_UNSUPPORTED;
+    KernelFn fn = softmax_rowreg_ptr(c.dtype, vb, NV);
+    if (!fn) return RMSNORM_ERR_UNSUPPORTED;
+    const int rpc = G >= 256 ? 1 : 256 / G;
+    const int block = G * rpc;
+    int occ = 0;
+    if (cached_occupancy(c.dv.dev, c.dv.smem_optin, fn, block, 0, 1, &occ) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t nblocks = (c.rows + rpc - 1) / rpc;
+    const int64_t target = static_cast<int64_t>(c.dv.sms) * occ * kSoftmaxWaves;
+    P->path = RMSNORM_PATH_ROWREG;
+    P->group = G;
+    P->block = block;
+    P->rpc = rpc;
+    P->grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid : (nblocks < target ? nblocks : target));
+    P->vb = vb;
+    P->nv = NV;
+    P->nvec = static_cast<int>(nvec);
+    P->fn = fn;
+    P->name = "softmax_rowreg";
+    return RMSNORM_OK;
+}
+
+rmsnorm_status_t sm_plan_threepass(const SmCall& c, SmPlan* P) {
+    int vb;
+    rmsnorm_status_t st = sm_pick_vb(c, &vb);
+    if (st != RMSNORM_OK) return st;
+    KernelFn fn = softmax_threepass_ptr(c.dtype, vb);
+    if (!fn) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t nvec = c.cols / (vb / c.sz);
+    const int maxb = softmax_threepass_block();
+    const int block = c.opt.threads > 0 ? c.opt.threads
+                                        : (nvec >= maxb ? maxb : sm_round_up(nvec, 32));
+    int occ = 0;
+    if (cached_occupancy(c.dv.dev, c.dv.smem_optin, fn, block, 0, 1, &occ) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t resident = static_cast<int64_t>(c.dv.sms) * occ;
+    P->path = RMSNORM_PATH_TWOPASS;
+    P->group = block;
+    P->block = block;
+    P->rpc = 1;
+    P->grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
+                                              : (c.rows < resident ? c.rows : resident));
+    P->vb = vb;
+    P->nv = 0;
+    P->nvec = static_cast<int>(nvec);
+    P->fn = fn;
+    P->name = "softmax_threepass";
+    return RMSNORM_OK;
+}
+
+rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
+    switch (c.opt.path) {
+        case RMSNORM_PATH_ROWREG: return sm_plan_rowreg(c, P);
+        case RMSNORM_PATH_TWOPASS: return sm_plan_threepass(c, P);
+        default: {
+            const rmsnorm_status_t st = sm_plan_rowreg(c, P);
+            if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+            return sm_plan_threepass(c, P);
+        }
+    }
+}
+
+rmsnorm_status_t sm_run(int32_t dtype, const void* x, void* y, int64_t rows, int64_t cols,
+                        const rmsnorm_options_t* opt, cudaStream_t stream) {
+    SmCall c;
+    rmsnorm_status_t st = sm_validate(dtype, x, y, rows, cols, opt, &c);
+    if (st != RMSNORM_OK) return st;
+    if (rows == 0) return RMSNORM_OK;
+    if (current_device(&c.dv) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    SmPlan P;
+    st = sm_make_plan(c, &P);
+    if (st != RMSNORM_OK) return st;
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = x;
+    p.y = y;
+    p.rows = rows;
+    p.hidden = static_cast<int32_t>(cols);
+    p.nvec = P.nvec;
+    p.group = P.group;
+    p.rows_per_cta = P.rpc;
+    p.cluster = 1;
+    p.status = c.dv.status;
+    p.timeout_ns = kDefaultTimeoutNs;
+    LaunchShape s{P.grid, P.block, 1, 0};
+    if (ensure_prepared(c.dv.dev, P.fn, c.dv.smem_optin) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (note(launch_ex(P.fn, s, stream, p)) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    return RMSNORM_OK;
+}
+
+}  // namespace
+}  // namespace rmsnorm
+
+using namespace rmsnorm;
+
+extern "C" {
+
+rmsnorm_status_t rowsoftmax_fwd_f32(const float* x, float* y, int64_t rows, int64_t cols,
+                                    rmsnorm_stream_t stream) {
+    return sm_run(RMSNORM_DTYPE_F32, x, y, rows, cols, nullptr,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+rmsnorm_status_t rowsoftmax_fwd_bf16(const uint16_t* x, uint16_t* y, int64_t rows,
+                                     int64_t cols, rmsnorm_stream_t stream) {
+    return sm_run(RMSNORM_DTYPE_BF16, x, y, rows, cols, nullptr,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+rmsnorm_status_t rowsoftmax_fwd_ex(int32_t dtype, const void* x, void* y, int64_t rows,
+                                   int64_t cols, const rmsnorm_options_t* opt,
+                                   rmsnorm_stream_t stream) {
+    return sm_run(dtype, x, y, rows, cols, opt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+rmsnorm_status_t rowsoftmax_plan(int32_t dtype, const void* x, const void* y, int64_t rows,
+                                 int64_t cols, const rmsnorm_options_t* opt,
+                                 rmsnorm_plan_t* plan) {
+    if (!plan) return RMSNORM_ERR_INVALID_ARG;
+    SmCall c;
+    rmsnorm_status_t st = sm_validate(dtype, x, y, rows, cols, opt, &c);
+    if (st != RMSNORM_OK) return st;
+    if (current_device(&c.dv) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (c.rows == 0) c.rows = 1;
+    SmPlan P;
+    st = sm_make_plan(c, &P);
+    if (st != RMSNORM_OK) return st;
+    std::memset(plan, 0, sizeof(*plan));
+    plan->path = P.path;
+    plan->cluster = 1;
+    plan->threads_per_row = P.group;
+    plan->block_threads = P.block;
+    plan->rows_per_cta = P.rpc;
+    plan->grid = P.grid;
+    plan->vec_bytes = P.vb;
+    plan->vecs_per_thread = P.nv;
+    std::snprintf(plan->kernel, sizeof(plan->kernel), "%s", P.name);
+    return RMSNORM_OK;
+}
+
+}  // extern "C"

@@ -61,6 +61,7 @@ class Workload:
     outlier_cols: int = 0
     outlier_scale: float = 1.0
     description: str = ""
+    op: str = "rmsnorm"   # "rmsnorm" or "softmax" (softmax has no weight)
 
     @property
     def rows(self) -> int:
@@ -79,8 +80,9 @@ class Workload:
 
     @property
     def bytes_per_call(self) -> int:
-        """Algorithmic bytes: read x once, write y once, read w once."""
-        return (2 * self.rows * self.hidden + self.hidden) * self.elem_bytes
+        """Algorithmic bytes: read x once, write y once, read w once (RMSNorm)."""
+        w = self.hidden if self.op == "rmsnorm" else 0
+        return (2 * self.rows * self.hidden + w) * self.elem_bytes
 
 
 WORKLOADS = {
@@ -134,6 +136,27 @@ for _model, _hidden, _eps in (("tinyllama", 2048, 1e-5), ("qwen7b", 3584, 1e-6))
                 ("normal", 0.0, 1.0), ("normal", 1.0, 0.1), _eps,
                 description=f"{_model}-shaped (batch {_batch}, seq {_seq}, hidden {_hidden})")
 WORKLOADS.update(MODEL_SWEEP)
+
+# Row softmax on the same skeleton: attention-score rows (batch 8 x 32 heads x
+# seq 512 rows of 512 columns, N(0,2) scores) and vocabulary logits (rows of
+# 32000, N(0,4)); x only, no weight.
+SOFTMAX_WORKLOADS = {
+    w.name: w for w in [
+        Workload("sm_attn_f32", 40, (8 * 32 * 512, 512), "f32", ("normal", 0.0, 2.0),
+                 ("normal", 1.0, 0.0), 0.0, op="softmax",
+                 description="softmax over attention scores (131072, 512) fp32"),
+        Workload("sm_attn_bf16", 41, (8 * 32 * 512, 512), "bf16", ("normal", 0.0, 2.0),
+                 ("normal", 1.0, 0.0), 0.0, op="softmax",
+                 description="softmax over attention scores (131072, 512) bf16"),
+        Workload("sm_vocab_f32", 42, (4096, 32000), "f32", ("normal", 0.0, 4.0),
+                 ("normal", 1.0, 0.0), 0.0, op="softmax",
+                 description="softmax over vocabulary logits (4096, 32000) fp32"),
+        Workload("sm_vocab_bf16", 43, (8192, 32000), "bf16", ("normal", 0.0, 4.0),
+                 ("normal", 1.0, 0.0), 0.0, op="softmax",
+                 description="softmax over vocabulary logits (8192, 32000) bf16"),
+    ]
+}
+WORKLOADS.update(SOFTMAX_WORKLOADS)
 
 
 def _torch_dtype(dtype: str):

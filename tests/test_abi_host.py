@@ -92,3 +92,25 @@ def test_product_path_has_no_fallback(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         binding.load()
+
+
+@pytest.mark.parametrize("fn", ["rowsoftmax_fwd_f32", "rowsoftmax_fwd_bf16"])
+def test_softmax_rejects_bad_arguments_before_launch(lib, fn):
+    f = getattr(binding.raw, fn)
+    assert f(0, B, 4, 8) == INVALID                  # x NULL
+    assert f(A, 0, 4, 8) == INVALID                  # y NULL
+    assert f(A, B, -1, 8) == INVALID                 # rows < 0
+    assert f(A, B, 4, 0) == INVALID                  # cols == 0
+    assert f(A, B, 4, 2 ** 31) == INVALID            # cols too large
+    assert f(A, A + 4, 4, 8) == INVALID              # partial overlap
+    assert f(A + 1, B, 4, 8) == INVALID              # misaligned element
+    assert f(A, B, 0, 8) == OK                       # no rows: nothing to do
+    assert f(A, A, 0, 8) == OK                       # in place, no rows
+
+
+def test_softmax_ex_rejects_rmsnorm_only_options(lib):
+    for field, value in (("cluster", 2), ("chunk_bytes", 4096), ("stages", 3), ("weights", 1),
+                         ("epilogue", 1), ("fault_inject", 1), ("path", 2), ("path", 5)):
+        o = binding.make_options()
+        setattr(o, field, value)
+        assert binding.raw.rowsoftmax_fwd_ex(0, A, B, 4, 8, o) == INVALID, field

@@ -1,0 +1,141 @@
+"""GPU parity of the row-wise softmax against the fp64 CPU oracle (C ABI via
+the ctypes binding).  Tolerances as for RMSNorm (tests/_parity.py): fp32
+|d| <= max(1e-5 |ref|, 1e-6); bf16 within 1 ulp of the single rounding."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _parity import check_bf16, check_f32
+from row_wise_rmsnorm_fwd_gb300 import binding, build, workloads
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    build.build()
+    binding.load()
+    yield
+    torch.cuda.synchronize()
+
+
+def ref_for(x_cpu):
+    if x_cpu.dtype == torch.float32:
+        return oracle.rowsoftmax_f32(x_cpu.numpy())
+    _, y16 = oracle.rowsoftmax_bf16(workloads.bf16_bits(x_cpu))
+    return y16
+
+
+def compare(y, ref, what):
+    y = y.detach().cpu().contiguous()
+    if y.dtype == torch.float32:
+        check_f32(y.numpy(), ref, what)
+    else:
+        check_bf16(workloads.bf16_bits(y), ref, what)
+
+
+def run(x, y=None, **opts):
+    if y is None:
+        y = torch.empty_like(x)
+    if opts:
+        binding.rowsoftmax_fwd_ex(x, y, options=opts)
+    elif x.dtype == torch.float32:
+        binding.rowsoftmax_fwd_f32(x, y)
+    else:
+        binding.rowsoftmax_fwd_bf16(x, y)
+    torch.cuda.synchronize()
+    return y
+
+
+def case(rows, cols, dtype, seed, std=3.0):
+    return workloads.make_random((rows, cols), dtype, seed, ("normal", 0.0, std))
+
+
+@pytest.mark.parametrize("name", sorted(workloads.SOFTMAX_WORKLOADS))
+def test_softmax_workloads_sampled(name):
+    wl = workloads.SOFTMAX_WORKLOADS[name]
+    x = workloads.make_x(wl, device="cuda")
+    y = run(x)
+    g = torch.Generator().manual_seed(wl.index)
+    pick = torch.cat([torch.arange(4), torch.arange(wl.rows - 4, wl.rows),
+                      torch.randint(0, wl.rows, (256,), generator=g)]).unique().cuda()
+    compare(y[pick], ref_for(x[pick].cpu()), name)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", [1, 2, 3, 31, 32, 33, 127, 512, 1000, 2049, 4096, 8193,
+                                  16384, 32000, 65536, 100000])
+def test_width_sweep(dtype, cols):
+    rows = 37 if cols <= 16384 else 5
+    x = case(rows, cols, dtype, cols)
+    compare(run(x.cuda()), ref_for(x), f"{dtype} cols={cols}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("path", ["rowreg", "twopass"])
+@pytest.mark.parametrize("rows,cols", [(300, 512), (7, 4096), (3, 32000), (64, 1000)])
+def test_forced_paths(dtype, path, rows, cols):
+    x = case(rows, cols, dtype, rows + cols)
+    try:
+        y = run(x.cuda(), path=path)
+    except binding.RmsnormError as e:
+        if e.status == binding.RMSNORM_ERR_UNSUPPORTED:
+            pytest.skip("path cannot serve this shape")
+        raise
+    compare(y, ref_for(x), f"{path} {dtype} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_special_values(dtype):
+    cols = 640
+    x = case(6, cols, "f32", 9)
+    x[0, ::3] = -float("inf")          # masked entries -> exactly 0
+    x[1] = -float("inf")               # fully masked row -> NaN
+    x[2, 17] = float("nan")            # NaN -> NaN row
+    x[3, 5] = float("inf")             # +inf -> NaN row
+    x[4] *= 40.0                       # wide spread: most outputs underflow to 0
+    x[5] = 7.25                        # uniform row -> 1/cols
+    x = x.to(DT[dtype])
+    y = run(x.cuda())
+    compare(y, ref_for(x), f"special {dtype}")
+    assert bool((y[0].cpu()[::3] == 0).all())
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols", [(64, 512), (5, 32000), (3, 100000)])
+def test_in_place_and_misaligned(dtype, rows, cols):
+    x = case(rows, cols, dtype, 3)
+    xc = x.cuda()
+    run(xc, y=xc)
+    compare(xc, ref_for(x), "in place")
+    n = rows * cols
+    buf = torch.zeros(n + 8, dtype=DT[dtype], device="cuda")
+    out = torch.zeros(n + 8, dtype=DT[dtype], device="cuda")
+    xv = buf[1:1 + n].view(rows, cols)
+    yv = out[3:3 + n].view(rows, cols)
+    xv.copy_(x)
+    run(xv, y=yv)
+    compare(yv, ref_for(x), "misaligned")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_guards_and_determinism(dtype):
+    rows, cols = 33, 4104
+    x = case(rows, cols, dtype, 4).cuda()
+    guard = 2048
+    buf = torch.full((guard + rows * cols + guard,), -5.0, dtype=DT[dtype], device="cuda")
+    y = buf[guard:guard + rows * cols].view(rows, cols)
+    run(x, y=y)
+    assert bool((buf[:guard] == -5.0).all()) and bool((buf[-guard:] == -5.0).all())
+    for _ in range(3):
+        assert torch.equal(run(x), y)
+
+
+def test_rows_sum_to_one_and_match_torch():
+    x = case(1000, 512, "f32", 5).cuda()
+    y = run(x)
+    torch.testing.assert_close(y.sum(-1), torch.ones(1000, device="cuda"), rtol=0, atol=2e-6)
+    torch.testing.assert_close(y, torch.softmax(x, -1), rtol=1e-5, atol=1e-7)
