@@ -142,6 +142,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(values, device="cpu"):
+    """All-reduce a list of timings with MAX over the ranks of the default
+    process group (NCCL on GPUs, gloo on CPU); returns the reduced list."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def weak_scaling_rates(world, bytes_per_step, rows_per_step, steps, slowest_ms):
+    """Whole-job GB/s and rows/s: every rank processed the full workload in
+    at most `slowest_ms` (the max over ranks)."""
+    seconds = slowest_ms / 1e3
+    return (world * bytes_per_step * steps / seconds / 1e9,
+            world * rows_per_step * steps / seconds)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -340,14 +358,10 @@ def run_ours(args, wl):
     kernel_ms = sum(per_launch_ms)          # device time of the K launches
     region_ms = t_begin.elapsed_time(t_end)  # whole timed region
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([kernel_ms, region_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        kernel_ms, region_ms = float(t[0]), float(t[1])
+        kernel_ms, region_ms = max_over_ranks([kernel_ms, region_ms], dev)
     ms_per_step = kernel_ms / args.steps
     bytes_step = wl.bytes_per_call
-    value = world * bytes_step * args.steps / (kernel_ms / 1e3) / 1e9
-    rows_per_s = world * rows * args.steps / (kernel_ms / 1e3)
+    value, rows_per_s = weak_scaling_rates(world, bytes_step, rows, args.steps, kernel_ms)
 
     peak, peak_src = peaks()
     avg_launch_s = (sum(per_launch_ms) / len(per_launch_ms)) / 1e3
@@ -451,10 +465,7 @@ def measure_e2e(args, wl, x_dev, w_dev, y_dev, fwd, binding, world):
         step()
     dt_s = time.perf_counter() - t0
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([dt_s], device=x_dev.device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dt_s = float(t[0])
+        dt_s = max_over_ranks([dt_s], x_dev.device)[0]
     # check the round trip landed (cheap spot check of one row against the device)
     if not torch.equal(yh2[-1].to(y_dev.device), yd2[-1]):
         raise RuntimeError("end-to-end copy-back mismatch")
