@@ -1,0 +1,59 @@
+"""bench.py's reference arm runs the oracle on the host (CPU only) and prints
+one JSON line with the contract's keys; its helpers read the committed
+profiles correctly."""
+import json
+import os
+import subprocess
+import sys
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_one_json_line():
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "c1",
+                          "--steps", "3", "--warmup", "3"], cwd=ROOT, capture_output=True,
+                         text=True, timeout=600, check=True).stdout.strip().splitlines()
+    assert len(out) == 1
+    d = json.loads(out[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["higher_is_better"] is True and d["steps"] == 3 and d["warmup"] == 3
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"].startswith("c1")
+
+
+def test_reference_arm_softmax_workload():
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                          "sm_attn_f32", "--steps", "3", "--warmup", "3"], cwd=ROOT,
+                         capture_output=True, text=True, timeout=600, check=True).stdout
+    d = json.loads(out.strip().splitlines()[-1])
+    assert d["metric"].startswith("row softmax") and d["value"] > 0
+
+
+def test_warmup_below_three_is_refused():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--warmup", "2"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0
+
+
+def test_committed_profiles_parse():
+    """Every committed per-kernel summary names its source files, and the
+    traffic of a profile is returned only while their hash matches."""
+    pdir = os.path.join(ROOT, "profiles")
+    found = 0
+    for name in os.listdir(pdir):
+        if not name.endswith(".txt") or name.startswith("launches"):
+            continue
+        text = open(os.path.join(pdir, name)).read()
+        head = text.splitlines()[0].split()      # "ncu summary: <kernel> on workload <w>"
+        kernel, workload = head[2], head[-1]
+        assert name == f"{kernel}_{workload}.txt"
+        assert "kernel_source_files:" in text and "traffic_bytes_per_launch:" in text
+        assert "ncu " in text and "--clock-control none" in text
+        found += 1
+        t = bench.profiled_traffic(workload, kernel)
+        assert t is None or t > 0
+    assert found >= 6
