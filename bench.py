@@ -160,6 +160,21 @@ def weak_scaling_rates(world, bytes_per_step, rows_per_step, steps, slowest_ms):
             world * rows_per_step * steps / seconds)
 
 
+def device_info(dev):
+    """GPU name, SM count and L2 size of `dev`, and the repository's git commit."""
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    sha = None
+    try:
+        sha = subprocess.run(["git", "rev-parse", "--short", "HEAD"], cwd=ROOT,
+                             capture_output=True, text=True, timeout=10).stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"name": props.name, "sms": props.multi_processor_count,
+            "l2_bytes": getattr(props, "L2_cache_size", None),
+            "memory_bytes": props.total_memory, "git": sha}
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -343,6 +358,7 @@ def run_ours(args, wl):
     with ClockSampler(local) as clocks:
         time.sleep(0.3)          # let the sampler start before the timed region
         barrier()
+        torch.cuda.nvtx.range_push("timed region")
         t_begin = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_begin.record(stream)
@@ -353,6 +369,7 @@ def run_ours(args, wl):
             step()
             ends[i].record(stream)
         t_end.record(stream)
+        torch.cuda.nvtx.range_pop()
         barrier()
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     kernel_ms = sum(per_launch_ms)          # device time of the K launches
@@ -403,6 +420,7 @@ def run_ours(args, wl):
             "e2e": e2e,
             "gpu_launches": args.steps,
             "timed_region_ms": region_ms,
+            "device": device_info(dev),
             "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)
