@@ -7,7 +7,7 @@
 // Compile-time policy of the instances (overridable for tuning builds):
 // prefetch, weights in registers, x-load and y-store cache policies.
 #ifndef RMSNORM_ROWREG_PF
-#define RMSNORM_ROWREG_PF 0
+#define RMSNORM_ROWREG_PF 1
 #endif
 #ifndef RMSNORM_ROWREG_WREG
 #define RMSNORM_ROWREG_WREG 1
