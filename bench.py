@@ -310,8 +310,10 @@ def run_ours(args, wl):
     handle = stream.cuda_stream
     options = None
     if softmax:
-        options = binding.make_options(path=args.path if args.path in ("rowreg", "twopass")
-                                       else "auto", grid=args.grid, threads=args.threads)
+        options = binding.make_options(
+            path=args.path if args.path in ("rowreg", "twopass", "cluster") else "auto",
+            cluster=args.cluster if args.path == "cluster" else 0,
+            grid=args.grid, threads=args.threads)
         dt_code = binding.RMSNORM_DTYPE_BF16 if wl.dtype == "bf16" else binding.RMSNORM_DTYPE_F32
 
         def fwd(xp, wp, yp, r, h, eps, s):

@@ -40,10 +40,13 @@ rmsnorm_status_t rowsoftmax_fwd_bf16(const uint16_t* x, uint16_t* y, int64_t row
 
 /*
  * Either dtype with options: opt->path may be RMSNORM_PATH_AUTO,
- * RMSNORM_PATH_ROWREG (row held in registers; rows up to 64 KiB) or
- * RMSNORM_PATH_TWOPASS (the wide-row kernel: reads each row three times, the
- * repeats normally from L2); opt->threads, opt->grid and opt->vec_bytes as
- * for rmsnorm_fwd_ex.  Other option fields must be zero.  `opt` may be NULL.
+ * RMSNORM_PATH_ROWREG (row held in registers; rows up to 64 KiB),
+ * RMSNORM_PATH_CLUSTER (each row split over opt->cluster = 2..16 CTAs of a
+ * thread-block cluster, row maximum and sum combined through distributed
+ * shared memory) or RMSNORM_PATH_TWOPASS (the wide-row kernel: reads each row
+ * three times, the repeats normally from L2); opt->threads, opt->grid,
+ * opt->vec_bytes and opt->wait_timeout_ns as for rmsnorm_fwd_ex.  Other
+ * option fields must be zero.  `opt` may be NULL.
  */
 rmsnorm_status_t rowsoftmax_fwd_ex(int32_t dtype, const void* x, void* y, int64_t rows,
                                    int64_t cols, const rmsnorm_options_t* opt,

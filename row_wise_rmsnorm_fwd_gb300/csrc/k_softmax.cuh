@@ -43,11 +43,15 @@ constexpr int softmax_max_threads() { return NV >= 4 ? 512 : 1024; }
 
 // PF: the next row's loads are issued before this row's two reductions
 // (register double buffer), doubling the bytes in flight for narrow rows.
+// With p.cluster > 1 a thread-block cluster of C CTAs shares each row: every
+// CTA holds a slice, and the row maximum and the row sum are each combined
+// across the cluster through distributed shared memory (bounded waits).
 template <typename T, int VB, int NV, bool PF>
 __global__ void __launch_bounds__(softmax_max_threads<NV>())
 softmax_rowreg_kernel(const Params p) {
     constexpr int EPV = VecTraits<T, VB>::kElems;
     __shared__ float red[2][2][32];      // [max | sum][double buffer][warp]
+    __shared__ ClusterExchange exmax, exsum;
 
     const int G = p.group;
     const int tid = threadIdx.x;
@@ -57,12 +61,23 @@ softmax_rowreg_kernel(const Params p) {
     const int wpg = G >> 5;
     const int gw0 = g * wpg;
 
+    const int ncta = p.cluster;
+    uint32_t rank = 0;
+    int64_t unit = blockIdx.x, nunits = gridDim.x;
+    if (ncta > 1) {
+        rank = cluster_ctarank();
+        unit = cluster_id_x();
+        nunits = cluster_count_x();
+        cluster_exchange_init(&exmax, ncta, &exsum);
+    }
+    const int vbase = (ncta > 1) ? static_cast<int>(rank) * p.slice_vecs : 0;
+    const int vlim = (ncta > 1) ? min(p.nvec, vbase + p.slice_vecs) : p.nvec;
     int vidx[NV];
     bool valid[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
-        vidx[i] = i * G + t;
-        valid[i] = vidx[i] < p.nvec;
+        vidx[i] = vbase + i * G + t;
+        valid[i] = vidx[i] < vlim;
     }
     const char* xb = static_cast<const char*>(p.x);
     char* yb = static_cast<char*>(p.y);
@@ -81,11 +96,11 @@ softmax_rowreg_kernel(const Params p) {
         }
     };
 
-    int64_t rb = blockIdx.x;
+    int64_t rb = unit;
     if (rb < nblocks) load_row(cur, rb);
     uint32_t it = 0;
-    for (; rb < nblocks; rb += gridDim.x, ++it) {
-        const int64_t nrb = rb + gridDim.x;
+    for (; rb < nblocks; rb += nunits, ++it) {
+        const int64_t nrb = rb + nunits;
         if (PF && nrb < nblocks) load_row(nxt, nrb);
         const int64_t row = rb * RPC + g;
         const bool row_ok = row < p.rows;
@@ -112,6 +127,12 @@ softmax_rowreg_kernel(const Params p) {
             m = -INFINITY;
             for (int k = 0; k < wpg; ++k) m = fmaxf(m, red[0][b][gw0 + k]);
         }
+        if (ncta > 1) {
+            float cm;
+            const bool ok = cluster_allreduce<true>(&exmax, m, ncta, rank, it, p, &cm, tid);
+            m = cm;
+            if (__syncthreads_or(!ok)) break;   // uniform: stop, then leave cleanly
+        }
         // exponentials and their sum
         const float ml2e = m * kLog2e;
         float s0 = 0.f, s1 = 0.f;
@@ -134,6 +155,12 @@ softmax_rowreg_kernel(const Params p) {
             s = 0.f;
             for (int k = 0; k < wpg; ++k) s += red[1][b][gw0 + k];
         }
+        if (ncta > 1) {
+            float cs;
+            const bool ok = cluster_allreduce(&exsum, s, ncta, rank, it, p, &cs, tid);
+            s = cs;
+            if (__syncthreads_or(!ok)) break;
+        }
         const float inv = 1.0f / s;
         if (row_ok) {
             char* dst = yb + row * row_bytes;
@@ -154,6 +181,8 @@ softmax_rowreg_kernel(const Params p) {
             load_row(cur, nrb);
         }
     }
+    // Keep this CTA's shared memory alive until every peer is done with it.
+    if (ncta > 1) cluster_sync_all();
 }
 
 constexpr int kSoftmaxWideThreads = 1024;

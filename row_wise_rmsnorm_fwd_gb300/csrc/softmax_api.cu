@@ -11,7 +11,9 @@
 namespace rmsnorm {
 namespace {
 
-constexpr int kSoftmaxWaves = 4;   // row-block CTAs per resident CTA slot
+constexpr int kSoftmaxWaves = 4;                        // row-block CTAs per resident slot
+constexpr int64_t kSoftmaxSplitRowBytes = 32768;        // few rows wider than this: split
+constexpr int64_t kSoftmaxSplitMinBytes = 16 << 20;     // or few rows totalling this much
 
 struct SmCall {
     int dtype;
@@ -24,6 +26,8 @@ struct SmCall {
 
 struct SmPlan {
     int path = 0;
+    int cluster = 1;
+    int slice_vecs = 0;
     int group = 0;
     int block = 0;
     int rpc = 1;
@@ -59,12 +63,15 @@ rmsnorm_status_t sm_validate(int32_t dtype, const void* x, const void* y, int64_
     if (opt) {
         c->opt = *opt;
         const rmsnorm_options_t& o = *opt;
-        if (o.cluster || o.chunk_bytes || o.stages || o.weights || o.fault_inject ||
-            o.reserved || o.epilogue)
+        if (o.chunk_bytes || o.stages || o.weights || o.fault_inject || o.reserved ||
+            o.epilogue)
             return RMSNORM_ERR_INVALID_ARG;
         if (o.path != RMSNORM_PATH_AUTO && o.path != RMSNORM_PATH_ROWREG &&
-            o.path != RMSNORM_PATH_TWOPASS)
+            o.path != RMSNORM_PATH_TWOPASS && o.path != RMSNORM_PATH_CLUSTER)
             return RMSNORM_ERR_INVALID_ARG;
+        if (o.cluster < 0 || o.cluster > 16 || (o.cluster & (o.cluster - 1)) != 0)
+            return RMSNORM_ERR_INVALID_ARG;
+        if (o.cluster > 1 && o.path != RMSNORM_PATH_CLUSTER) return RMSNORM_ERR_INVALID_ARG;
         if (o.threads < 0 || o.threads % 32 != 0 || o.threads > 1024 || o.grid < 0)
             return RMSNORM_ERR_INVALID_ARG;
     }
@@ -85,26 +92,28 @@ rmsnorm_status_t sm_pick_vb(const SmCall& c, int* vb) {
     return RMSNORM_OK;
 }
 
-rmsnorm_status_t sm_plan_rowreg(const SmCall& c, SmPlan* P) {
+// Register-resident softmax; cluster > 1 splits every row over a cluster.
+rmsnorm_status_t sm_plan_rowreg(const SmCall& c, int cluster, SmPlan* P) {
     int vb;
     rmsnorm_status_t st = sm_pick_vb(c, &vb);
     if (st != RMSNORM_OK) return st;
     const int64_t nvec = c.cols / (vb / c.sz);
+    const int64_t per = cluster > 1 ? (nvec + cluster - 1) / cluster : nvec;
     int G, NV;
     if (c.opt.threads > 0) {
         G = c.opt.threads;
-        const int64_t need = (nvec + G - 1) / G;
+        const int64_t need = (per + G - 1) / G;
         if (need > 8) return RMSNORM_ERR_UNSUPPORTED;
         NV = sm_pow2_ceil(need);
-    } else if (nvec <= 32 * 4) {
+    } else if (cluster == 1 && per <= 32 * 4) {
         G = 32;
-        NV = sm_pow2_ceil((nvec + 31) / 32);
+        NV = sm_pow2_ceil((per + 31) / 32);
     } else {
         NV = 4;
-        int64_t g = sm_round_up((nvec + NV - 1) / NV, 32);
+        int64_t g = sm_round_up((per + NV - 1) / NV, 32);
         if (g > softmax_rowreg_max_block(NV)) {
             NV = 8;
-            g = sm_round_up((nvec + NV - 1) / NV, 32);
+            g = sm_round_up((per + NV - 1) / NV, 32);
         }
         if (g > softmax_rowreg_max_block(NV)) return RMSNORM_ERR_UNSUPPORTED;
         G = static_cast<int>(g);
@@ -112,24 +121,35 @@ rmsnorm_status_t sm_plan_rowreg(const SmCall& c, SmPlan* P) {
     if (G > softmax_rowreg_max_block(NV)) return RMSNORM_ERR_UNSUPPORTED;
     KernelFn fn = softmax_rowreg_ptr(c.dtype, vb, NV);
     if (!fn) return RMSNORM_ERR_UNSUPPORTED;
-    const int rpc = G >= 256 ? 1 : 256 / G;
+    const int rpc = cluster == 1 ? (G >= 256 ? 1 : 256 / G) : 1;
     const int block = G * rpc;
     int occ = 0;
-    if (cached_occupancy(c.dv.dev, c.dv.smem_optin, fn, block, 0, 1, &occ) != cudaSuccess)
+    if (cached_occupancy(c.dv.dev, c.dv.smem_optin, fn, block, 0, cluster, &occ) != cudaSuccess)
         return RMSNORM_ERR_CUDA;
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
-    const int64_t nblocks = (c.rows + rpc - 1) / rpc;
-    const int64_t target = static_cast<int64_t>(c.dv.sms) * occ * kSoftmaxWaves;
-    P->path = RMSNORM_PATH_ROWREG;
+    int grid;
+    if (cluster == 1) {
+        const int64_t nblocks = (c.rows + rpc - 1) / rpc;
+        const int64_t target = static_cast<int64_t>(c.dv.sms) * occ * kSoftmaxWaves;
+        grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
+                                               : (nblocks < target ? nblocks : target));
+    } else {
+        const int64_t nclusters = c.opt.grid > 0 ? (c.opt.grid + cluster - 1) / cluster
+                                                 : (c.rows < occ ? c.rows : occ);
+        grid = static_cast<int>(nclusters * cluster);
+    }
+    P->path = cluster == 1 ? RMSNORM_PATH_ROWREG : RMSNORM_PATH_CLUSTER;
+    P->cluster = cluster;
+    P->slice_vecs = static_cast<int>(per);
     P->group = G;
     P->block = block;
     P->rpc = rpc;
-    P->grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid : (nblocks < target ? nblocks : target));
+    P->grid = grid;
     P->vb = vb;
     P->nv = NV;
     P->nvec = static_cast<int>(nvec);
     P->fn = fn;
-    P->name = "softmax_rowreg";
+    P->name = cluster == 1 ? "softmax_rowreg" : "softmax_cluster_rowreg";
     return RMSNORM_OK;
 }
 
@@ -162,16 +182,32 @@ rmsnorm_status_t sm_plan_threepass(const SmCall& c, SmPlan* P) {
     return RMSNORM_OK;
 }
 
+// Automatic choice: rows that fit one CTA's registers go to the register
+// kernel; few rows of wide rows (or large few-row inputs) are split over a
+// cluster (up to 8 CTAs, slices of at least 4 KB), as for RMSNorm; the rest
+// go to the three-pass kernel.
 rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
     switch (c.opt.path) {
-        case RMSNORM_PATH_ROWREG: return sm_plan_rowreg(c, P);
+        case RMSNORM_PATH_ROWREG: return sm_plan_rowreg(c, 1, P);
+        case RMSNORM_PATH_CLUSTER: return sm_plan_rowreg(c, c.opt.cluster ? c.opt.cluster : 2, P);
         case RMSNORM_PATH_TWOPASS: return sm_plan_threepass(c, P);
-        default: {
-            const rmsnorm_status_t st = sm_plan_rowreg(c, P);
+        default: break;
+    }
+    const int64_t row_bytes = c.cols * c.sz;
+    rmsnorm_status_t st;
+    if (c.rows < c.dv.sms && (row_bytes > kSoftmaxSplitRowBytes ||
+                              c.rows * row_bytes >= kSoftmaxSplitMinBytes)) {
+        int want = 1;
+        while (static_cast<int64_t>(want) * 2 * c.rows <= c.dv.sms && want < 8) want <<= 1;
+        while (want > 1 && row_bytes / want < 4096) want >>= 1;
+        for (int cl = want; cl > 1 && cl <= 16; cl <<= 1) {
+            st = sm_plan_rowreg(c, cl, P);
             if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
-            return sm_plan_threepass(c, P);
         }
     }
+    st = sm_plan_rowreg(c, 1, P);
+    if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+    return sm_plan_threepass(c, P);
 }
 
 rmsnorm_status_t sm_run(int32_t dtype, const void* x, void* y, int64_t rows, int64_t cols,
@@ -193,10 +229,11 @@ rmsnorm_status_t sm_run(int32_t dtype, const void* x, void* y, int64_t rows, int
     p.nvec = P.nvec;
     p.group = P.group;
     p.rows_per_cta = P.rpc;
-    p.cluster = 1;
+    p.cluster = P.cluster;
+    p.slice_vecs = P.slice_vecs;
     p.status = c.dv.status;
-    p.timeout_ns = kDefaultTimeoutNs;
-    LaunchShape s{P.grid, P.block, 1, 0};
+    p.timeout_ns = c.opt.wait_timeout_ns ? c.opt.wait_timeout_ns : kDefaultTimeoutNs;
+    LaunchShape s{P.grid, P.block, P.cluster, 0};
     if (ensure_prepared(c.dv.dev, P.fn, c.dv.smem_optin) != cudaSuccess) return RMSNORM_ERR_CUDA;
     if (note(launch_ex(P.fn, s, stream, p)) != cudaSuccess) return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
@@ -241,7 +278,7 @@ rmsnorm_status_t rowsoftmax_plan(int32_t dtype, const void* x, const void* y, in
     if (st != RMSNORM_OK) return st;
     std::memset(plan, 0, sizeof(*plan));
     plan->path = P.path;
-    plan->cluster = 1;
+    plan->cluster = P.cluster;
     plan->threads_per_row = P.group;
     plan->block_threads = P.block;
     plan->rows_per_cta = P.rpc;

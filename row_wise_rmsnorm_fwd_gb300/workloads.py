@@ -138,8 +138,9 @@ for _model, _hidden, _eps in (("tinyllama", 2048, 1e-5), ("qwen7b", 3584, 1e-6))
 WORKLOADS.update(MODEL_SWEEP)
 
 # Row softmax on the same skeleton: attention-score rows (batch 8 x 32 heads x
-# seq 512 rows of 512 columns, N(0,2) scores) and vocabulary logits (rows of
-# 32000, N(0,4)); x only, no weight.
+# seq 512 rows of 512 columns, N(0,2) scores), vocabulary logits (rows of
+# 32000, N(0,4)) and decode-step logits (few rows of a 128256 vocabulary);
+# x only, no weight.
 SOFTMAX_WORKLOADS = {
     w.name: w for w in [
         Workload("sm_attn_f32", 40, (8 * 32 * 512, 512), "f32", ("normal", 0.0, 2.0),
@@ -154,6 +155,12 @@ SOFTMAX_WORKLOADS = {
         Workload("sm_vocab_bf16", 43, (8192, 32000), "bf16", ("normal", 0.0, 4.0),
                  ("normal", 1.0, 0.0), 0.0, op="softmax",
                  description="softmax over vocabulary logits (8192, 32000) bf16"),
+        Workload("sm_decode_f32", 44, (8, 128256), "f32", ("normal", 0.0, 4.0),
+                 ("normal", 1.0, 0.0), 0.0, op="softmax",
+                 description="decode-step logits, 8 sequences x 128256 vocabulary, fp32"),
+        Workload("sm_decode_bf16", 45, (64, 128256), "bf16", ("normal", 0.0, 4.0),
+                 ("normal", 1.0, 0.0), 0.0, op="softmax",
+                 description="decode-step logits, 64 sequences x 128256 vocabulary, bf16"),
     ]
 }
 WORKLOADS.update(SOFTMAX_WORKLOADS)

@@ -75,17 +75,34 @@ def test_width_sweep(dtype, cols):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("path", ["rowreg", "twopass"])
-@pytest.mark.parametrize("rows,cols", [(300, 512), (7, 4096), (3, 32000), (64, 1000)])
-def test_forced_paths(dtype, path, rows, cols):
+@pytest.mark.parametrize("path,cluster", [("rowreg", 0), ("twopass", 0), ("cluster", 2),
+                                          ("cluster", 4), ("cluster", 8), ("cluster", 16)])
+@pytest.mark.parametrize("rows,cols", [(300, 512), (7, 4096), (3, 32000), (64, 1000),
+                                       (5, 128256), (2, 262144)])
+def test_forced_paths(dtype, path, cluster, rows, cols):
     x = case(rows, cols, dtype, rows + cols)
     try:
-        y = run(x.cuda(), path=path)
+        y = run(x.cuda(), path=path, cluster=cluster)
     except binding.RmsnormError as e:
         if e.status == binding.RMSNORM_ERR_UNSUPPORTED:
             pytest.skip("path cannot serve this shape")
         raise
-    compare(y, ref_for(x), f"{path} {dtype} {rows}x{cols}")
+    compare(y, ref_for(x), f"{path} C={cluster} {dtype} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_cluster_special_values(dtype):
+    """Masked, fully masked, NaN and +inf rows through the cluster split (the
+    maximum and the sum cross the cluster)."""
+    cols = 65536
+    x = case(4, cols, "f32", 19)
+    x[0, ::7] = -float("inf")
+    x[1] = -float("inf")
+    x[2, 60000] = float("nan")
+    x[3, 3] = float("inf")
+    x = x.to(DT[dtype])
+    y = run(x.cuda(), path="cluster", cluster=8)
+    compare(y, ref_for(x), f"cluster special {dtype}")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
