@@ -184,64 +184,110 @@ def dist_env():
 
 # ------------------------------------------------------------ CPU baseline --
 
-def cpu_oracle_sample(wl, budget_s: float = 10.0, chunk_rows: int = 2048, max_chunks: int = 48):
-    """Time the oracle (as it stands, one host thread) on chunks of the
-    workload's rows until about `budget_s` seconds of CPU work are done."""
+_oracle_out = threading.local()
+
+
+def _oracle_chunk_call(oracle, wl, x, w):
+    """One oracle call on a host chunk of rows (the arithmetic is all in C).
+    Each thread writes into its own output buffers, reused from call to
+    call: fresh buffers would make the threads fault pages in side by side,
+    which the host kernel serialises."""
+    import numpy as np
+
+    bufs = getattr(_oracle_out, "bufs", None)
+    if bufs is None or bufs[0].shape != x.shape:
+        bufs = (np.zeros(x.shape, np.float64), np.zeros(x.shape, np.uint16))
+        _oracle_out.bufs = bufs
+    y64, y16 = bufs
+    softmax = wl.op == "softmax"
+    if wl.dtype == "bf16":
+        if softmax:
+            oracle.rowsoftmax_bf16(x, out64=y64, out16=y16)
+        else:
+            oracle.rmsnorm_bf16(x, w, wl.eps, out64=y64, out16=y16)
+    elif softmax:
+        oracle.rowsoftmax_f32(x, out=y64)
+    else:
+        oracle.rmsnorm_f32(x, w, wl.eps, out=y64)
+
+
+def host_cores() -> int:
+    return max(1, len(os.sched_getaffinity(0)))
+
+
+def cpu_oracle_sample(wl, budget_s: float = 10.0, threads: int = 1, max_rounds: int = 64):
+    """Time the oracle (as it stands) on bounded samples of the workload's rows.
+
+    Each round draws ``threads`` fresh chunks of rows (outside the clock), then
+    ``threads`` host threads run the oracle on one chunk each at the same time
+    (the oracle is a C library called through ctypes, which releases the
+    interpreter lock); the wall clock of the rounds is summed until about
+    ``budget_s`` seconds.  ``threads=1`` is the plain single-thread oracle."""
+    import concurrent.futures as cf
+
     import oracle
     from row_wise_rmsnorm_fwd_gb300 import workloads
 
     oracle.build()
     softmax = wl.op == "softmax"
-    w = None if softmax else workloads.make_w(wl)
-    chunk_rows = min(chunk_rows, wl.rows)
-    done_rows, elapsed, k = 0, 0.0, 0
-    if wl.dtype == "bf16" and not softmax:
-        wb = workloads.bf16_bits(w)
-    while elapsed < budget_s and k < max_chunks:
+    chunk_rows = max(1, min(wl.rows, (1 << 22) // wl.hidden))
+    w = None
+    if not softmax:
+        w = workloads.make_w(wl)
+        w = workloads.bf16_bits(w) if wl.dtype == "bf16" else w.numpy()
+
+    def draw(k):
         x = workloads.make_x(wl, rows=chunk_rows, seed_offset=k)
-        if wl.dtype == "bf16":
-            xb = workloads.bf16_bits(x)
+        return workloads.bf16_bits(x) if wl.dtype == "bf16" else x.numpy()
+
+    done_rows, elapsed, rounds = 0, 0.0, 0
+    with cf.ThreadPoolExecutor(threads) as ex:
+        while elapsed < budget_s and rounds < max_rounds:
+            chunks = list(ex.map(draw, range(rounds * threads, (rounds + 1) * threads)))
             t0 = time.perf_counter()
-            if softmax:
-                oracle.rowsoftmax_bf16(xb)
-            else:
-                oracle.rmsnorm_bf16(xb, wb, wl.eps)
-        else:
-            xn = x.numpy()
-            t0 = time.perf_counter()
-            if softmax:
-                oracle.rowsoftmax_f32(xn)
-            else:
-                oracle.rmsnorm_f32(xn, w.numpy(), wl.eps)
-        elapsed += time.perf_counter() - t0
-        done_rows += chunk_rows
-        k += 1
+            list(ex.map(lambda c: _oracle_chunk_call(oracle, wl, c, w), chunks))
+            elapsed += time.perf_counter() - t0
+            done_rows += threads * chunk_rows
+            rounds += 1
     bytes_done = (2 * done_rows * wl.hidden) * wl.elem_bytes + \
-        (0 if softmax else wl.hidden * wl.elem_bytes)
+        (0 if softmax else rounds * threads * wl.hidden * wl.elem_bytes)
+    how = ("single-thread" if threads == 1 else
+           f"{threads} host threads, one chunk each at a time,")
     return {
         "value": bytes_done / elapsed / 1e9,
         "unit": "GB/s",
         "rows_per_s": done_rows / elapsed,
-        "cores": 1,
+        "cores": threads,
         "kind": "oracle",
-        "sample": f"{done_rows} rows x {wl.hidden} of workload {wl.name} in {k} chunks "
-                  f"of {chunk_rows} rows ({elapsed:.1f} s of single-thread fp64 oracle time)",
+        "sample": f"{done_rows} rows x {wl.hidden} of workload {wl.name}: {rounds} rounds of "
+                  f"{threads} chunk(s) of {chunk_rows} rows ({elapsed:.1f} s wall clock of "
+                  f"{how} fp64 oracle)",
         "seconds": elapsed,
     }
+
+
+def cpu_baseline_line(wl):
+    """The bench line's cpu_baseline: the oracle row-parallel over all host
+    cores, with the single-thread figure beside it."""
+    par = cpu_oracle_sample(wl, budget_s=10.0, threads=host_cores())
+    one = cpu_oracle_sample(wl, budget_s=5.0, threads=1)
+    for c in (par, one):
+        c.pop("seconds", None)
+    par["single_thread"] = one
+    return par
 
 
 def run_reference(args, wl):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    budget = max(1.0, 10.0 / max(1, args.steps))
-    cb = None
+    budget = 10.0 / max(1, args.steps)      # every step runs at least one round
+    threads = host_cores()
     for _ in range(args.warmup):
-        cpu_oracle_sample(wl, budget_s=0.5, max_chunks=1)
+        cpu_oracle_sample(wl, budget_s=0.1, threads=threads, max_rounds=1)
     per = []
     for _ in range(args.steps):
-        cb = cpu_oracle_sample(wl, budget_s=budget)
-        per.append(cb)
+        per.append(cpu_oracle_sample(wl, budget_s=budget, threads=threads))
     total_bytes = sum(c["value"] * c["seconds"] for c in per)
     total_s = sum(c["seconds"] for c in per)
     value = total_bytes / total_s
@@ -254,7 +300,7 @@ def run_reference(args, wl):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_block(wl, world),
         "rows_per_s": sum(c["rows_per_s"] * c["seconds"] for c in per) / total_s,
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"{args.steps} steps, each: {per[-1]['sample']}"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -268,6 +314,14 @@ def forced(args) -> bool:
                 or args.epilogue != "none")
 
 
+def l2_note(wl, args=None) -> str:
+    if wl.bytes_per_call > 4 * 129e6:
+        return "inputs larger than L2 (no flush needed)"
+    if args is not None and args.l2 == "hot":
+        return "L2 hot: no flush between steps (inputs may be served from L2)"
+    return "L2 flushed between steps (read of a 258 MB buffer)"
+
+
 def config_block(wl, world, args=None):
     extra = {}
     if args is not None and forced(args):
@@ -279,8 +333,7 @@ def config_block(wl, world, args=None):
         "shape": list(wl.shape), "io_dtype": wl.dtype, "eps": wl.eps,
         "bytes_per_step_per_gpu": wl.bytes_per_call,
         "rows_per_step_per_gpu": wl.rows,
-        "l2": "inputs larger than L2 (no flush needed)" if wl.bytes_per_call > 4 * 129e6
-              else "L2 flushed between steps (read of a 258 MB buffer)",
+        "l2": l2_note(wl, args),
         "parallelism": f"rows replicated per GPU x{world} (independent rows, no collective)",
     }
 
@@ -331,7 +384,7 @@ def run_ours(args, wl):
     plan = (binding.rowsoftmax_plan(x, y, options=options) if softmax
             else binding.rmsnorm_plan(x, w, y, options=options))
     flush = None
-    if wl.bytes_per_call <= 4 * 129e6:
+    if wl.bytes_per_call <= 4 * 129e6 and args.l2 == "cold":
         # read-only flush: summing a 258 MB buffer evicts x and y from L2 and
         # leaves only clean lines (a write-based flush would leave ~129 MB of
         # dirty lines whose write-back then competes with the next launch)
@@ -396,8 +449,7 @@ def run_ours(args, wl):
     torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_sample(wl)
-        cpu.pop("seconds", None)
+        cpu = cpu_baseline_line(wl)
 
     if rank == 0:
         line = {
@@ -413,6 +465,8 @@ def run_ours(args, wl):
                        "vecs_per_thread": plan["vecs_per_thread"],
                        "threads_per_row": plan["threads_per_row"],
                        "launch_ms_median": per_launch_sorted[len(per_launch_sorted) // 2],
+                       "launch_ms_p10": per_launch_sorted[len(per_launch_sorted) // 10],
+                       "launch_ms_p90": per_launch_sorted[(9 * len(per_launch_sorted)) // 10],
                        "launch_ms_min": per_launch_sorted[0],
                        "launch_ms_max": per_launch_sorted[-1]},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -514,6 +568,9 @@ def main():
     ap.add_argument("--chunk", type=int, default=0, help="staged path: bytes per bulk copy")
     ap.add_argument("--epilogue", default="none", choices=["none", "scale", "relu"],
                     help="fused epilogue (measures its cost; default none)")
+    ap.add_argument("--l2", default="cold", choices=["cold", "hot"],
+                    help="cold (default): read a 258 MB buffer between steps of workloads "
+                         "that fit L2; hot: no flush, for the L2-resident figure")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()

@@ -94,6 +94,17 @@ def _as2d(x: np.ndarray, w: np.ndarray):
     return rows, hidden
 
 
+def _out(out, shape, dtype):
+    """A caller-supplied output buffer (reused across calls, so that host
+    threads running the oracle side by side do not all fault in fresh pages),
+    else a new one."""
+    if out is None:
+        return np.empty(shape, dtype=dtype)
+    if out.shape != tuple(shape) or out.dtype != dtype or not out.flags.c_contiguous:
+        raise ValueError(f"output buffer must be a contiguous {dtype} array of shape {shape}")
+    return out
+
+
 def _check(status: int):
     if status != 0:
         raise ValueError(f"oracle rejected the arguments (status {status})")
@@ -110,32 +121,35 @@ def rmsnorm_f64(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
     return y
 
 
-def rmsnorm_f32(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
-    """binary32 inputs (widened exactly), binary64 result of the same shape."""
+def rmsnorm_f32(x: np.ndarray, w: np.ndarray, eps: float, out=None) -> np.ndarray:
+    """binary32 inputs (widened exactly), binary64 result of the same shape
+    (written into ``out`` when given)."""
     x = np.ascontiguousarray(x)
     w = np.ascontiguousarray(w)
     if x.dtype != np.float32 or w.dtype != np.float32:
         raise TypeError("rmsnorm_f32 takes float32 arrays")
     rows, hidden = _as2d(x, w)
-    y = np.empty(x.shape, dtype=np.float64)
+    y = _out(out, x.shape, np.float64)
     _check(_load().oracle_rmsnorm_f32(_ptr(x), _ptr(w), _ptr(y), rows,
                                       hidden, float(eps)))
     return y
 
 
-def rmsnorm_bf16(x_bits: np.ndarray, w_bits: np.ndarray, eps: float):
+def rmsnorm_bf16(x_bits: np.ndarray, w_bits: np.ndarray, eps: float,
+                 out64=None, out16=None):
     """bfloat16 bit patterns (uint16) in.
 
     Returns ``(y64, y16)``: the binary64 result and its single
-    round-to-nearest-even rounding to bfloat16 bits.
+    round-to-nearest-even rounding to bfloat16 bits (written into ``out64``
+    and ``out16`` when given).
     """
     x_bits = np.ascontiguousarray(x_bits)
     w_bits = np.ascontiguousarray(w_bits)
     if x_bits.dtype != np.uint16 or w_bits.dtype != np.uint16:
         raise TypeError("rmsnorm_bf16 takes uint16 bit patterns")
     rows, hidden = _as2d(x_bits, w_bits)
-    y64 = np.empty(x_bits.shape, dtype=np.float64)
-    y16 = np.empty(x_bits.shape, dtype=np.uint16)
+    y64 = _out(out64, x_bits.shape, np.float64)
+    y16 = _out(out16, x_bits.shape, np.uint16)
     _check(_load().oracle_rmsnorm_bf16(_ptr(x_bits), _ptr(w_bits), _ptr(y64),
                                        _ptr(y16), rows, hidden, float(eps)))
     return y64, y16
@@ -206,25 +220,26 @@ def rowsoftmax_f64(x: np.ndarray) -> np.ndarray:
     return y
 
 
-def rowsoftmax_f32(x: np.ndarray) -> np.ndarray:
-    """binary32 input (widened exactly), binary64 result."""
+def rowsoftmax_f32(x: np.ndarray, out=None) -> np.ndarray:
+    """binary32 input (widened exactly), binary64 result (into ``out`` when given)."""
     x = np.ascontiguousarray(x)
     if x.dtype != np.float32:
         raise TypeError("rowsoftmax_f32 takes float32")
     rows, cols = _rows_cols(x)
-    y = np.empty(x.shape, dtype=np.float64)
+    y = _out(out, x.shape, np.float64)
     _check(_load().oracle_rowsoftmax_f32(_ptr(x), _ptr(y), rows, cols))
     return y
 
 
-def rowsoftmax_bf16(x_bits: np.ndarray):
-    """bfloat16 bits in; returns (y64, y16) with y16 the single RNE rounding."""
+def rowsoftmax_bf16(x_bits: np.ndarray, out64=None, out16=None):
+    """bfloat16 bits in; returns (y64, y16) with y16 the single RNE rounding
+    (written into ``out64`` and ``out16`` when given)."""
     x_bits = np.ascontiguousarray(x_bits)
     if x_bits.dtype != np.uint16:
         raise TypeError("rowsoftmax_bf16 takes uint16 bit patterns")
     rows, cols = _rows_cols(x_bits)
-    y64 = np.empty(x_bits.shape, dtype=np.float64)
-    y16 = np.empty(x_bits.shape, dtype=np.uint16)
+    y64 = _out(out64, x_bits.shape, np.float64)
+    y16 = _out(out16, x_bits.shape, np.uint16)
     _check(_load().oracle_rowsoftmax_bf16(_ptr(x_bits), _ptr(y64), _ptr(y16), rows, cols))
     return y64, y16
 

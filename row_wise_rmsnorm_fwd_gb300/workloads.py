@@ -17,6 +17,7 @@ c1         (1, 32, 2048)            f32    N(0,1)            N(1,0.1)         1e
 c2         (1, 128, 2048)           f32    N(0,1)            N(1,0.1)         1e-5
 c2t        (1, 128, 2050)           f32    N(0,1)            N(1,0.1)         1e-5
 c3         (4, 512, 3584)           f32    N(0,1), 36 outlier columns x50     1e-6
+c3e        (4, 512, 3584)           f32    N(0,1), 1% of entries x50          1e-6
 c4         (65536, 4096)            f32    N(0,1)            U(0.5,1.5)       1e-6
 c5a        (262144, 8192)           bf16   N(0,2) (std 2)    N(1,0.1)         1e-6
 c5b        (8, 262144)              bf16   N(0,2)            N(1,0.1)         1e-6
@@ -33,10 +34,12 @@ adds the model-shaped batch x seq grid (see below).
 
 Readings: "N(0,2)" is mean 0, standard deviation 2; the Qwen-shaped case's
 "1% outlier channels" are round(0.01*3584) = 36 whole columns, picked by a
-seeded permutation and multiplied by 50 in every row.  bf16 values are drawn
+seeded permutation and multiplied by 50 in every row; c3e is the other
+reading of the same phrase, 1% of the entries picked independently (each
+with probability 0.01, seeded) and multiplied by 50.  bf16 values are drawn
 in fp32 and rounded to bf16 by torch's round-to-nearest-even cast.
 
-Seeds: x uses 1000+k, w uses 2000+k, the outlier columns 3000+k, where k is
+Seeds: x uses 1000+k, w uses 2000+k, the outliers 3000+k, where k is
 the workload's index in the table.  On the CPU the draws are bit-reproducible;
 ``device="cuda"`` draws from torch's CUDA generator with the same seed (a
 different but equally seeded stream), used where the full tensor is too large
@@ -59,6 +62,7 @@ class Workload:
     w_dist: tuple         # ("normal", mean, std) or ("uniform", lo, hi)
     eps: float
     outlier_cols: int = 0
+    outlier_frac: float = 0.0   # fraction of i.i.d. entries scaled by outlier_scale
     outlier_scale: float = 1.0
     description: str = ""
     op: str = "rmsnorm"   # "rmsnorm" or "softmax" (softmax has no weight)
@@ -100,6 +104,10 @@ WORKLOADS = {
                  ("normal", 1.0, 0.1), 1e-6, outlier_cols=36,
                  outlier_scale=50.0,
                  description="Qwen2.5-7B-shaped (4,512,3584), 36 outlier columns x50"),
+        Workload("c3e", 8, (4, 512, 3584), "f32", ("normal", 0.0, 1.0),
+                 ("normal", 1.0, 0.1), 1e-6, outlier_frac=0.01,
+                 outlier_scale=50.0,
+                 description="Qwen2.5-7B-shaped (4,512,3584), 1% of entries x50"),
         Workload("c4", 3, (65536, 4096), "f32", ("normal", 0.0, 1.0),
                  ("uniform", 0.5, 1.5), 1e-6,
                  description="bandwidth-bound fp32 (65536,4096)"),
@@ -208,6 +216,10 @@ def make_x(wl: Workload, device: str = "cpu", rows: int | None = None,
     if wl.outlier_cols:
         cols = outlier_columns(wl).to(device)
         x[..., cols] *= wl.outlier_scale
+    if wl.outlier_frac:
+        go = _generator(3000 + wl.index + seed_offset, device)
+        hit = torch.rand(shape, generator=go, device=device) < wl.outlier_frac
+        x[hit] *= wl.outlier_scale
     return x.to(_torch_dtype(wl.dtype))
 
 

@@ -78,6 +78,53 @@ def check_bf16(bits_gpu: np.ndarray, bits_ref: np.ndarray, what: str = ""):
             f"ref 0x{int(bits_ref[ok][i]):04x} ({int(d[i])} ulp)")
 
 
+def compare_every_row(x_dev: torch.Tensor, y_dev: torch.Tensor, w_cpu: torch.Tensor,
+                      eps: float, what: str = "", chunk_rows: int = 16384,
+                      piece_elems: int = 1 << 20, threads: int = 0):
+    """Check every row of a full-size GPU result against the oracle.
+
+    Rows are copied to the host in chunks of ``chunk_rows``; each chunk is cut
+    into pieces of about ``piece_elems`` elements that host threads run
+    through the oracle and the comparison at the same time (the oracle is a C
+    library called through ctypes, which releases the interpreter lock, and
+    numpy's element-wise kernels release it too).  Small pieces keep numpy's
+    temporaries in the allocator's reused heap instead of fresh pages."""
+    import concurrent.futures as cf
+    import os
+
+    import threading
+
+    rows, hidden = x_dev.shape
+    piece_rows = max(1, piece_elems // hidden)
+    threads = threads or max(1, len(os.sched_getaffinity(0)))
+    f32 = x_dev.dtype == torch.float32
+    w_host = w_cpu.numpy() if f32 else workloads.bf16_bits(w_cpu)
+    local = threading.local()
+
+    def piece(args):
+        xs, ys, lo = args
+        # per-thread output buffers, reused: threads faulting in fresh pages
+        # side by side are serialised by the host kernel
+        bufs = getattr(local, "bufs", None)
+        if bufs is None or bufs[0].shape != tuple(xs.shape):
+            bufs = (np.zeros(tuple(xs.shape), np.float64), np.zeros(tuple(xs.shape), np.uint16))
+            local.bufs = bufs
+        if f32:
+            ref = oracle.rmsnorm_f32(xs.numpy(), w_host, eps, out=bufs[0])
+        else:
+            _, ref = oracle.rmsnorm_bf16(workloads.bf16_bits(xs), w_host, eps,
+                                         out64=bufs[0], out16=bufs[1])
+        compare(ys, ref, f"{what} rows {lo}..{lo + xs.shape[0] - 1}")
+
+    with cf.ThreadPoolExecutor(threads) as ex:
+        for a in range(0, rows, chunk_rows):
+            b = min(rows, a + chunk_rows)
+            xc, yc = x_dev[a:b].cpu(), y_dev[a:b].cpu()
+            jobs = [(xc[p:p + piece_rows], yc[p:p + piece_rows], a + p)
+                    for p in range(0, b - a, piece_rows)]
+            list(ex.map(piece, jobs))
+
+
 def compare(y_gpu: torch.Tensor, ref, what: str = ""):
     """Compare a GPU result (any device) with the oracle's output for it."""
     y = y_gpu.detach().cpu().contiguous()

@@ -19,10 +19,20 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(out[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["higher_is_better"] is True and d["steps"] == 3 and d["warmup"] == 3
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["cpu_baseline"]["cores"] == bench.host_cores()
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert d["config"]["workload"].startswith("c1")
+
+
+def test_cpu_baseline_is_row_parallel_with_single_thread_beside_it():
+    from row_wise_rmsnorm_fwd_gb300 import workloads
+    d = bench.cpu_baseline_line(workloads.WORKLOADS["c1"])
+    assert d["kind"] == "oracle" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cores"] == bench.host_cores() and "seconds" not in d
+    one = d["single_thread"]
+    assert one["cores"] == 1 and one["value"] > 0 and "single-thread" in one["sample"]
 
 
 def test_reference_arm_softmax_workload():

@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from _parity import compare, oracle_for
+from _parity import compare, compare_every_row, oracle_for
 from row_wise_rmsnorm_fwd_gb300 import binding, build, workloads
 
 pytestmark = pytest.mark.gpu
@@ -58,14 +58,14 @@ def check_case(x_cpu, w_cpu, eps, what, **opts):
 
 # ------------------------------------------------------------- workloads --
 
-@pytest.mark.parametrize("name", ["c1", "c2", "c2t", "c3", "c5b"])
+@pytest.mark.parametrize("name", ["c1", "c2", "c2t", "c3", "c3e", "c5b"])
 def test_workload_full(name):
     wl = workloads.WORKLOADS[name]
     x, w = workloads.make_x(wl), workloads.make_w(wl)
     check_case(x, w, wl.eps, name)
 
 
-@pytest.mark.parametrize("name", ["c1", "c2", "c2t", "c3"])
+@pytest.mark.parametrize("name", ["c1", "c2", "c2t", "c3", "c3e"])
 def test_workload_page_schedule(name):
     """The write-up's own schedule, rebuilt as a comparison kernel, on the
     workloads it fits (the page's example is c1)."""
@@ -75,22 +75,18 @@ def test_workload_page_schedule(name):
 
 
 @pytest.mark.parametrize("name", ["c4", "c5a"])
-def test_workload_full_size_sampled_rows(name):
+def test_workload_full_size_every_row(name):
     """Full-size workload in the bench's launch configuration (automatic
-    path, current stream); full rows sampled and checked against the oracle."""
+    path, current stream, inputs drawn on the device); every row is checked
+    against the oracle, 16384 rows at a time, on all host cores."""
     wl = workloads.WORKLOADS[name]
     x = workloads.make_x(wl, device="cuda")
     w = workloads.make_w(wl, device="cuda")
     y = run(x, w, wl.eps)
     rows, hidden = wl.rows, wl.hidden
-    x2, y2 = x.view(rows, hidden), y.view(rows, hidden)
-    g = torch.Generator().manual_seed(5)
-    pick = torch.cat([torch.arange(64), torch.arange(rows - 64, rows),
-                      torch.randint(0, rows, (768,), generator=g)]).unique()
-    xs = x2[pick.cuda()].cpu()
-    ref = oracle_for(xs, w.cpu(), wl.eps)
-    compare(y2[pick.cuda()], ref, f"{name} sampled rows")
-    del x, y, x2, y2
+    compare_every_row(x.view(rows, hidden), y.view(rows, hidden), w.cpu(), wl.eps,
+                      f"{name} full size")
+    del x, y
     torch.cuda.empty_cache()
 
 

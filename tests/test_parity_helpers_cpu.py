@@ -1,0 +1,42 @@
+"""The every-row checker used on the full-size workloads, exercised on the
+CPU: with the oracle's own result it passes, and one planted bad element in
+any chunk or piece (including the ragged last ones) is found and located."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _parity import compare_every_row
+from row_wise_rmsnorm_fwd_gb300 import workloads
+
+
+def _case(dtype, rows=300, hidden=257, seed=11):
+    x = workloads.make_random((rows, hidden), dtype, seed)
+    w = workloads.make_random((hidden,), dtype, seed + 1, ("normal", 1.0, 0.1))
+    if dtype == "f32":
+        y = torch.from_numpy(oracle.rmsnorm_f32(x.numpy(), w.numpy(), 1e-6).astype(np.float32))
+    else:
+        _, y16 = oracle.rmsnorm_bf16(workloads.bf16_bits(x), workloads.bf16_bits(w), 1e-6)
+        y = workloads.from_bf16_bits(y16)
+    return x, w, y
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_every_row_passes_on_the_oracle_result(dtype):
+    x, w, y = _case(dtype)
+    compare_every_row(x, y, w, 1e-6, "clean", chunk_rows=128, piece_elems=40 * 257, threads=3)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("row", [0, 127, 128, 255, 299])
+def test_every_row_finds_one_bad_element(dtype, row):
+    x, w, y = _case(dtype)
+    y[row, 200] = y[row, 200] * 1.25 + 0.5
+    with pytest.raises(AssertionError) as e:
+        compare_every_row(x, y, w, 1e-6, "planted", chunk_rows=128, piece_elems=40 * 257,
+                          threads=3)
+    lo = int(str(e.value).split("rows ")[1].split("..")[0])
+    hi = int(str(e.value).split("..")[1].split(":")[0])
+    assert lo <= row <= hi
