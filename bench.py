@@ -311,7 +311,7 @@ def run_reference(args, wl):
 
 def forced(args) -> bool:
     return bool(args.path != "auto" or args.cluster or args.grid or args.threads or args.chunk
-                or args.epilogue != "none")
+                or args.stages or args.epilogue != "none")
 
 
 def l2_note(wl, args=None) -> str:
@@ -327,7 +327,7 @@ def config_block(wl, world, args=None):
     if args is not None and forced(args):
         extra["forced"] = {"path": args.path, "cluster": args.cluster, "grid": args.grid,
                            "threads": args.threads, "chunk_bytes": args.chunk,
-                           "epilogue": args.epilogue}
+                           "stages": args.stages, "epilogue": args.epilogue}
     return {**extra,
         "workload": f"{wl.name}: {wl.description}",
         "shape": list(wl.shape), "io_dtype": wl.dtype, "eps": wl.eps,
@@ -363,10 +363,12 @@ def run_ours(args, wl):
     handle = stream.cuda_stream
     options = None
     if softmax:
+        staged = args.path == "staged"
         options = binding.make_options(
-            path=args.path if args.path in ("rowreg", "twopass", "cluster") else "auto",
+            path=args.path if args.path in ("rowreg", "twopass", "cluster", "staged") else "auto",
             cluster=args.cluster if args.path == "cluster" else 0,
-            grid=args.grid, threads=args.threads)
+            grid=args.grid, threads=args.threads,
+            chunk_bytes=args.chunk if staged else 0, stages=args.stages if staged else 0)
         dt_code = binding.RMSNORM_DTYPE_BF16 if wl.dtype == "bf16" else binding.RMSNORM_DTYPE_F32
 
         def fwd(xp, wp, yp, r, h, eps, s):
@@ -374,7 +376,7 @@ def run_ours(args, wl):
     elif forced(args):
         options = binding.make_options(path=args.path, cluster=args.cluster, grid=args.grid,
                                        threads=args.threads, chunk_bytes=args.chunk,
-                                       epilogue=args.epilogue, alpha=0.5)
+                                       stages=args.stages, epilogue=args.epilogue, alpha=0.5)
         dt_code = binding.RMSNORM_DTYPE_BF16 if wl.dtype == "bf16" else binding.RMSNORM_DTYPE_F32
 
         def fwd(xp, wp, yp, r, h, eps, s):
@@ -566,6 +568,7 @@ def main():
     ap.add_argument("--grid", type=int, default=0, help="force the CTA count")
     ap.add_argument("--threads", type=int, default=0, help="force threads per row group")
     ap.add_argument("--chunk", type=int, default=0, help="staged path: bytes per bulk copy")
+    ap.add_argument("--stages", type=int, default=0, help="staged path: ring slots")
     ap.add_argument("--epilogue", default="none", choices=["none", "scale", "relu"],
                     help="fused epilogue (measures its cost; default none)")
     ap.add_argument("--l2", default="cold", choices=["cold", "hot"],

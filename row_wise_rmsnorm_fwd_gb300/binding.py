@@ -333,7 +333,8 @@ def rowsoftmax_fwd_bf16(x, y=None, stream=None):
 
 
 def rowsoftmax_fwd_ex(x, y=None, options=None, stream=None):
-    """Either dtype with options (path auto / rowreg / twopass, threads, grid)."""
+    """Either dtype with options (path auto / rowreg / cluster / staged /
+    twopass, threads, grid; chunk_bytes and stages for the staged path)."""
     torch = _torch()
     if y is None:
         y = torch.empty_like(x)

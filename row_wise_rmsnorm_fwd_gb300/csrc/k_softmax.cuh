@@ -2,11 +2,12 @@
 //
 // y[r,j] = exp(x[r,j] - m[r]) / sum_k exp(x[r,k] - m[r]),  m[r] = max_k x[r,k]
 //
-// exp(x - m) is evaluated as exp2f(x*log2(e) - m*log2(e)) with one fused
-// multiply-add: CUDA's exp2f maps to the SFU's base-2 exponential, several
-// times cheaper than expf, which keeps the bf16 variant from becoming
-// instruction-bound; the identity exp(t) = 2^(t*log2 e) costs at most
-// |m|*log2(e)*2^-24 absolute error in the exponent.
+// exp(x - m) is evaluated as 2^(x*log2(e) - m*log2(e)) with one fused
+// multiply-add and a base-2 exponential (exp2f for fp32 rows, a single SFU
+// instruction for bf16 rows: see row_exp), much cheaper than expf, which
+// keeps the kernels from becoming instruction-bound; the identity exp(t) =
+// 2^(t*log2 e) costs at most |m|*log2(e)*2^-24 absolute error in the
+// exponent, a factor common to the whole row.
 //
 // The second small reduction the compiler write-up ("A hackable Python ML
 // compiler, part 2") lists among its wins, built from the same parts as the
@@ -17,11 +18,13 @@
 // each output rounded once.  IEEE special cases follow the definition: -inf
 // entries give 0, a row of -inf or any NaN or +inf gives a NaN row.
 //
-// softmax_threepass_kernel serves rows too wide for registers: one CTA per
-// row reads x three times (max, sum, write); the second and third reads are
-// normally served by L2.
+// softmax_staged_kernel brings rows in through the bulk-copy slot ring
+// (k_ring.cuh) and holds each in registers, so that the next rows are already
+// in flight while a row's reductions run; softmax_threepass_kernel serves
+// rows too wide for registers: one CTA per row reads x three times (max, sum,
+// write), the second and third reads normally served by L2.
 #pragma once
-#include "common.cuh"
+#include "k_ring.cuh"
 
 namespace rmsnorm {
 
@@ -30,6 +33,34 @@ constexpr float kLog2e = 1.4426950408889634f;
 // exp(v - m) as 2^(v*log2e - m*log2e); ml2e = m * log2e.
 __device__ __forceinline__ float exp_shifted(float v, float ml2e) {
     return exp2f(fmaf(v, kLog2e, -ml2e));
+}
+
+// The register and staged kernels evaluate every exponential of a row as
+// 2^(v*log2e + c) with a per-row constant c = row_exp_bias<T>() - m*log2e.
+//   fp32: exp2f, bias 0: e = exp(v - m) itself.
+//   bf16: the PTX instruction ex2.approx.ftz.f32 (one SFU operation,
+//     relative error about 2^-22, far below bf16's 2^-9), with bias 8: every
+//     exponential is scaled by 2^8, which cancels in e / sum, and keeps each
+//     one whose output a bf16 can resolve (e >= 2^-133, since sum >= 1) a
+//     normal number, so that flushing subnormal results to zero loses
+//     nothing.  Any rounding of c is a common factor of the row and cancels
+//     too.  exp2f costs several instructions more per element, and bf16 rows
+//     carry twice the elements per byte.
+template <typename T>
+__device__ __forceinline__ float row_exp_bias() {
+    return sizeof(T) == 2 ? 8.0f : 0.0f;
+}
+
+template <typename T>
+__device__ __forceinline__ float row_exp(float v, float c) {
+    const float a = fmaf(v, kLog2e, c);
+    if constexpr (sizeof(T) == 2) {
+        float r;
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+        return r;
+    } else {
+        return exp2f(a);
+    }
 }
 
 __device__ __forceinline__ float warp_allreduce_max(float v) {
@@ -43,10 +74,13 @@ constexpr int softmax_max_threads() { return NV >= 4 ? 512 : 1024; }
 
 // PF: the next row's loads are issued before this row's two reductions
 // (register double buffer), doubling the bytes in flight for narrow rows.
-// With p.cluster > 1 a thread-block cluster of C CTAs shares each row: every
-// CTA holds a slice, and the row maximum and the row sum are each combined
-// across the cluster through distributed shared memory (bounded waits).
-template <typename T, int VB, int NV, bool PF>
+// CL: a thread-block cluster of p.cluster CTAs shares each row: every CTA
+// holds a slice, and the row maximum and the row sum are each combined across
+// the cluster through distributed shared memory (bounded waits).  A compile-
+// time switch, so that the plain instances carry none of the cluster code
+// (measured: with the cluster branches present but idle, 1 KB bf16 rows ran
+// about 8% slower).
+template <typename T, int VB, int NV, bool PF, bool CL>
 __global__ void __launch_bounds__(softmax_max_threads<NV>())
 softmax_rowreg_kernel(const Params p) {
     constexpr int EPV = VecTraits<T, VB>::kElems;
@@ -61,17 +95,17 @@ softmax_rowreg_kernel(const Params p) {
     const int wpg = G >> 5;
     const int gw0 = g * wpg;
 
-    const int ncta = p.cluster;
+    const int ncta = CL ? p.cluster : 1;
     uint32_t rank = 0;
     int64_t unit = blockIdx.x, nunits = gridDim.x;
-    if (ncta > 1) {
+    if (CL) {
         rank = cluster_ctarank();
         unit = cluster_id_x();
         nunits = cluster_count_x();
         cluster_exchange_init(&exmax, ncta, &exsum);
     }
-    const int vbase = (ncta > 1) ? static_cast<int>(rank) * p.slice_vecs : 0;
-    const int vlim = (ncta > 1) ? min(p.nvec, vbase + p.slice_vecs) : p.nvec;
+    const int vbase = CL ? static_cast<int>(rank) * p.slice_vecs : 0;
+    const int vlim = CL ? min(p.nvec, vbase + p.slice_vecs) : p.nvec;
     int vidx[NV];
     bool valid[NV];
 #pragma unroll
@@ -106,7 +140,7 @@ softmax_rowreg_kernel(const Params p) {
         const bool row_ok = row < p.rows;
         const int b = it & 1;
         float e[NV][EPV];
-        float m = -INFINITY;
+        float mk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // 4 independent chains
         if (row_ok) {
 #pragma unroll
             for (int i = 0; i < NV; ++i) {
@@ -114,11 +148,12 @@ softmax_rowreg_kernel(const Params p) {
 #pragma unroll
                     for (int k = 0; k < EPV; ++k) {
                         e[i][k] = get<T, VB>(cur[i], k);
-                        m = fmaxf(m, e[i][k]);
+                        mk[k & 3] = fmaxf(mk[k & 3], e[i][k]);
                     }
                 }
             }
         }
+        float m = fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3]));
         // row maximum
         m = warp_allreduce_max(m);
         if (wpg > 1) {
@@ -127,35 +162,35 @@ softmax_rowreg_kernel(const Params p) {
             m = -INFINITY;
             for (int k = 0; k < wpg; ++k) m = fmaxf(m, red[0][b][gw0 + k]);
         }
-        if (ncta > 1) {
+        if (CL) {
             float cm;
             const bool ok = cluster_allreduce<true>(&exmax, m, ncta, rank, it, p, &cm, tid);
             m = cm;
             if (__syncthreads_or(!ok)) break;   // uniform: stop, then leave cleanly
         }
         // exponentials and their sum
-        const float ml2e = m * kLog2e;
-        float s0 = 0.f, s1 = 0.f;
+        const float c = row_exp_bias<T>() - m * kLog2e;
+        float sk[4] = {0.f, 0.f, 0.f, 0.f};
         if (row_ok) {
 #pragma unroll
             for (int i = 0; i < NV; ++i) {
                 if (valid[i]) {
 #pragma unroll
                     for (int k = 0; k < EPV; ++k) {
-                        e[i][k] = exp_shifted(e[i][k], ml2e);
-                        if (k & 1) s1 += e[i][k]; else s0 += e[i][k];
+                        e[i][k] = row_exp<T>(e[i][k], c);
+                        sk[k & 3] += e[i][k];
                     }
                 }
             }
         }
-        float s = warp_allreduce_sum(s0 + s1);
+        float s = warp_allreduce_sum((sk[0] + sk[1]) + (sk[2] + sk[3]));
         if (wpg > 1) {
             if (lane == 0) red[1][b][warp] = s;
             __syncthreads();
             s = 0.f;
             for (int k = 0; k < wpg; ++k) s += red[1][b][gw0 + k];
         }
-        if (ncta > 1) {
+        if (CL) {
             float cs;
             const bool ok = cluster_allreduce(&exsum, s, ncta, rank, it, p, &cs, tid);
             s = cs;
@@ -182,7 +217,152 @@ softmax_rowreg_kernel(const Params p) {
         }
     }
     // Keep this CTA's shared memory alive until every peer is done with it.
-    if (ncta > 1) cluster_sync_all();
+    if (CL) cluster_sync_all();
+}
+
+// Rows staged in shared memory, then held in registers.  The CTA's rows
+// stream through the slot ring in chunks (chunk n of the stream in slot
+// n % S); every thread waits for a row's chunks, copies its NV vectors into
+// registers (widened to fp32), and after the block's first reduction barrier
+// -- every thread has its copy by then -- thread 0 refills the row's slots
+// with chunks n + S.  The following rows' loads are thus in flight through
+// the whole computation of a row (maximum, exponentials, sum, outputs from
+// registers) without taking registers: the register kernel's prefetch needs a
+// second register copy of the row, which does not fit for rows of 16 KB and
+// more.  No producer warp: 16 warps of 128 registers fill an SM's register
+// file, where a 17th warp would cap every thread at 96.  Thread t owns
+// vectors t, t + blockDim.x, ...; chunk_bytes is a power of two unless a row
+// fits one chunk.
+constexpr int kSoftmaxStagedMaxThreads = 512;
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kernel(const Params p) {
+    constexpr int EPV = 16 / static_cast<int>(sizeof(T));
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    float* red = reinterpret_cast<float*>(smem + 8 * kStagedMaxSlots);   // [max|sum][buffer][warp]
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int NT = blockDim.x;
+    const int NW = NT >> 5;
+    const int NCH = p.nchunks;
+    const int S = p.nslots;
+    const int CB = p.chunk_bytes;
+    const int64_t row_bytes = static_cast<int64_t>(p.hidden) * sizeof(T);
+    const SlotRing ring{full, nullptr, smem + kStagedHeader, S, NCH, CB, row_bytes};
+    const int64_t unit = blockIdx.x, nunits = gridDim.x;
+    const uint64_t policy = policy_evict_first();
+
+    int64_t issued = 0;            // chunks issued so far (thread 0's count)
+    RingCursor cur{unit, 0, 0};    // the next chunk to issue (thread 0)
+    if (tid == 0) {
+        for (int k = 0; k < S; ++k) mbar_init(smem_addr(&full[k]), 1);
+        fence_mbarrier_init_cluster();
+        while (issued < S && ring_issue_next(p, ring, cur, nunits, row_bytes, policy)) ++issued;
+    }
+    __syncthreads();
+
+    const int shift = (CB & (CB - 1)) == 0 ? __ffs(CB) - 1 : 31;
+    int kidx[NV], off[NV];
+    bool valid[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int v = i * NT + tid;
+        valid[i] = v < p.nvec;
+        kidx[i] = (v * 16) >> shift;                   // chunk of the row holding vector v
+        off[i] = v * 16 - (kidx[i] << shift);           // its byte offset in that chunk
+    }
+    char* yb = static_cast<char*>(p.y);
+    uint32_t it = 0;
+    int64_t base = 0;              // stream index of this row's chunk 0
+    int slot0 = 0;                 // its slot, base % S
+    uint32_t lap0 = 0;             // its phase parity, (base / S) & 1
+    for (int64_t row = unit; row < p.rows; row += nunits, ++it, base += NCH) {
+        const int b = it & 1;
+        bool ok = true;
+        for (int k = 0; k < NCH; ++k) {
+            int sl = slot0 + k;
+            uint32_t par = lap0;
+            if (sl >= S) {
+                sl -= S;
+                par ^= 1u;
+            }
+            if (!mbar_wait_bounded<false>(smem_addr(&full[sl]), par, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+        }
+        float e[NV][EPV];
+        float mk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // 4 independent chains
+        if (ok) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                if (valid[i]) {
+                    int slot = slot0 + kidx[i];
+                    if (slot >= S) slot -= S;
+                    const Vec<16> xv = as_vec(*reinterpret_cast<const uint4*>(
+                        ring.slots + static_cast<int64_t>(slot) * CB + off[i]));
+#pragma unroll
+                    for (int k = 0; k < EPV; ++k) {
+                        e[i][k] = get<T, 16>(xv, k);
+                        mk[k & 3] = fmaxf(mk[k & 3], e[i][k]);
+                    }
+                }
+            }
+        }
+        float m = warp_allreduce_max(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])));
+        if (lane == 0) red[b * 32 + warp] = m;
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) report_timeout(p.status, kSiteStagedFull);
+            break;
+        }
+        // every thread holds its part of the row: refill the row's slots
+        if (tid == 0)
+            while (issued < base + NCH + S &&
+                   ring_issue_next(p, ring, cur, nunits, row_bytes, policy))
+                ++issued;
+        slot0 += NCH;              // NCH <= S: one wrap at most
+        if (slot0 >= S) {
+            slot0 -= S;
+            lap0 ^= 1u;
+        }
+        m = -INFINITY;
+        for (int k = 0; k < NW; ++k) m = fmaxf(m, red[b * 32 + k]);
+        const float c = row_exp_bias<T>() - m * kLog2e;
+        float sk[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            if (valid[i]) {
+#pragma unroll
+                for (int k = 0; k < EPV; ++k) {
+                    e[i][k] = row_exp<T>(e[i][k], c);
+                    sk[k & 3] += e[i][k];
+                }
+            }
+        }
+        float sum = warp_allreduce_sum((sk[0] + sk[1]) + (sk[2] + sk[3]));
+        if (lane == 0) red[64 + b * 32 + warp] = sum;
+        __syncthreads();
+        sum = 0.f;
+        for (int k = 0; k < NW; ++k) sum += red[64 + b * 32 + k];
+        const float inv = 1.0f / sum;
+        char* dst = yb + row * row_bytes;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            if (valid[i]) {
+                float o[EPV];
+#pragma unroll
+                for (int k = 0; k < EPV; ++k) o[k] = e[i][k] * inv;
+                st_stream<16>(dst + static_cast<int64_t>(i * NT + tid) * 16, pack<T, 16>(o));
+            }
+        }
+    }
+    // After a timeout, copies may still be in flight: wait (bounded) for the
+    // last S issued before the CTA leaves.  Normally every one was consumed.
+    if (tid == 0)
+        for (int64_t n = issued > S ? issued - S : 0; n < issued; ++n)
+            ring_wait_full(ring, n, p.timeout_ns);
 }
 
 constexpr int kSoftmaxWideThreads = 1024;

@@ -29,11 +29,17 @@ KernelFn rowreg_kernel_ptr(int dtype, int vb, int nv, bool pf, int epi);
 int rowreg_max_block(int nv);
 KernelFn twopass_kernel_ptr(int dtype, int vb, int epi);
 int twopass_block();
-// Row softmax: register-resident kernel and the three-pass wide-row kernel.
-KernelFn softmax_rowreg_ptr(int dtype, int vb, int nv);
+// Row softmax: register-resident kernel (cluster = rows split over a
+// thread-block cluster) and the three-pass wide-row kernel.
+KernelFn softmax_rowreg_ptr(int dtype, int vb, int nv, bool cluster);
 int softmax_rowreg_max_block(int nv);
 KernelFn softmax_threepass_ptr(int dtype, int vb);
 int softmax_threepass_block();
+// Row softmax staged in shared memory and held in registers: up to 512
+// threads of nv 16-byte vectors each (fp32: 4, 8 or 16; bf16: 2, 4 or 8);
+// dynamic shared memory = kStagedHeaderHost + nslots * chunk bytes.
+KernelFn softmax_staged_ptr(int dtype, int nv);
+int softmax_staged_max_threads();
 
 // Comparison kernel with the compiler write-up's schedule (one CTA per row).
 KernelFn page_kernel_ptr(int dtype);

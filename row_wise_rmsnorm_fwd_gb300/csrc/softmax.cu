@@ -6,34 +6,38 @@ namespace rmsnorm {
 
 // Rows of up to two vectors per thread prefetch the next row (cheap in
 // registers, and narrow rows are where a warp has too few bytes in flight).
-template <typename T, int VB>
+template <typename T, int VB, bool CL>
 static KernelFn softmax_pick_nv(int nv) {
     if constexpr (VB < static_cast<int>(sizeof(T))) {
         return nullptr;
     } else {
         switch (nv) {
-            case 1: return softmax_rowreg_kernel<T, VB, 1, true>;
-            case 2: return softmax_rowreg_kernel<T, VB, 2, true>;
-            case 4: return softmax_rowreg_kernel<T, VB, 4, false>;
-            case 8: return softmax_rowreg_kernel<T, VB, 8, false>;
+            case 1: return softmax_rowreg_kernel<T, VB, 1, true, CL>;
+            case 2: return softmax_rowreg_kernel<T, VB, 2, true, CL>;
+            case 4: return softmax_rowreg_kernel<T, VB, 4, false, CL>;
+            case 8: return softmax_rowreg_kernel<T, VB, 8, false, CL>;
             default: return nullptr;
         }
     }
 }
 
-template <typename T>
+template <typename T, bool CL>
 static KernelFn softmax_pick(int vb, int nv) {
     switch (vb) {
-        case 16: return softmax_pick_nv<T, 16>(nv);
-        case 8: return softmax_pick_nv<T, 8>(nv);
-        case 4: return softmax_pick_nv<T, 4>(nv);
-        case 2: return softmax_pick_nv<T, 2>(nv);
+        case 16: return softmax_pick_nv<T, 16, CL>(nv);
+        case 8: return softmax_pick_nv<T, 8, CL>(nv);
+        case 4: return softmax_pick_nv<T, 4, CL>(nv);
+        case 2: return softmax_pick_nv<T, 2, CL>(nv);
         default: return nullptr;
     }
 }
 
-KernelFn softmax_rowreg_ptr(int dtype, int vb, int nv) {
-    return dtype == 0 ? softmax_pick<float>(vb, nv) : softmax_pick<__nv_bfloat16>(vb, nv);
+KernelFn softmax_rowreg_ptr(int dtype, int vb, int nv, bool cluster) {
+    if (cluster)
+        return dtype == 0 ? softmax_pick<float, true>(vb, nv)
+                          : softmax_pick<__nv_bfloat16, true>(vb, nv);
+    return dtype == 0 ? softmax_pick<float, false>(vb, nv)
+                      : softmax_pick<__nv_bfloat16, false>(vb, nv);
 }
 
 int softmax_rowreg_max_block(int nv) { return nv >= 4 ? 512 : 1024; }
@@ -56,5 +60,28 @@ KernelFn softmax_threepass_ptr(int dtype, int vb) {
 }
 
 int softmax_threepass_block() { return kSoftmaxWideThreads; }
+
+static_assert(8 * kStagedMaxSlots + 4 * 32 * sizeof(float) <= kStagedHeader,
+              "staged softmax header overflows");
+
+// Vectors per consumer thread: up to 64 fp32 values of a row in registers.
+KernelFn softmax_staged_ptr(int dtype, int nv) {
+    if (dtype == 0) {
+        switch (nv) {
+            case 4: return softmax_staged_kernel<float, 4>;
+            case 8: return softmax_staged_kernel<float, 8>;
+            case 16: return softmax_staged_kernel<float, 16>;
+            default: return nullptr;
+        }
+    }
+    switch (nv) {
+        case 2: return softmax_staged_kernel<__nv_bfloat16, 2>;
+        case 4: return softmax_staged_kernel<__nv_bfloat16, 4>;
+        case 8: return softmax_staged_kernel<__nv_bfloat16, 8>;
+        default: return nullptr;
+    }
+}
+
+int softmax_staged_max_threads() { return kSoftmaxStagedMaxThreads; }
 
 }  // namespace rmsnorm

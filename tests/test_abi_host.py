@@ -110,7 +110,21 @@ def test_softmax_rejects_bad_arguments_before_launch(lib, fn):
 
 def test_softmax_ex_rejects_rmsnorm_only_options(lib):
     for field, value in (("cluster", 2), ("chunk_bytes", 4096), ("stages", 3), ("weights", 1),
-                         ("epilogue", 1), ("fault_inject", 1), ("path", 2), ("path", 5)):
+                         ("epilogue", 1), ("fault_inject", 1), ("path", 5)):
         o = binding.make_options()
         setattr(o, field, value)
         assert binding.raw.rowsoftmax_fwd_ex(0, A, B, 4, 8, o) == INVALID, field
+
+
+def test_softmax_ex_staged_shape_options_are_checked(lib):
+    """chunk_bytes and stages shape only the staged kernel; bad values are
+    rejected before any CUDA call."""
+    for path in ("rowreg", "twopass", "cluster"):
+        for field in ("chunk_bytes", "stages"):
+            o = binding.make_options(path=path)
+            setattr(o, field, 32)
+            assert binding.raw.rowsoftmax_fwd_ex(0, A, B, 4, 8, o) == INVALID, (path, field)
+    for field, value in (("chunk_bytes", 4100), ("chunk_bytes", -16), ("stages", -1)):
+        o = binding.make_options(path="staged")
+        setattr(o, field, value)
+        assert binding.raw.rowsoftmax_fwd_ex(0, A, B, 4, 8, o) == INVALID, (field, value)

@@ -75,8 +75,9 @@ def test_width_sweep(dtype, cols):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("path,cluster", [("rowreg", 0), ("twopass", 0), ("cluster", 2),
-                                          ("cluster", 4), ("cluster", 8), ("cluster", 16)])
+@pytest.mark.parametrize("path,cluster", [("rowreg", 0), ("twopass", 0), ("staged", 0),
+                                          ("cluster", 2), ("cluster", 4), ("cluster", 8),
+                                          ("cluster", 16)])
 @pytest.mark.parametrize("rows,cols", [(300, 512), (7, 4096), (3, 32000), (64, 1000),
                                        (5, 128256), (2, 262144)])
 def test_forced_paths(dtype, path, cluster, rows, cols):
@@ -103,6 +104,45 @@ def test_cluster_special_values(dtype):
     x = x.to(DT[dtype])
     y = run(x.cuda(), path="cluster", cluster=8)
     compare(y, ref_for(x), f"cluster special {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols,chunk,stages,grid,threads", [
+    (300, 512, 0, 0, 0, 0),            # one chunk per row, the ring holds many rows
+    (300, 512, 0, 0, 3, 0),            # 100 rows per CTA: the ring wraps many times
+    (41, 32000, 0, 0, 5, 0),           # vocabulary rows, several rows per CTA
+    (41, 32000, 4096, 0, 4, 512),      # 16 chunks, a short last chunk
+    (41, 32000, 4096, 16, 4, 0),       # ring of exactly one row (no lookahead)
+    (41, 32000, 4096, 17, 2, 0),       # one slot of lookahead: slot index drifts per row
+    (9, 8200, 1024, 32, 2, 256),       # the largest ring, 17 chunks per row, 256 threads
+    (17, 40, 0, 0, 0, 0),              # a row shorter than one vector per consumer thread
+    (5, 5000, 16384, 3, 0, 128),       # row of 10/20 KB in one chunk (not a power of two)
+])
+def test_staged_ring_shapes(dtype, rows, cols, chunk, stages, grid, threads):
+    """The shared-memory staged softmax over ring sizes, chunk sizes and CTA
+    counts that make every slot-reuse pattern occur.  `chunk` is in bytes of
+    bf16 rows; fp32 rows use twice as many bytes, so both dtypes cut a row
+    into the same number of chunks."""
+    x = case(rows, cols, dtype, rows * 7 + cols)
+    chunk_bytes = chunk * (2 if dtype == "f32" else 1)
+    y = run(x.cuda(), path="staged", chunk_bytes=chunk_bytes, stages=stages, grid=grid,
+            threads=threads)
+    compare(y, ref_for(x), f"staged {dtype} {rows}x{cols} chunk={chunk} S={stages} g={grid}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_staged_special_values(dtype):
+    """Masked, fully masked, NaN and +inf rows through the staged kernel
+    (each row's maximum and sum cross its consumer warps)."""
+    x = case(5, 32000, "f32", 23)
+    x[0, ::7] = -float("inf")
+    x[1] = -float("inf")
+    x[2, 31999] = float("nan")
+    x[3, 0] = float("inf")
+    x[4] = -3.5
+    x = x.to(DT[dtype])
+    y = run(x.cuda(), path="staged", grid=2)
+    compare(y, ref_for(x), f"staged special {dtype}")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
