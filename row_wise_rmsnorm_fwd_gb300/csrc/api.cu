@@ -137,13 +137,23 @@ rmsnorm_status_t plan_rowreg(const Call& c, int cluster, Plan* P) {
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
     int grid;
     if (cluster == 1) {
-        // Grid-stride over row blocks with about sixteen waves of resident CTAs:
-        // measured on GB300 to keep HBM busier than one resident wave (CTAs
-        // fall out of phase, so loads, reductions and stores overlap): on c4
-        // and c5a 1 wave gives 98%, 4 waves 98.5-100%, 16 waves 99-102% of
-        // the measured copy peak.
+        // Grid-stride over row blocks with k waves of resident CTAs, k = the
+        // row blocks per resident CTA slot / 3, between 1 and 16: every CTA
+        // works on three or more row blocks (so the next-row prefetch has
+        // something to fetch and the weight slice loaded per CTA is reused),
+        // and the grid is a whole number of resident waves.  Measured on
+        // GB300: up to sixteen waves keep HBM busier than one (CTAs fall out
+        // of phase, so loads, reductions and stores overlap: on c4 and c5a 1
+        // wave gives 98%, 4 waves 98.5-100%, 16 waves 99-102% of the measured
+        // copy peak), while one CTA per row block on inputs of 3 to 16 waves
+        // lost 10-15% (c3: 14.9 against 12.8 us; 8192 bf16 rows of 8192:
+        // 50.3 against 43.9 us).  Fewer row blocks than resident slots: one
+        // CTA each.
         const int64_t nblocks = (c.rows + rpc - 1) / rpc;
-        const int64_t target = static_cast<int64_t>(c.info->sms) * occ * kRowregWaves;
+        const int64_t resident = static_cast<int64_t>(c.info->sms) * occ;
+        int64_t waves = nblocks / (3 * resident);
+        waves = waves < 1 ? 1 : (waves > kRowregWaves ? kRowregWaves : waves);
+        const int64_t target = resident * waves;
         grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
                                                : (nblocks < target ? nblocks : target));
     } else {
