@@ -562,7 +562,7 @@ def main():
     ap.add_argument("--rows", type=int, default=0,
                     help="use only this many rows of the workload (small profiling cases)")
     ap.add_argument("--path", default="auto",
-                    choices=["auto", "rowreg", "staged", "cluster", "twopass", "page"],
+                    choices=["auto", "rowreg", "staged", "cluster", "twopass", "page", "ringreg"],
                     help="force a kernel family through rmsnorm_fwd_ex (evidence runs)")
     ap.add_argument("--cluster", type=int, default=0)
     ap.add_argument("--grid", type=int, default=0, help="force the CTA count")

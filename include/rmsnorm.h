@@ -68,10 +68,16 @@ typedef enum {
     RMSNORM_PATH_CLUSTER = 3,  /* split row: a thread-block cluster per row, slices in
                                   registers, partial sums exchanged through DSMEM     */
     RMSNORM_PATH_TWOPASS = 4,  /* generic fallback: read x twice (any width/alignment) */
-    RMSNORM_PATH_PAGE = 5      /* comparison only, never automatic: the compiler write-up's
+    RMSNORM_PATH_PAGE = 5,     /* comparison only, never automatic: the compiler write-up's
                                   schedule (one 256-thread CTA per row, whole row staged
                                   in shared memory, 4-byte accesses, 3-level tree); rows
                                   up to the shared-memory limit (about 56K elements) */
+    RMSNORM_PATH_RINGREG = 6   /* wide rows (up to 128 KB, 16-byte aligned x, w, y and
+                                  pitch): rows streamed through a shared-memory ring by
+                                  bulk copies and held in registers, the weight row in
+                                  shared memory; opt->threads = consumer threads,
+                                  opt->chunk_bytes = 2 or 4 vectors per consumer thread
+                                  (x 16 bytes x threads), opt->stages = ring slots */
 } rmsnorm_path_t;
 
 /* Options for rmsnorm_fwd_ex / rmsnorm_plan.  Zero-initialise, then set what you

@@ -28,7 +28,8 @@ RMSNORM_ERR_TIMEOUT = 4
 RMSNORM_DTYPE_F32 = 0
 RMSNORM_DTYPE_BF16 = 1
 
-PATHS = {"auto": 0, "rowreg": 1, "staged": 2, "cluster": 3, "twopass": 4, "page": 5}
+PATHS = {"auto": 0, "rowreg": 1, "staged": 2, "cluster": 3, "twopass": 4, "page": 5,
+         "ringreg": 6}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 

@@ -39,6 +39,9 @@ constexpr int64_t kRowregMaxRowBytes = 32768;   // auto: register-resident up to
 constexpr int64_t kStagedMaxRowBytes = 65536;   // auto: fp32 staged up to here
 constexpr int kAutoMaxCluster = 8;              // auto: portable cluster sizes only
 constexpr int64_t kSplitMinBytes = 16 << 20;    // auto: split narrow few-row inputs from here
+constexpr int kRingregSlots = 3;                 // ring-to-register kernel: ring slots
+constexpr int64_t kRingregLowMaxRowBytes = 57344;    // auto: ringreg for rows above 32 KB to here
+constexpr int64_t kRingregHighMinRowBytes = 114688;  // auto: and above this (to 128 KB)
 
 struct Call {
     int dtype;
@@ -275,6 +278,79 @@ rmsnorm_status_t plan_staged(const Call& c, int cluster, Plan* P) {
     return RMSNORM_OK;
 }
 
+// Ring-to-register kernel for wide rows: 16-byte vectors only (bulk copies
+// of whole 16-byte-aligned rows); the fewest vectors per consumer thread (8
+// or 16) that cover the row with at most 512 consumer threads (or
+// opt->threads consumer threads); chunks of M = 4 vectors per consumer
+// thread (32 KB at 512 threads; opt->chunk_bytes may ask for M = 2) and a
+// ring of 3 slots (or opt->stages, at least 2).  Measured on 1.5 GB inputs of
+// rows from 36 to 128 KB: deeper rings were slower, down to 70-80% of the
+// HBM roofline with 16 or more slots, and M = 4 with 3 slots was the best or
+// within 3 points of it wherever this kernel is chosen automatically.
+rmsnorm_status_t plan_ringreg(const Call& c, Plan* P) {
+    if (c.opt.vec_bytes != 0 && c.opt.vec_bytes != 16) return RMSNORM_ERR_UNSUPPORTED;
+    if (widest_vb(c) != 16) return RMSNORM_ERR_UNSUPPORTED;
+    if (c.opt.weights != 0 || c.opt.cluster > 1) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t row_bytes = c.hidden * c.sz;
+    const int64_t nvec = row_bytes / 16;
+    const int max_nt = ringreg_max_consumers();
+    int nv = 8, nt;
+    if (c.opt.threads > 0) {
+        nt = c.opt.threads;
+        if (nt % 32 != 0 || nt > max_nt) return RMSNORM_ERR_UNSUPPORTED;
+        if (static_cast<int64_t>(nv) * nt < nvec) nv = 16;
+        if (static_cast<int64_t>(nv) * nt < nvec) return RMSNORM_ERR_UNSUPPORTED;
+    } else {
+        if (static_cast<int64_t>(nv) * max_nt < nvec) nv = 16;
+        if (static_cast<int64_t>(nv) * max_nt < nvec) return RMSNORM_ERR_UNSUPPORTED;
+        nt = round_up((nvec + nv - 1) / nv, 32);
+    }
+    int m = 4;
+    if (c.opt.chunk_bytes != 0) {
+        if (c.opt.chunk_bytes == 2 * nt * 16) m = 2;
+        else if (c.opt.chunk_bytes == 4 * nt * 16) m = 4;
+        else return RMSNORM_ERR_UNSUPPORTED;
+    }
+    const int64_t chunk = static_cast<int64_t>(m) * nt * 16;
+    const int64_t nchunks = (row_bytes + chunk - 1) / chunk;
+    const int64_t wres = (row_bytes + 127) / 128 * 128;
+    const int64_t budget = c.info->smem_optin - kStagedHeaderHost - wres;
+    if (c.opt.stages < 0) return RMSNORM_ERR_INVALID_ARG;
+    int64_t slots = c.opt.stages ? c.opt.stages : kRingregSlots;
+    if (!c.opt.stages && slots * chunk > budget) slots = budget / chunk;
+    if (slots < 2 || slots > kStagedMaxSlotsHost || slots * chunk > budget)
+        return RMSNORM_ERR_UNSUPPORTED;
+    KernelFn fn = ringreg_kernel_ptr(c.dtype, nv, m, c.opt.epilogue);
+    if (!fn) return RMSNORM_ERR_UNSUPPORTED;
+    const int block = nt + 32;
+    const int64_t smem = kStagedHeaderHost + wres + slots * chunk;
+    int occ = 0;
+    if (cached_occupancy(c.dev, c.info->smem_optin, fn, block, static_cast<int>(smem), 1, &occ) !=
+        cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t resident = static_cast<int64_t>(c.info->sms) * occ;
+    P->path = RMSNORM_PATH_RINGREG;
+    P->cluster = 1;
+    P->group = nt;
+    P->block = block;
+    P->rpc = 1;
+    P->grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
+                                              : (c.rows < resident ? c.rows : resident));
+    P->vb = 16;
+    P->nv = nv;
+    P->smem = static_cast<int>(smem);
+    P->chunk = static_cast<int>(chunk);
+    P->nchunks = static_cast<int>(nchunks);
+    P->nslots = static_cast<int>(slots);
+    P->w_staged = 1;
+    P->nvec = static_cast<int>(nvec);
+    P->slice_vecs = static_cast<int>(nvec);
+    P->fn = fn;
+    P->name = "ringreg";
+    return RMSNORM_OK;
+}
+
 // Generic fallback: any width and alignment.
 rmsnorm_status_t plan_twopass(const Call& c, Plan* P) {
     int vb;
@@ -374,7 +450,21 @@ rmsnorm_status_t plan_auto(const Call& c, Plan* P) {
         st = plan_rowreg(c, 1, P);
         if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
     }
-    if (row_bytes <= kStagedMaxRowBytes && c.dtype == RMSNORM_DTYPE_F32) {
+    // Wider rows, by measurement (1.5 GB inputs, % of the measured HBM peak):
+    //   above 32 to 56 KB: ring-to-register, 92-99% (two-pass 76-99%,
+    //     staged 47-72%);
+    //   above 56 KB to 112 KB: the two-pass kernel, 95-100%, except fp32 rows
+    //     of 64 KB, where the staged kernel's two 32 KB chunks per row give
+    //     97% (two-pass 96%; at 56 KB it gave only 67%);
+    //   above 112 KB to 128 KB: ring-to-register, 99% (two-pass 91-92%).
+    const bool ringreg = (row_bytes > kRowregMaxRowBytes && row_bytes <= kRingregLowMaxRowBytes) ||
+                         row_bytes > kRingregHighMinRowBytes;
+    if (ringreg) {
+        st = plan_ringreg(c, P);
+        if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+    }
+    if (row_bytes > kRingregLowMaxRowBytes && row_bytes <= kStagedMaxRowBytes &&
+        c.dtype == RMSNORM_DTYPE_F32) {
         st = plan_staged(c, 1, P);
         if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
     }
@@ -408,6 +498,9 @@ rmsnorm_status_t make_plan(const Call& c, Plan* P) {
             return plan_twopass(c, P);
         case RMSNORM_PATH_PAGE:
             return plan_page(c, P);
+        case RMSNORM_PATH_RINGREG:
+            if (cl > 1) return RMSNORM_ERR_INVALID_ARG;
+            return plan_ringreg(c, P);
         default:
             return RMSNORM_ERR_INVALID_ARG;
     }
@@ -584,7 +677,7 @@ int32_t rmsnorm_last_cuda_error(char* msg, size_t len) {
     return static_cast<int32_t>(e);
 }
 
-int32_t rmsnorm_abi_version(void) { return 10000; }
+int32_t rmsnorm_abi_version(void) { return 10100; }
 
 // Present in every build; non-zero only in the failure-injection test build.
 int32_t rmsnorm_fault_injection_enabled(void) { return RMSNORM_FAULT_INJECT; }

@@ -45,6 +45,13 @@ int softmax_staged_max_threads();
 KernelFn page_kernel_ptr(int dtype);
 int page_block();
 
+// Ring-to-register wide-row kernel: one producer warp plus up to 512 consumer
+// threads of nv (8 or 16) vectors each; a chunk is m (2 or 4) vectors per
+// consumer thread.  Dynamic shared memory = kStagedHeaderHost + the weight row
+// rounded up to 128 bytes + nslots * chunk bytes.
+KernelFn ringreg_kernel_ptr(int dtype, int nv, int m, int epi);
+int ringreg_max_consumers();
+
 // Staged kernel: one producer warp plus 4 or 8 consumer warps.
 KernelFn staged_kernel_ptr(int dtype, int consumer_warps, int epi);
 constexpr int kStagedMaxSlotsHost = 32;

@@ -39,7 +39,7 @@ def test_status_strings(lib):
         s = binding.rmsnorm_status_string(code)
         assert isinstance(s, str) and s
     assert binding.rmsnorm_status_string(99) == "unknown status"
-    assert binding.rmsnorm_abi_version() == 10000
+    assert binding.rmsnorm_abi_version() == 10100
 
 
 def test_struct_sizes_match_header():
@@ -110,7 +110,7 @@ def test_softmax_rejects_bad_arguments_before_launch(lib, fn):
 
 def test_softmax_ex_rejects_rmsnorm_only_options(lib):
     for field, value in (("cluster", 2), ("chunk_bytes", 4096), ("stages", 3), ("weights", 1),
-                         ("epilogue", 1), ("fault_inject", 1), ("path", 5)):
+                         ("epilogue", 1), ("fault_inject", 1), ("path", 5), ("path", 6)):
         o = binding.make_options()
         setattr(o, field, value)
         assert binding.raw.rowsoftmax_fwd_ex(0, A, B, 4, 8, o) == INVALID, field

@@ -64,6 +64,7 @@ CASES = [
      (8, 65536)),
     ("staged cluster withholds a partial", dict(path="staged", cluster=2, fault_inject=2),
      (16, 8192)),
+    ("ring-to-register withholds a copy", dict(path="ringreg", fault_inject=1), (64, 16384)),
 ]
 
 

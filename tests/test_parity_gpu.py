@@ -127,7 +127,8 @@ FORCED = [
     ("staged", {"weights": 1}), ("staged", {"weights": 2, "chunk_bytes": 2048}),
     ("staged", {"stages": 32, "chunk_bytes": 1024}), ("staged", {"cluster": 2, "weights": 1}),
     ("cluster", {"cluster": 2}), ("cluster", {"cluster": 4}), ("cluster", {"cluster": 8}),
-    ("cluster", {"cluster": 16}), ("page", {}),
+    ("cluster", {"cluster": 16}), ("page", {}), ("ringreg", {}), ("ringreg", {"stages": 2}),
+    ("ringreg", {"threads": 256}), ("ringreg", {"grid": 2}),
 ]
 
 
@@ -145,6 +146,34 @@ def test_forced_paths(dtype, path, extra, rows, hidden):
             pytest.skip(f"{path} {extra} cannot serve {rows}x{hidden}")
         raise
     compare(y, oracle_for(x, w, 1e-6), f"{path} {extra} {dtype} {rows}x{hidden}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,hidden", [(41, 32768), (37, 18432), (9, 16384), (300, 1024),
+                                         (5, 8200)])
+@pytest.mark.parametrize("extra", [{}, {"stages": 2}, {"stages": 8, "grid": 3}, {"m2": 1},
+                                   {"m2": 1, "stages": 2, "grid": 1}, {"m2": 1, "stages": 7},
+                                   {"grid": 7}],
+                         ids=lambda v: str(v))
+def test_ringreg_shapes(dtype, rows, hidden, extra):
+    """The ring-to-register kernel over ring depths (2 to 8 slots, fewer or
+    more than a row's chunks), both chunk sizes (4 and 2 vectors per consumer
+    thread) and CTA counts that give every CTA many rows."""
+    if dtype == "bf16" and hidden == 32768:
+        hidden = 65536                       # 128 KB rows in both dtypes
+    x, w = rand_case(rows, hidden, dtype, seed=rows * 3 + hidden)
+    xc, wc = x.cuda(), w.cuda()
+    opts = dict(path="ringreg", **{k: v for k, v in extra.items() if k != "m2"})
+    if extra.get("m2"):
+        plan = binding.rmsnorm_plan(xc, wc, torch.empty_like(xc), options={"path": "ringreg"})
+        opts["chunk_bytes"] = 2 * plan["threads_per_row"] * 16
+    try:
+        y = run(xc, wc, 1e-6, **opts)
+    except binding.RmsnormError as e:
+        if e.status == binding.RMSNORM_ERR_UNSUPPORTED:
+            pytest.skip(f"ringreg {extra} cannot serve {rows}x{hidden}")
+        raise
+    compare(y, oracle_for(x, w, 1e-6), f"ringreg {extra} {dtype} {rows}x{hidden}")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -193,7 +222,8 @@ def test_in_place(dtype, rows, hidden):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("path", ["auto", "rowreg", "staged", "cluster", "twopass", "page"])
+@pytest.mark.parametrize("path", ["auto", "rowreg", "staged", "cluster", "twopass", "page",
+                                  "ringreg"])
 def test_guard_regions_untouched(dtype, path):
     """Sentinels before and after y stay intact (no out-of-bounds stores)."""
     rows, hidden = 21, 4104
@@ -244,7 +274,8 @@ def test_eps_zero_zero_row_is_nan():
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("path", ["auto", "rowreg", "staged", "cluster", "twopass", "page"])
+@pytest.mark.parametrize("path", ["auto", "rowreg", "staged", "cluster", "twopass", "page",
+                                  "ringreg"])
 def test_deterministic(dtype, path):
     x, w = rand_case(64, 8192, dtype, seed=123)
     xc, wc = x.cuda(), w.cuda()
@@ -293,7 +324,8 @@ def test_unsupported_forced_option_launches_nothing():
 
 # --------------------------------------------------------- fused epilogue --
 
-EPI_PATHS = [("auto", {}), ("rowreg", {}), ("staged", {}), ("cluster", {"cluster": 2}),
+EPI_PATHS = [("auto", {}), ("rowreg", {}), ("staged", {}), ("ringreg", {}),
+             ("cluster", {"cluster": 2}),
              ("cluster", {"cluster": 8}), ("twopass", {}), ("rowreg", {"vec_bytes": 4})]
 
 
