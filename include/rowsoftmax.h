@@ -44,11 +44,14 @@ rmsnorm_status_t rowsoftmax_fwd_bf16(const uint16_t* x, uint16_t* y, int64_t row
  * RMSNORM_PATH_CLUSTER (each row split over opt->cluster = 2..16 CTAs of a
  * thread-block cluster, row maximum and sum combined through distributed
  * shared memory), RMSNORM_PATH_STAGED (rows staged in shared memory by
- * bulk copies that run ahead into the next rows; needs 16-byte aligned x and
- * y and a row of a multiple of 16 bytes, else RMSNORM_ERR_UNSUPPORTED;
- * opt->chunk_bytes (a multiple of 16) and opt->stages size its copies and
- * its ring of shared-memory slots, zero for the defaults; opt->threads 128
- * or 256 consumer threads) or RMSNORM_PATH_TWOPASS (the wide-row kernel:
+ * bulk copies that run ahead into the next rows, then held in registers;
+ * needs 16-byte aligned x and y and a row of a multiple of 16 bytes, else
+ * RMSNORM_ERR_UNSUPPORTED; opt->chunk_bytes (a power of two, or at least the
+ * row) and opt->stages size its copies and its ring of shared-memory slots,
+ * zero for the defaults; opt->threads = threads per CTA, a multiple of 32 up
+ * to 512; opt->cluster = 2..16 splits each row over a thread-block cluster,
+ * maximum and sum combined through distributed shared memory) or
+ * RMSNORM_PATH_TWOPASS (the wide-row kernel:
  * reads each row three times, the repeats normally from L2); opt->threads,
  * opt->grid, opt->vec_bytes and opt->wait_timeout_ns as for rmsnorm_fwd_ex.
  * chunk_bytes and stages with any other path, and the other option fields,

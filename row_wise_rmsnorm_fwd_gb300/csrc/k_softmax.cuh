@@ -30,12 +30,7 @@ namespace rmsnorm {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// exp(v - m) as 2^(v*log2e - m*log2e); ml2e = m * log2e.
-__device__ __forceinline__ float exp_shifted(float v, float ml2e) {
-    return exp2f(fmaf(v, kLog2e, -ml2e));
-}
-
-// The register and staged kernels evaluate every exponential of a row as
+// Every kernel evaluates every exponential of a row as
 // 2^(v*log2e + c) with a per-row constant c = row_exp_bias<T>() - m*log2e.
 //   fp32: exp2f, bias 0: e = exp(v - m) itself.
 //   bf16: the PTX instruction ex2.approx.ftz.f32 (one SFU operation,
@@ -67,6 +62,47 @@ __device__ __forceinline__ float warp_allreduce_max(float v) {
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
     return v;
+}
+
+// One exchange per row of a (maximum, sum of exponentials) pair over a
+// thread-block cluster: the combine of the online softmax.  Each CTA sends
+// its slice's maximum m_r and its sum s_r of exp(x - m_r) to every peer; every
+// CTA then forms M = max_r m_r and S = sum_r s_r * exp(m_r - M) in rank order,
+// so all CTAs hold the bitwise same pair.  Double-buffered by row parity, a
+// bounded wait, as cluster_allreduce (common.cuh); the caller passes a block
+// barrier after each call.  A slice of -inf only has m_r = -inf and s_r = 0
+// and adds exp(-inf) * 0 = 0; a row of -inf gives M = -inf and a NaN sum, as
+// the definition does.
+struct PairExchange {
+    alignas(8) unsigned long long bar[2];
+    float2 slot[2][16];
+};
+
+__device__ __forceinline__ bool cluster_pair_allreduce(PairExchange* ex, float m, float s,
+                                                       int ncta, uint32_t rank, uint32_t it,
+                                                       const Params& p, float* M, float* S,
+                                                       int lt) {
+    const uint32_t b = it & 1u;
+    if (lt < ncta) {
+        const uint32_t peer = static_cast<uint32_t>(lt);
+        const uint32_t slot = map_to_rank(smem_addr(&ex->slot[b][rank]), peer);
+        asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" :: "r"(slot), "f"(m), "f"(s)
+                     : "memory");
+        mbar_arrive_remote(map_to_rank(smem_addr(&ex->bar[b]), peer));
+    }
+    const bool ok = mbar_wait_bounded<true>(smem_addr(&ex->bar[b]), (it >> 1) & 1u,
+                                            p.timeout_ns);
+    float mx = -INFINITY, sum = 0.f;
+    if (ok) {
+        for (int c = 0; c < ncta; ++c) mx = fmaxf(mx, ex->slot[b][c].x);
+        for (int c = 0; c < ncta; ++c)
+            sum += ex->slot[b][c].y * exp2f((ex->slot[b][c].x - mx) * kLog2e);
+    } else if (lt == 0) {
+        report_timeout(p.status, kSiteClusterExchange);
+    }
+    *M = mx;
+    *S = sum;
+    return ok;
 }
 
 template <int NV>
@@ -231,16 +267,26 @@ softmax_rowreg_kernel(const Params p) {
 // second register copy of the row, which does not fit for rows of 16 KB and
 // more.  No producer warp: 16 warps of 128 registers fill an SM's register
 // file, where a 17th warp would cap every thread at 96.  Thread t owns
-// vectors t, t + blockDim.x, ...; chunk_bytes is a power of two unless a row
-// fits one chunk.
+// vectors t, t + blockDim.x, ... of its row (or slice); chunk_bytes is a
+// power of two unless a slice fits one chunk.
+// CL: rows too wide for one CTA's registers are split over a thread-block
+// cluster of p.cluster CTAs; CTA rank r streams slice r (p.slice_vecs
+// vectors) of each of its cluster's rows, computes the exponentials and
+// their sum relative to its slice's maximum, and one exchange of the
+// (maximum, sum) pair through distributed shared memory (bounded wait) gives
+// every CTA the row's maximum and sum, with which it rescales its slice --
+// the online-softmax combine, one cluster round trip per row instead of two
+// -- while the ring keeps loading the next rows' slices.
 constexpr int kSoftmaxStagedMaxThreads = 512;
 
-template <typename T, int NV>
+template <typename T, int NV, bool CL>
 __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kernel(const Params p) {
     constexpr int EPV = 16 / static_cast<int>(sizeof(T));
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    float* red = reinterpret_cast<float*>(smem + 8 * kStagedMaxSlots);   // [max|sum][buffer][warp]
+    // header: full[32] | red[max|sum][buffer][16 warps] | the cluster pair exchange
+    float* red = reinterpret_cast<float*>(smem + 8 * kStagedMaxSlots);
+    PairExchange* ex = reinterpret_cast<PairExchange*>(smem + 8 * kStagedMaxSlots + 256);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -249,9 +295,21 @@ __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kerne
     const int NCH = p.nchunks;
     const int S = p.nslots;
     const int CB = p.chunk_bytes;
+    const int ncta = CL ? p.cluster : 1;
+    uint32_t rank = 0;
+    int64_t unit = blockIdx.x, nunits = gridDim.x;
+    if (CL) {
+        rank = cluster_ctarank();
+        unit = cluster_id_x();
+        nunits = cluster_count_x();
+    }
     const int64_t row_bytes = static_cast<int64_t>(p.hidden) * sizeof(T);
-    const SlotRing ring{full, nullptr, smem + kStagedHeader, S, NCH, CB, row_bytes};
-    const int64_t unit = blockIdx.x, nunits = gridDim.x;
+    const int64_t slice_nom = CL ? static_cast<int64_t>(p.slice_vecs) * 16 : row_bytes;
+    const int64_t sbeg = static_cast<int64_t>(rank) * slice_nom;
+    const int64_t send = sbeg + slice_nom < row_bytes ? sbeg + slice_nom : row_bytes;
+    const int64_t my_bytes = send > sbeg ? send - sbeg : 0;
+    const int my_vecs = static_cast<int>(my_bytes / 16);
+    const SlotRing ring{full, nullptr, smem + kStagedHeader, S, NCH, CB, my_bytes};
     const uint64_t policy = policy_evict_first();
 
     int64_t issued = 0;            // chunks issued so far (thread 0's count)
@@ -259,9 +317,20 @@ __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kerne
     if (tid == 0) {
         for (int k = 0; k < S; ++k) mbar_init(smem_addr(&full[k]), 1);
         fence_mbarrier_init_cluster();
-        while (issued < S && ring_issue_next(p, ring, cur, nunits, row_bytes, policy)) ++issued;
+        while (issued < S && ring_issue_next(p, ring, cur, nunits, row_bytes, sbeg, policy))
+            ++issued;
     }
-    __syncthreads();
+    if (CL) {
+        if (tid == 0) {
+            mbar_init(smem_addr(&ex->bar[0]), ncta);
+            mbar_init(smem_addr(&ex->bar[1]), ncta);
+            fence_mbarrier_init_cluster();
+        }
+        __syncthreads();
+        cluster_sync_all();        // no peer arrives before the barriers exist
+    } else {
+        __syncthreads();
+    }
 
     const int shift = (CB & (CB - 1)) == 0 ? __ffs(CB) - 1 : 31;
     int kidx[NV], off[NV];
@@ -269,8 +338,8 @@ __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kerne
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int v = i * NT + tid;
-        valid[i] = v < p.nvec;
-        kidx[i] = (v * 16) >> shift;                   // chunk of the row holding vector v
+        valid[i] = v < my_vecs;
+        kidx[i] = (v * 16) >> shift;                   // chunk of the slice holding vector v
         off[i] = v * 16 - (kidx[i] << shift);           // its byte offset in that chunk
     }
     char* yb = static_cast<char*>(p.y);
@@ -312,7 +381,7 @@ __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kerne
             }
         }
         float m = warp_allreduce_max(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])));
-        if (lane == 0) red[b * 32 + warp] = m;
+        if (lane == 0) red[b * 16 + warp] = m;
         if (__syncthreads_or(!ok)) {
             if (tid == 0) report_timeout(p.status, kSiteStagedFull);
             break;
@@ -320,7 +389,7 @@ __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kerne
         // every thread holds its part of the row: refill the row's slots
         if (tid == 0)
             while (issued < base + NCH + S &&
-                   ring_issue_next(p, ring, cur, nunits, row_bytes, policy))
+                   ring_issue_next(p, ring, cur, nunits, row_bytes, sbeg, policy))
                 ++issued;
         slot0 += NCH;              // NCH <= S: one wrap at most
         if (slot0 >= S) {
@@ -328,8 +397,10 @@ __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kerne
             lap0 ^= 1u;
         }
         m = -INFINITY;
-        for (int k = 0; k < NW; ++k) m = fmaxf(m, red[b * 32 + k]);
-        const float c = row_exp_bias<T>() - m * kLog2e;
+        for (int k = 0; k < NW; ++k) m = fmaxf(m, red[b * 16 + k]);
+        // exponentials relative to this CTA's maximum: the whole row's when
+        // the row is not split; a slice of -inf keeps -inf (exp(-inf) = 0)
+        const float c = (CL && m == -INFINITY) ? -INFINITY : row_exp_bias<T>() - m * kLog2e;
         float sk[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
@@ -342,12 +413,18 @@ __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kerne
             }
         }
         float sum = warp_allreduce_sum((sk[0] + sk[1]) + (sk[2] + sk[3]));
-        if (lane == 0) red[64 + b * 32 + warp] = sum;
+        if (lane == 0) red[32 + b * 16 + warp] = sum;
         __syncthreads();
         sum = 0.f;
-        for (int k = 0; k < NW; ++k) sum += red[64 + b * 32 + k];
-        const float inv = 1.0f / sum;
-        char* dst = yb + row * row_bytes;
+        for (int k = 0; k < NW; ++k) sum += red[32 + b * 16 + k];
+        float inv = 1.0f / sum;
+        if (CL) {
+            float M, S;
+            const bool cok = cluster_pair_allreduce(ex, m, sum, ncta, rank, it, p, &M, &S, tid);
+            if (__syncthreads_or(!cok)) break;   // uniform: stop, then leave cleanly
+            inv = exp2f((m - M) * kLog2e) / S;    // rescale this slice to the row's maximum
+        }
+        char* dst = yb + row * row_bytes + sbeg;
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             if (valid[i]) {
@@ -363,6 +440,8 @@ __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kerne
     if (tid == 0)
         for (int64_t n = issued > S ? issued - S : 0; n < issued; ++n)
             ring_wait_full(ring, n, p.timeout_ns);
+    // Keep this CTA's shared memory alive until every peer is done with it.
+    if (CL) cluster_sync_all();
 }
 
 constexpr int kSoftmaxWideThreads = 1024;
@@ -394,14 +473,14 @@ __global__ void __launch_bounds__(kSoftmaxWideThreads) softmax_threepass_kernel(
         __syncthreads();
         m = -INFINITY;
         for (int k = 0; k < nwarps; ++k) m = fmaxf(m, red[0][b][k]);
-        const float ml2e = m * kLog2e;
+        const float c = row_exp_bias<T>() - m * kLog2e;
 
         float s0 = 0.f, s1 = 0.f;
         for (int v = tid; v < p.nvec; v += nthr) {
             const Vec<VB> xv = ld_plain<VB>(src + static_cast<int64_t>(v) * VB);
 #pragma unroll
             for (int k = 0; k < EPV; ++k) {
-                const float ev = exp_shifted(get<T, VB>(xv, k), ml2e);
+                const float ev = row_exp<T>(get<T, VB>(xv, k), c);
                 if (k & 1) s1 += ev; else s0 += ev;
             }
         }
@@ -418,7 +497,7 @@ __global__ void __launch_bounds__(kSoftmaxWideThreads) softmax_threepass_kernel(
             const Vec<VB> xv = ld_stream<VB>(src + off);
             float o[EPV];
 #pragma unroll
-            for (int k = 0; k < EPV; ++k) o[k] = exp_shifted(get<T, VB>(xv, k), ml2e) * inv;
+            for (int k = 0; k < EPV; ++k) o[k] = row_exp<T>(get<T, VB>(xv, k), c) * inv;
             st_stream<VB>(dst + off, pack<T, VB>(o));
         }
     }

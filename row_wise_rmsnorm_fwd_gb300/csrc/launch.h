@@ -37,8 +37,9 @@ KernelFn softmax_threepass_ptr(int dtype, int vb);
 int softmax_threepass_block();
 // Row softmax staged in shared memory and held in registers: up to 512
 // threads of nv 16-byte vectors each (fp32: 4, 8 or 16; bf16: 2, 4 or 8);
-// dynamic shared memory = kStagedHeaderHost + nslots * chunk bytes.
-KernelFn softmax_staged_ptr(int dtype, int nv);
+// cluster = rows split over a thread-block cluster; dynamic shared memory =
+// kStagedHeaderHost + nslots * chunk bytes.
+KernelFn softmax_staged_ptr(int dtype, int nv, bool cluster);
 int softmax_staged_max_threads();
 
 // Comparison kernel with the compiler write-up's schedule (one CTA per row).

@@ -61,25 +61,30 @@ KernelFn softmax_threepass_ptr(int dtype, int vb) {
 
 int softmax_threepass_block() { return kSoftmaxWideThreads; }
 
-static_assert(8 * kStagedMaxSlots + 4 * 32 * sizeof(float) <= kStagedHeader,
+static_assert(8 * kStagedMaxSlots + 4 * 16 * sizeof(float) + sizeof(PairExchange) <= kStagedHeader,
               "staged softmax header overflows");
 
-// Vectors per consumer thread: up to 64 fp32 values of a row in registers.
-KernelFn softmax_staged_ptr(int dtype, int nv) {
+// Vectors per thread: up to 64 fp32 values of a row (or slice) in registers.
+template <bool CL>
+static KernelFn softmax_staged_pick(int dtype, int nv) {
     if (dtype == 0) {
         switch (nv) {
-            case 4: return softmax_staged_kernel<float, 4>;
-            case 8: return softmax_staged_kernel<float, 8>;
-            case 16: return softmax_staged_kernel<float, 16>;
+            case 4: return softmax_staged_kernel<float, 4, CL>;
+            case 8: return softmax_staged_kernel<float, 8, CL>;
+            case 16: return softmax_staged_kernel<float, 16, CL>;
             default: return nullptr;
         }
     }
     switch (nv) {
-        case 2: return softmax_staged_kernel<__nv_bfloat16, 2>;
-        case 4: return softmax_staged_kernel<__nv_bfloat16, 4>;
-        case 8: return softmax_staged_kernel<__nv_bfloat16, 8>;
+        case 2: return softmax_staged_kernel<__nv_bfloat16, 2, CL>;
+        case 4: return softmax_staged_kernel<__nv_bfloat16, 4, CL>;
+        case 8: return softmax_staged_kernel<__nv_bfloat16, 8, CL>;
         default: return nullptr;
     }
+}
+
+KernelFn softmax_staged_ptr(int dtype, int nv, bool cluster) {
+    return cluster ? softmax_staged_pick<true>(dtype, nv) : softmax_staged_pick<false>(dtype, nv);
 }
 
 int softmax_staged_max_threads() { return kSoftmaxStagedMaxThreads; }

@@ -16,6 +16,7 @@ constexpr int64_t kSoftmaxSplitRowBytes = 32768;        // few rows wider than t
 constexpr int64_t kSoftmaxSplitMinBytes = 16 << 20;     // or few rows totalling this much
 constexpr int64_t kSoftmaxStagedChunk = 65536;          // bytes per bulk copy (default)
 constexpr int64_t kSoftmaxStagedMinCols = 8192;         // wider rows go to the staged kernel
+constexpr int kSoftmaxMaxStagedCluster = 8;             // portable cluster sizes only
 
 struct SmCall {
     int dtype;
@@ -82,7 +83,8 @@ rmsnorm_status_t sm_validate(int32_t dtype, const void* x, const void* y, int64_
             return RMSNORM_ERR_INVALID_ARG;
         if (o.cluster < 0 || o.cluster > 16 || (o.cluster & (o.cluster - 1)) != 0)
             return RMSNORM_ERR_INVALID_ARG;
-        if (o.cluster > 1 && o.path != RMSNORM_PATH_CLUSTER) return RMSNORM_ERR_INVALID_ARG;
+        if (o.cluster > 1 && o.path != RMSNORM_PATH_CLUSTER && o.path != RMSNORM_PATH_STAGED)
+            return RMSNORM_ERR_INVALID_ARG;
         if (o.threads < 0 || o.threads % 32 != 0 || o.threads > 1024 || o.grid < 0)
             return RMSNORM_ERR_INVALID_ARG;
     }
@@ -201,35 +203,38 @@ rmsnorm_status_t sm_plan_threepass(const SmCall& c, SmPlan* P) {
 // one chunk); as many ring slots as the shared memory holds, up to 32 (or
 // opt->stages).  Measured on 1 GB inputs: chunks of 8, 16, 32 and 64 KB gave
 // 58, 66, 71 and 76% of the HBM roofline on bf16 rows of 32000.
-rmsnorm_status_t sm_plan_staged(const SmCall& c, SmPlan* P) {
+rmsnorm_status_t sm_plan_staged(const SmCall& c, int cluster, SmPlan* P) {
     int vb;
     rmsnorm_status_t st = sm_pick_vb(c, &vb);
     if (st != RMSNORM_OK) return st;
     if (vb != 16) return RMSNORM_ERR_UNSUPPORTED;
     const int64_t row_bytes = c.cols * c.sz;
     const int64_t nvec = row_bytes / 16;
+    const int64_t per = (nvec + cluster - 1) / cluster;       // vectors per CTA slice
+    if (static_cast<int64_t>(cluster - 1) * per >= nvec) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t slice_bytes = per * 16;
     const int max_nc = softmax_staged_max_threads();
     const int nv_min = c.sz == 4 ? 4 : 2, nv_max = c.sz == 4 ? 16 : 8;
     int nv = nv_min, nc;
     if (c.opt.threads > 0) {
         if (c.opt.threads > max_nc) return RMSNORM_ERR_UNSUPPORTED;
         nc = c.opt.threads;
-        while (nv < nv_max && static_cast<int64_t>(nv) * nc < nvec) nv <<= 1;
-        if (static_cast<int64_t>(nv) * nc < nvec) return RMSNORM_ERR_UNSUPPORTED;
+        while (nv < nv_max && static_cast<int64_t>(nv) * nc < per) nv <<= 1;
+        if (static_cast<int64_t>(nv) * nc < per) return RMSNORM_ERR_UNSUPPORTED;
     } else {
-        while (nv < nv_max && static_cast<int64_t>(nv) * max_nc < nvec) nv <<= 1;
-        if (static_cast<int64_t>(nv) * max_nc < nvec) return RMSNORM_ERR_UNSUPPORTED;
-        nc = sm_round_up((nvec + nv - 1) / nv, 32);
+        while (nv < nv_max && static_cast<int64_t>(nv) * max_nc < per) nv <<= 1;
+        if (static_cast<int64_t>(nv) * max_nc < per) return RMSNORM_ERR_UNSUPPORTED;
+        nc = sm_round_up((per + nv - 1) / nv, 32);
     }
-    KernelFn fn = softmax_staged_ptr(c.dtype, nv);
+    KernelFn fn = softmax_staged_ptr(c.dtype, nv, cluster > 1);
     if (!fn) return RMSNORM_ERR_UNSUPPORTED;
     int64_t chunk = c.opt.chunk_bytes ? c.opt.chunk_bytes : kSoftmaxStagedChunk;
-    if (chunk >= row_bytes) {
-        chunk = row_bytes;                               // one chunk per row
+    if (chunk >= slice_bytes) {
+        chunk = slice_bytes;                             // one chunk per row (slice)
     } else if ((chunk & (chunk - 1)) != 0) {
         return RMSNORM_ERR_UNSUPPORTED;                  // chunks must be a power of two
     }
-    const int64_t nchunks = (row_bytes + chunk - 1) / chunk;
+    const int64_t nchunks = (slice_bytes + chunk - 1) / chunk;
     const int64_t budget = c.dv.smem_optin - kStagedHeaderHost;
     int64_t slots = c.opt.stages ? c.opt.stages : budget / chunk;
     if (!c.opt.stages && slots > kStagedMaxSlotsHost) slots = kStagedMaxSlotsHost;
@@ -238,16 +243,27 @@ rmsnorm_status_t sm_plan_staged(const SmCall& c, SmPlan* P) {
     const int block = nc;
     const int smem = static_cast<int>(kStagedHeaderHost + slots * chunk);
     int occ = 0;
-    if (cached_occupancy(c.dv.dev, c.dv.smem_optin, fn, block, smem, 1, &occ) != cudaSuccess)
+    if (cached_occupancy(c.dv.dev, c.dv.smem_optin, fn, block, smem, cluster, &occ) !=
+        cudaSuccess)
         return RMSNORM_ERR_CUDA;
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
-    const int64_t resident = static_cast<int64_t>(c.dv.sms) * occ;
+    int grid;
+    if (cluster == 1) {
+        const int64_t resident = static_cast<int64_t>(c.dv.sms) * occ;
+        grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
+                                               : (c.rows < resident ? c.rows : resident));
+    } else {
+        const int64_t nclusters = c.opt.grid > 0 ? (c.opt.grid + cluster - 1) / cluster
+                                                 : (c.rows < occ ? c.rows : occ);
+        grid = static_cast<int>(nclusters * cluster);
+    }
     P->path = RMSNORM_PATH_STAGED;
+    P->cluster = cluster;
+    P->slice_vecs = static_cast<int>(per);
     P->group = nc;
     P->block = block;
     P->rpc = 1;
-    P->grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
-                                              : (c.rows < resident ? c.rows : resident));
+    P->grid = grid;
     P->vb = vb;
     P->nv = nv;
     P->nvec = static_cast<int>(nvec);
@@ -256,7 +272,7 @@ rmsnorm_status_t sm_plan_staged(const SmCall& c, SmPlan* P) {
     P->nchunks = static_cast<int>(nchunks);
     P->nslots = static_cast<int>(slots);
     P->fn = fn;
-    P->name = "softmax_staged";
+    P->name = cluster == 1 ? "softmax_staged" : "softmax_cluster_staged";
     return RMSNORM_OK;
 }
 
@@ -274,7 +290,7 @@ rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
         case RMSNORM_PATH_ROWREG: return sm_plan_rowreg(c, 1, P);
         case RMSNORM_PATH_CLUSTER: return sm_plan_rowreg(c, c.opt.cluster ? c.opt.cluster : 2, P);
         case RMSNORM_PATH_TWOPASS: return sm_plan_threepass(c, P);
-        case RMSNORM_PATH_STAGED: return sm_plan_staged(c, P);
+        case RMSNORM_PATH_STAGED: return sm_plan_staged(c, c.opt.cluster ? c.opt.cluster : 1, P);
         default: break;
     }
     const int64_t row_bytes = c.cols * c.sz;
@@ -290,8 +306,17 @@ rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
         }
     }
     if (c.cols > kSoftmaxStagedMinCols) {
-        st = sm_plan_staged(c, P);
+        st = sm_plan_staged(c, 1, P);
         if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+        // fp32 rows too wide for one CTA's registers: split each over the
+        // smallest cluster whose slices fit (up to 8 CTAs).  Measured on
+        // prefill logits (rows of 128256): fp32 69% of the HBM roofline split
+        // against 50% for the three-pass kernel; bf16 59% split against 65%,
+        // so bf16 rows stay with the three-pass kernel.
+        for (int cl = 2; c.dtype == RMSNORM_DTYPE_F32 && cl <= kSoftmaxMaxStagedCluster; cl <<= 1) {
+            st = sm_plan_staged(c, cl, P);
+            if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+        }
     }
     st = sm_plan_rowreg(c, 1, P);
     if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;

@@ -147,8 +147,8 @@ WORKLOADS.update(MODEL_SWEEP)
 
 # Row softmax on the same skeleton: attention-score rows (batch 8 x 32 heads x
 # seq 512 rows of 512 columns, N(0,2) scores), vocabulary logits (rows of
-# 32000, N(0,4)) and decode-step logits (few rows of a 128256 vocabulary);
-# x only, no weight.
+# 32000, N(0,4)), decode-step logits (few rows of a 128256 vocabulary) and
+# prefill logits (many rows of a 128256 vocabulary); x only, no weight.
 SOFTMAX_WORKLOADS = {
     w.name: w for w in [
         Workload("sm_attn_f32", 40, (8 * 32 * 512, 512), "f32", ("normal", 0.0, 2.0),
@@ -169,6 +169,12 @@ SOFTMAX_WORKLOADS = {
         Workload("sm_decode_bf16", 45, (64, 128256), "bf16", ("normal", 0.0, 4.0),
                  ("normal", 1.0, 0.0), 0.0, op="softmax",
                  description="decode-step logits, 64 sequences x 128256 vocabulary, bf16"),
+        Workload("sm_prefill_f32", 46, (1024, 128256), "f32", ("normal", 0.0, 4.0),
+                 ("normal", 1.0, 0.0), 0.0, op="softmax",
+                 description="prefill logits, 1024 tokens x 128256 vocabulary, fp32"),
+        Workload("sm_prefill_bf16", 47, (2048, 128256), "bf16", ("normal", 0.0, 4.0),
+                 ("normal", 1.0, 0.0), 0.0, op="softmax",
+                 description="prefill logits, 2048 tokens x 128256 vocabulary, bf16"),
     ]
 }
 WORKLOADS.update(SOFTMAX_WORKLOADS)

@@ -131,6 +131,47 @@ def test_staged_ring_shapes(dtype, rows, cols, chunk, stages, grid, threads):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols,cluster,chunk,stages,grid", [
+    (37, 128256, 4, 0, 0, 0),          # prefill logits: the automatic split
+    (37, 128256, 8, 0, 0, 16),         # two clusters: many rows each
+    (9, 65536, 2, 0, 0, 0),
+    (300, 20000, 2, 8192, 0, 0),       # several chunks per slice
+    (300, 20000, 4, 0, 2, 8),          # a two-slot ring, a row per cluster at a time
+    (50, 1928, 16, 64, 0, 0),          # 16-CTA clusters; the last slice is short, so
+                                       # some of its chunks are empty
+    (5, 8200, 8, 1024, 0, 0),
+])
+def test_staged_cluster_split(dtype, rows, cols, cluster, chunk, stages, grid):
+    """Rows split over a cluster of CTAs, each staging its slice through its
+    own ring into registers; maximum and sum cross the cluster."""
+    x = case(rows, cols, dtype, rows + cols + cluster)
+    chunk_bytes = chunk * (2 if dtype == "f32" else 1)
+    try:
+        y = run(x.cuda(), path="staged", cluster=cluster, chunk_bytes=chunk_bytes,
+                stages=stages, grid=grid)
+    except binding.RmsnormError as e:
+        if e.status == binding.RMSNORM_ERR_UNSUPPORTED:
+            pytest.skip("this split cannot serve the shape")
+        raise
+    compare(y, ref_for(x), f"staged C={cluster} {dtype} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_staged_cluster_special_values(dtype):
+    """Masked, fully masked, NaN and +inf rows through the cluster-split
+    staged kernel (special values in different slices)."""
+    x = case(6, 128256, "f32", 29)
+    x[0, ::5] = -float("inf")
+    x[1] = -float("inf")
+    x[2, 128000] = float("nan")        # in the last slice
+    x[3, 10] = float("inf")            # in the first slice
+    x[4] = 2.0                         # uniform row
+    x = x.to(DT[dtype])
+    y = run(x.cuda(), path="staged", cluster=4)
+    compare(y, ref_for(x), f"staged cluster special {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_staged_special_values(dtype):
     """Masked, fully masked, NaN and +inf rows through the staged kernel
     (each row's maximum and sum cross its consumer warps)."""
