@@ -30,7 +30,7 @@ namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s
 
-constexpr int kRowregWaves = 16;   // row-block CTAs per resident CTA slot
+constexpr int kRowregWaves = 16;   // at most this many waves of resident CTAs
 constexpr int64_t kStagedChunk = 16384;   // bytes per bulk copy
 constexpr int64_t kStagedLookahead = 2;   // ring slots beyond one row slice
 constexpr int kStagedConsumerWarps = 8;       // default consumer warps per CTA (fp32)

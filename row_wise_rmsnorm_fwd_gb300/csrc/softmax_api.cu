@@ -11,7 +11,7 @@
 namespace rmsnorm {
 namespace {
 
-constexpr int kSoftmaxWaves = 4;                        // row-block CTAs per resident slot
+constexpr int kSoftmaxWaves = 4;                        // at most this many resident waves
 constexpr int64_t kSoftmaxSplitRowBytes = 32768;        // few rows wider than this: split
 constexpr int64_t kSoftmaxSplitMinBytes = 16 << 20;     // or few rows totalling this much
 constexpr int64_t kSoftmaxStagedChunk = 65536;          // bytes per bulk copy (default)
@@ -142,8 +142,13 @@ rmsnorm_status_t sm_plan_rowreg(const SmCall& c, int cluster, SmPlan* P) {
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
     int grid;
     if (cluster == 1) {
+        // whole waves of resident CTAs, each with three or more row blocks
+        // (as for the RMSNorm register kernel), at most kSoftmaxWaves waves
         const int64_t nblocks = (c.rows + rpc - 1) / rpc;
-        const int64_t target = static_cast<int64_t>(c.dv.sms) * occ * kSoftmaxWaves;
+        const int64_t resident = static_cast<int64_t>(c.dv.sms) * occ;
+        int64_t waves = nblocks / (3 * resident);
+        waves = waves < 1 ? 1 : (waves > kSoftmaxWaves ? kSoftmaxWaves : waves);
+        const int64_t target = resident * waves;
         grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
                                                : (nblocks < target ? nblocks : target));
     } else {
