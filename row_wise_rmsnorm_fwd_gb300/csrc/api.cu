@@ -30,7 +30,7 @@ namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s
 
-constexpr int kRowregWaves = 16;   // at most this many waves of resident CTAs
+constexpr int kRowregBlocksPerCta = 3;   // row blocks each CTA of the row kernel works on
 constexpr int64_t kStagedChunk = 16384;   // bytes per bulk copy
 constexpr int64_t kStagedLookahead = 2;   // ring slots beyond one row slice
 constexpr int kStagedConsumerWarps = 8;       // default consumer warps per CTA (fp32)
@@ -140,22 +140,23 @@ rmsnorm_status_t plan_rowreg(const Call& c, int cluster, Plan* P) {
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
     int grid;
     if (cluster == 1) {
-        // Grid-stride over row blocks with k waves of resident CTAs, k = the
-        // row blocks per resident CTA slot / 3, between 1 and 16: every CTA
-        // works on three or more row blocks (so the next-row prefetch has
-        // something to fetch and the weight slice loaded per CTA is reused),
-        // and the grid is a whole number of resident waves.  Measured on
-        // GB300: up to sixteen waves keep HBM busier than one (CTAs fall out
-        // of phase, so loads, reductions and stores overlap: on c4 and c5a 1
-        // wave gives 98%, 4 waves 98.5-100%, 16 waves 99-102% of the measured
-        // copy peak), while one CTA per row block on inputs of 3 to 16 waves
-        // lost 10-15% (c3: 14.9 against 12.8 us; 8192 bf16 rows of 8192:
-        // 50.3 against 43.9 us).  Fewer row blocks than resident slots: one
+        // Grid-stride over row blocks with k whole waves of resident CTAs, k =
+        // the row blocks per resident CTA slot / 3 (at least 1): every CTA
+        // works on about three row blocks, so the next-row prefetch has
+        // something to fetch and the weight slice loaded per CTA is reused,
+        // while CTAs start and finish all the time, which keeps them out of
+        // phase (loads, reductions and stores of different CTAs overlap).
+        // Measured on GB300 (% of the measured HBM copy peak): c5a with 16 /
+        // 48 / 120 / 143 / 431 waves (27 / 9 / 3.6 / 3.0 / 1 row blocks per
+        // CTA) 101.5 / 103.3 / 104.3 / 104.2 / 88.9%; c4 with 16 / 35 / 48 /
+        // 96 waves (6.7 / 3.1 / 2.2 / 1.1) 102.3 / 103.4 / 104.1 / 98.3%;
+        // c3 (3.4 row blocks per slot) 1 wave 12.8 us against 14.9 us with
+        // one CTA per row block.  Fewer row blocks than resident slots: one
         // CTA each.
         const int64_t nblocks = (c.rows + rpc - 1) / rpc;
         const int64_t resident = static_cast<int64_t>(c.info->sms) * occ;
-        int64_t waves = nblocks / (3 * resident);
-        waves = waves < 1 ? 1 : (waves > kRowregWaves ? kRowregWaves : waves);
+        int64_t waves = nblocks / (kRowregBlocksPerCta * resident);
+        if (waves < 1) waves = 1;
         const int64_t target = resident * waves;
         grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
                                                : (nblocks < target ? nblocks : target));
