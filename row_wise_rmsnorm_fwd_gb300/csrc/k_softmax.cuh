@@ -109,7 +109,7 @@ template <int NV>
 constexpr int softmax_max_threads() { return NV >= 4 ? 512 : 1024; }
 
 // PF: the next row's loads are issued before this row's two reductions
-// (register double buffer), doubling the bytes in flight for narrow rows.
+// (register double buffer), doubling the bytes in flight per thread.
 // CL: a thread-block cluster of p.cluster CTAs shares each row: every CTA
 // holds a slice, and the row maximum and the row sum are each combined across
 // the cluster through distributed shared memory (bounded waits).  A compile-

@@ -11,11 +11,13 @@
 namespace rmsnorm {
 namespace {
 
-constexpr int kSoftmaxWaves = 4;                        // at most this many resident waves
+constexpr int kSoftmaxWavesF32 = 8;                     // at most this many resident waves
+constexpr int kSoftmaxWavesBf16 = 4;
 constexpr int64_t kSoftmaxSplitRowBytes = 32768;        // few rows wider than this: split
 constexpr int64_t kSoftmaxSplitMinBytes = 16 << 20;     // or few rows totalling this much
 constexpr int64_t kSoftmaxStagedChunk = 65536;          // bytes per bulk copy (default)
-constexpr int64_t kSoftmaxStagedMinCols = 8192;         // wider rows go to the staged kernel
+constexpr int64_t kSoftmaxStagedMinCols = 8192;         // wider fp32 rows go to the staged kernel
+constexpr int64_t kSoftmaxStagedMinColsBf16 = 16384;    // wider bf16 rows go to the staged kernel
 constexpr int kSoftmaxMaxStagedCluster = 8;             // portable cluster sizes only
 
 struct SmCall {
@@ -142,13 +144,21 @@ rmsnorm_status_t sm_plan_rowreg(const SmCall& c, int cluster, SmPlan* P) {
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
     int grid;
     if (cluster == 1) {
-        // whole waves of resident CTAs, each with three or more row blocks
-        // (as for the RMSNorm register kernel), at most kSoftmaxWaves waves
+        // Whole waves of resident CTAs, each with three or more row blocks
+        // (as for the RMSNorm register kernel), at most 8 waves for fp32 and 4
+        // for bf16.  bf16 rows of four vectors per thread instead run two CTAs
+        // per SM, each through many rows.  Measured (% of the HBM roofline):
+        // fp32 rows of 512 with 2 / 4 / 8 waves 93 / 96 / 97; bf16 rows of
+        // 512 with 4 / 8 waves 87 / 83; bf16 rows of 1024 / 2048 / 4096 /
+        // 8192 elements 83 / 71 / 76 / 75 with two CTAs per SM against 83 /
+        // 66 / 74 / 74 with four waves.
         const int64_t nblocks = (c.rows + rpc - 1) / rpc;
         const int64_t resident = static_cast<int64_t>(c.dv.sms) * occ;
+        const int64_t max_waves = c.dtype == RMSNORM_DTYPE_F32 ? kSoftmaxWavesF32 : kSoftmaxWavesBf16;
         int64_t waves = nblocks / (3 * resident);
-        waves = waves < 1 ? 1 : (waves > kSoftmaxWaves ? kSoftmaxWaves : waves);
-        const int64_t target = resident * waves;
+        waves = waves < 1 ? 1 : (waves > max_waves ? max_waves : waves);
+        int64_t target = resident * waves;
+        if (c.dtype == RMSNORM_DTYPE_BF16 && NV == 4) target = 2 * static_cast<int64_t>(c.dv.sms);
         grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
                                                : (nblocks < target ? nblocks : target));
     } else {
@@ -282,14 +292,15 @@ rmsnorm_status_t sm_plan_staged(const SmCall& c, int cluster, SmPlan* P) {
 }
 
 // Automatic choice: few rows of wide rows (or large few-row inputs) are split
-// over a cluster (up to 8 CTAs, slices of at least 4 KB), as for RMSNorm; rows
-// of more than 8192 elements are staged through shared memory (measured on
-// 1 GB inputs: bf16 rows of 16384 / 32000 elements 60 / 76% of the HBM
-// roofline staged against 46 / 59% in registers; fp32 rows of 16384 / 32000
-// 87 / 97% against 78 / 86% for the best other kernel; at 8192 elements the
-// register kernel wins, 58 / 85% against 49 / 76%); narrower rows are held in
-// registers by the register kernel; what neither takes goes to the three-pass
-// kernel.
+// over a cluster (up to 8 CTAs, slices of at least 4 KB), as for RMSNorm;
+// fp32 rows of more than 8192 elements and bf16 rows of more than 16384 are
+// staged through shared memory (measured on 1 GB inputs, % of the HBM
+// roofline: fp32 rows of 16384 / 32000 elements 87 / 97 staged against 78 /
+// 86 for the best other kernel, rows of 8192 89 in registers against 75
+// staged; bf16 rows of 32000 86 staged against 61 in registers, rows of
+// 16384 64 in registers against 60 staged); narrower rows are held in
+// registers by the register kernel; what neither takes goes to the
+// three-pass kernel.
 rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
     switch (c.opt.path) {
         case RMSNORM_PATH_ROWREG: return sm_plan_rowreg(c, 1, P);
@@ -310,7 +321,7 @@ rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
             if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
         }
     }
-    if (c.cols > kSoftmaxStagedMinCols) {
+    if (c.cols > (c.dtype == RMSNORM_DTYPE_BF16 ? kSoftmaxStagedMinColsBf16 : kSoftmaxStagedMinCols)) {
         st = sm_plan_staged(c, 1, P);
         if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
         // fp32 rows too wide for one CTA's registers: split each over the
