@@ -85,7 +85,8 @@ typedef enum {
 typedef struct {
     int32_t path;            /* rmsnorm_path_t */
     int32_t cluster;         /* CTAs per row for CLUSTER (2..16) or STAGED (1..16) */
-    int32_t threads;         /* threads per row group (multiple of 32, <= 1024);
+    int32_t threads;         /* threads per row group (multiple of 32, <= 1024, or
+                                1, 2, 4, 8, 16 for ROWREG: several rows per warp);
                                 STAGED: consumer threads, 128 or 256 */
     int32_t grid;            /* CTAs to launch (rounded to the cluster size) */
     int32_t vec_bytes;       /* 16, 8, 4 or 2 (bf16 only); must suit the alignment */

@@ -251,6 +251,15 @@ __device__ __forceinline__ float warp_allreduce_sum(float v) {
     return v;
 }
 
+// The same within aligned groups of g lanes (g a power of two, 1..32): lane
+// masks below g never cross a group boundary.
+__device__ __forceinline__ float group_allreduce_sum(float v, int g) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1)
+        if (m < g) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+
 // ------------------------------------------------------------ status word --
 
 __device__ __forceinline__ void report_timeout(unsigned* status, unsigned site) {

@@ -1,8 +1,10 @@
 // k_rowreg.cuh -- single-pass, register-resident RMSNorm forward.
 //
-// One group of G threads (G a multiple of 32) owns one row at a time; each
-// thread owns NV vectors of VB bytes at vector indices t, t+G, t+2G, ... so
-// every load instruction of a warp covers 32*VB contiguous bytes.  The row is
+// One group of G threads (a multiple of 32, or a power of two below 32 for
+// rows of fewer than 32 vectors: 32 / G rows per warp) owns one row at a
+// time; each thread owns NV vectors of VB bytes at vector indices t, t+G,
+// t+2G, ... so every load instruction of a warp covers 32*VB contiguous
+// bytes (G < 32: consecutive rows, which are contiguous).  The row is
 // read from HBM exactly once (streaming, evict-first), kept in registers, and
 // written once.  The weight slice of each thread is loaded once per CTA and
 // stays in registers for every row the CTA processes.
@@ -10,7 +12,8 @@
 // Schedule per row (page "A hackable Python ML compiler, part 2": the Loop IR
 // and the generated kernel's cooperative reduction, redesigned):
 //   1. fp32 sum of squares of the thread's elements,
-//   2. butterfly shuffle sum within each warp,
+//   2. butterfly shuffle sum within each warp (within each G-lane group when
+//      G < 32),
 //   3. one shared-memory slot per warp, ONE barrier, then every thread adds
 //      its group's warp totals in a fixed order (the page's kernel used a
 //      three-level tree with a barrier per level),
@@ -122,8 +125,8 @@ rowreg_kernel(const Params p) {
                 }
             }
         }
-        // 2. warp butterfly
-        float ss = warp_allreduce_sum(s0 + s1);
+        // 2. warp butterfly (lane groups of G when a warp holds several rows)
+        float ss = G >= 32 ? warp_allreduce_sum(s0 + s1) : group_allreduce_sum(s0 + s1, G);
         // 3. cross-warp combine: one barrier, fixed order
         if (wpg > 1 || ncta > 1) {
             const int b = it & 1;

@@ -11,8 +11,9 @@
 //
 // The second small reduction the compiler write-up ("A hackable Python ML
 // compiler, part 2") lists among its wins, built from the same parts as the
-// RMSNorm row kernel: a group of G threads per row holding the row in
-// registers as NV vectors of VB bytes, persistent grid-stride row blocks, and
+// RMSNorm row kernel: a group of G threads per row (a multiple of 32, or a
+// power of two below 32 lanes for rows of fewer than 32 vectors) holding the
+// row in registers as NV vectors of VB bytes, persistent grid-stride row blocks, and
 // the warp butterfly + one-slot-per-warp combine -- used twice (max, then
 // sum of exponentials).  fp32 arithmetic; bf16 inputs widened exactly and
 // each output rounded once.  IEEE special cases follow the definition: -inf
@@ -61,6 +62,14 @@ __device__ __forceinline__ float row_exp(float v, float c) {
 __device__ __forceinline__ float warp_allreduce_max(float v) {
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+    return v;
+}
+
+// The same within aligned groups of g lanes (g a power of two, 1..32).
+__device__ __forceinline__ float group_allreduce_max(float v, int g) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1)
+        if (m < g) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
     return v;
 }
 
@@ -190,8 +199,8 @@ softmax_rowreg_kernel(const Params p) {
             }
         }
         float m = fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3]));
-        // row maximum
-        m = warp_allreduce_max(m);
+        // row maximum (within lane groups of G when a warp holds several rows)
+        m = G >= 32 ? warp_allreduce_max(m) : group_allreduce_max(m, G);
         if (wpg > 1) {
             if (lane == 0) red[0][b][warp] = m;
             __syncthreads();
@@ -219,7 +228,8 @@ softmax_rowreg_kernel(const Params p) {
                 }
             }
         }
-        float s = warp_allreduce_sum((sk[0] + sk[1]) + (sk[2] + sk[3]));
+        const float sl = (sk[0] + sk[1]) + (sk[2] + sk[3]);
+        float s = G >= 32 ? warp_allreduce_sum(sl) : group_allreduce_sum(sl, G);
         if (wpg > 1) {
             if (lane == 0) red[1][b][warp] = s;
             __syncthreads();

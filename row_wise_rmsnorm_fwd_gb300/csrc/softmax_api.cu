@@ -87,8 +87,10 @@ rmsnorm_status_t sm_validate(int32_t dtype, const void* x, const void* y, int64_
             return RMSNORM_ERR_INVALID_ARG;
         if (o.cluster > 1 && o.path != RMSNORM_PATH_CLUSTER && o.path != RMSNORM_PATH_STAGED)
             return RMSNORM_ERR_INVALID_ARG;
-        if (o.threads < 0 || o.threads % 32 != 0 || o.threads > 1024 || o.grid < 0)
+        const bool sub_warp = o.threads > 0 && o.threads < 32 && (o.threads & (o.threads - 1)) == 0;
+        if (o.threads < 0 || (o.threads % 32 != 0 && !sub_warp) || o.threads > 1024 || o.grid < 0)
             return RMSNORM_ERR_INVALID_ARG;
+        if (sub_warp && o.path != RMSNORM_PATH_ROWREG) return RMSNORM_ERR_INVALID_ARG;
     }
     return RMSNORM_OK;
 }
@@ -120,9 +122,24 @@ rmsnorm_status_t sm_plan_rowreg(const SmCall& c, int cluster, SmPlan* P) {
         const int64_t need = (per + G - 1) / G;
         if (need > 8) return RMSNORM_ERR_UNSUPPORTED;
         NV = sm_pow2_ceil(need);
+    } else if (cluster == 1 && c.dtype == RMSNORM_DTYPE_BF16 && per <= 8 * 256) {
+        // bf16 rows of up to 2048 vectors: 8 vectors per thread (2 for rows
+        // of at most 16 vectors), pow2(vectors / NV) lanes per row.  bf16
+        // softmax is instruction bound, and the per-row work (reductions,
+        // shuffles) is best spread over many elements per thread.  Measured
+        // (% of the HBM roofline) on 128 MB inputs, rows of 64 / 128 / 256 /
+        // 512 / 1024 / 2048 elements: 87 / 87 / 89 / 90 / 90 / 90, against
+        // 81 / 85 / 85 / 83 / 83 / 69 with 4 vectors per thread; on 512 MB
+        // inputs, rows of 4096 / 8192 / 16384: 80 / 81 / 81 against 78 / 77 /
+        // 65 (and 62 staged at 16384).
+        NV = per <= 16 ? (per >= 2 ? 2 : 1) : 8;
+        G = sm_pow2_ceil((per + NV - 1) / NV);
     } else if (cluster == 1 && per <= 32 * 4) {
-        G = 32;
-        NV = sm_pow2_ceil((per + 31) / 32);
+        // rows of up to 128 vectors: 4 vectors per thread (fewer for rows of
+        // fewer than 4) and pow2(vectors / 4) lanes per row, 32 / G rows per
+        // warp (as for the RMSNorm register kernel)
+        NV = per >= 4 ? 4 : sm_pow2_ceil(per);
+        G = sm_pow2_ceil((per + NV - 1) / NV);
     } else {
         NV = 4;
         int64_t g = sm_round_up((per + NV - 1) / NV, 32);
@@ -146,19 +163,23 @@ rmsnorm_status_t sm_plan_rowreg(const SmCall& c, int cluster, SmPlan* P) {
     if (cluster == 1) {
         // Whole waves of resident CTAs, each with three or more row blocks
         // (as for the RMSNorm register kernel), at most 8 waves for fp32 and 4
-        // for bf16.  bf16 rows of four vectors per thread instead run two CTAs
-        // per SM, each through many rows.  Measured (% of the HBM roofline):
-        // fp32 rows of 512 with 2 / 4 / 8 waves 93 / 96 / 97; bf16 rows of
-        // 512 with 4 / 8 waves 87 / 83; bf16 rows of 1024 / 2048 / 4096 /
-        // 8192 elements 83 / 71 / 76 / 75 with two CTAs per SM against 83 /
-        // 66 / 74 / 74 with four waves.
+        // for bf16.  bf16 rows of four or more vectors per thread instead run
+        // two CTAs per SM, each through many rows, and bf16 rows of two
+        // vectors per thread eight CTAs per SM.  Measured (% of the HBM
+        // roofline): fp32 rows of 512 with 2 / 4 / 8 waves 93 / 96 / 97; bf16
+        // rows of 1024 / 2048 / 4096 / 8192 elements at 4 vectors per thread
+        // 83 / 71 / 76 / 75 with two CTAs per SM against 83 / 66 / 74 / 74
+        // with four waves; bf16 rows of 512 at 8 vectors per thread 90 with
+        // two CTAs per SM, 87 with eight.
         const int64_t nblocks = (c.rows + rpc - 1) / rpc;
         const int64_t resident = static_cast<int64_t>(c.dv.sms) * occ;
         const int64_t max_waves = c.dtype == RMSNORM_DTYPE_F32 ? kSoftmaxWavesF32 : kSoftmaxWavesBf16;
         int64_t waves = nblocks / (3 * resident);
         waves = waves < 1 ? 1 : (waves > max_waves ? max_waves : waves);
         int64_t target = resident * waves;
-        if (c.dtype == RMSNORM_DTYPE_BF16 && NV == 4) target = 2 * static_cast<int64_t>(c.dv.sms);
+        if (c.dtype == RMSNORM_DTYPE_BF16 && NV >= 4) target = 2 * static_cast<int64_t>(c.dv.sms);
+        if (c.dtype == RMSNORM_DTYPE_BF16 && NV <= 2 && G < 32)
+            target = 8 * static_cast<int64_t>(c.dv.sms);
         grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
                                                : (nblocks < target ? nblocks : target));
     } else {

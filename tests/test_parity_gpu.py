@@ -191,6 +191,27 @@ def test_forced_launch_shapes(dtype):
     compare(run(xc, wc, 1e-6, path="twopass", threads=96), ref, "twopass 96")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("hidden", [1, 4, 24, 64, 100, 128, 200, 256])
+def test_sub_warp_row_groups(dtype, hidden):
+    """Rows of fewer than 32 vectors: 1-16 lanes per row, several rows per
+    warp; the group reduction must not mix neighbouring rows (rows of very
+    different scale sit next to each other)."""
+    rows = 1000
+    x, w = rand_case(rows, hidden, dtype, seed=hidden + 17)
+    x = x * torch.logspace(-3, 3, rows).to(x.dtype).unsqueeze(1)
+    ref = oracle_for(x, w, 1e-6)
+    xc, wc = x.cuda(), w.cuda()
+    compare(run(xc, wc, 1e-6), ref, f"auto {dtype} H={hidden}")
+    for g in (1, 2, 4, 8, 16):
+        try:
+            y = run(xc, wc, 1e-6, path="rowreg", threads=g, grid=77)
+        except binding.RmsnormError as e:
+            assert e.status == binding.RMSNORM_ERR_UNSUPPORTED
+            continue
+        compare(y, ref, f"G={g} {dtype} H={hidden}")
+
+
 # ----------------------------------------------------- layout edge cases --
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])

@@ -172,6 +172,26 @@ def test_staged_cluster_special_values(dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", [1, 3, 16, 64, 100, 128, 255])
+def test_sub_warp_row_groups(dtype, cols):
+    """Rows of fewer than 32 vectors: 1-16 lanes per row, several rows per
+    warp; the group maximum and sum must not mix neighbouring rows."""
+    rows = 700
+    x = case(rows, cols, dtype, cols + 5)
+    x = (x.float() + torch.linspace(-50, 50, rows).unsqueeze(1)).to(DT[dtype])
+    ref = ref_for(x)
+    xc = x.cuda()
+    compare(run(xc), ref, f"auto {dtype} cols={cols}")
+    for g in (1, 2, 4, 8, 16):
+        try:
+            y = run(xc, path="rowreg", threads=g, grid=53)
+        except binding.RmsnormError as e:
+            assert e.status == binding.RMSNORM_ERR_UNSUPPORTED
+            continue
+        compare(y, ref, f"G={g} {dtype} cols={cols}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_staged_special_values(dtype):
     """Masked, fully masked, NaN and +inf rows through the staged kernel
     (each row's maximum and sum cross its consumer warps)."""
