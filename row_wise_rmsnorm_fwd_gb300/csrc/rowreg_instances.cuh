@@ -48,6 +48,11 @@ KernelFn rowreg_pick_nv(int nv, bool pf) {
                 }
             }
         }
+        if constexpr (VB == 16) {
+            // 3 vectors per thread fit rows of 3 x 32k vectors without the idle
+            // lanes 4 would leave (16-byte vectors only)
+            if (nv == 3) return rowreg_instance<T, VB, 3, kPF, EPI>();
+        }
         switch (nv) {
             case 1: return rowreg_instance<T, VB, 1, kPF, EPI>();
             case 2: return rowreg_instance<T, VB, 2, kPF, EPI>();
