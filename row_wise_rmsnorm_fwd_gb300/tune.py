@@ -7,7 +7,8 @@ The row kernel has four compile-time policies (``rowreg_instances.cuh``):
 register prefetch of the next row (PF), weights held in registers (WREG), the
 cache policy of the x loads (LD) and of the y stores (ST).  This builds one
 library per variant from the same sources (``_build/tune/``), then times every
-variant on each workload for a few grid sizes, interleaving variants and
+variant on each workload for a few grid sizes (the automatic one among them),
+interleaving variants and
 repeating three times (median), and prints one JSON line per (variant,
 workload, grid).  The product library keeps the defaults this measured best.
 """
@@ -77,7 +78,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--variants", default=",".join(VARIANTS))
     ap.add_argument("--workloads", default="c4,c5a")
-    ap.add_argument("--waves", default="1,4,16", help="grid = waves x resident CTAs")
+    ap.add_argument("--grids", default="0,9728,29184,86944",
+                    help="CTA counts to time (0 = the library's automatic grid)")
     ap.add_argument("--iters", type=int, default=30)
     ap.add_argument("--out", default="")
     args = ap.parse_args()
@@ -96,9 +98,8 @@ def main():
         y = torch.empty_like(x)
         dt = binding.RMSNORM_DTYPE_F32 if wl.dtype == "f32" else binding.RMSNORM_DTYPE_BF16
         handle = torch.cuda.current_stream().cuda_stream
-        base_plan = binding.rmsnorm_plan(x, w, y, options={"path": "rowreg"})
-        resident = max(1, base_plan["grid"] // 16)          # the default launches 16 waves
-        grids = [int(k) * resident for k in args.waves.split(",")]
+        auto_grid = binding.rmsnorm_plan(x, w, y, options={"path": "rowreg"})["grid"]
+        grids = [int(g) or auto_grid for g in args.grids.split(",")]
         times = {}
         for _ in range(3):
             for n in names:

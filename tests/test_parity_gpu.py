@@ -332,6 +332,35 @@ def test_plan_reports_families():
     assert p["cluster"] > 1
 
 
+@pytest.mark.parametrize("shape,dtype,kernel,lanes,nv", [
+    ((262144, 8192), "bf16", "rowreg", 256, 4),      # c5a
+    ((65536, 4096), "f32", "rowreg", 256, 4),        # c4
+    ((4096, 128), "bf16", "rowreg", 4, 4),           # per-head QK norm: 8 rows per warp
+    ((4096, 1536), "bf16", "rowreg", 64, 3),         # 3 vectors leave no lane idle
+    ((1024, 16384), "f32", "staged_bulk", 256, 0),   # fp32 rows of 64 KB
+    ((1024, 12288), "f32", "ringreg", 384, 8),       # fp32 rows of 48 KB
+    ((1024, 32768), "f32", "ringreg", 512, 16),      # fp32 rows of 128 KB
+    ((1024, 24576), "f32", "twopass", 1024, 0),      # fp32 rows of 96 KB
+    ((8, 262144), "bf16", "cluster_rowreg", 512, 8), # c5b: few wide rows
+])
+def test_automatic_choice(shape, dtype, kernel, lanes, nv):
+    """The automatic kernel choice for representative shapes (a guard on the
+    measured selection rules; no launch)."""
+    x = torch.empty(shape, dtype=DT[dtype], device="cuda")
+    w = torch.empty(shape[-1], dtype=DT[dtype], device="cuda")
+    p = binding.rmsnorm_plan(x, w)
+    assert p["kernel"] == kernel, p
+    assert p["threads_per_row"] == lanes and p["vecs_per_thread"] == nv, p
+
+
+def test_row_kernel_grid_has_about_three_row_blocks_per_cta():
+    x = torch.empty(262144, 8192, dtype=torch.bfloat16, device="cuda")
+    w = torch.empty(8192, dtype=torch.bfloat16, device="cuda")
+    p = binding.rmsnorm_plan(x, w)
+    blocks = 262144 // p["rows_per_cta"]
+    assert 3 <= blocks / p["grid"] < 4, p
+
+
 def test_unsupported_forced_option_launches_nothing():
     x = torch.ones(4, 2050, device="cuda")   # 8200-byte rows: no 16-byte pitch
     w = torch.ones(2050, device="cuda")

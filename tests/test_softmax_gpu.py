@@ -252,6 +252,23 @@ def test_guards_and_determinism(dtype):
         assert torch.equal(run(x), y)
 
 
+@pytest.mark.parametrize("shape,dtype,kernel", [
+    ((131072, 512), "f32", "softmax_rowreg"),
+    ((131072, 512), "bf16", "softmax_rowreg"),
+    ((4096, 32000), "f32", "softmax_staged"),
+    ((8192, 32000), "bf16", "softmax_staged"),
+    ((16384, 16384), "bf16", "softmax_rowreg"),          # eight vectors per thread
+    ((1024, 128256), "f32", "softmax_cluster_staged"),   # prefill logits, fp32
+    ((2048, 128256), "bf16", "softmax_threepass"),       # prefill logits, bf16
+    ((8, 128256), "f32", "softmax_cluster_rowreg"),      # decode logits
+])
+def test_automatic_choice(shape, dtype, kernel):
+    """The automatic kernel choice for representative shapes (no launch)."""
+    x = torch.empty(shape, dtype=DT[dtype], device="cuda")
+    p = binding.rowsoftmax_plan(x, torch.empty_like(x))
+    assert p["kernel"] == kernel, p
+
+
 def test_rows_sum_to_one_and_match_torch():
     x = case(1000, 512, "f32", 5).cuda()
     y = run(x)
