@@ -90,13 +90,14 @@ typedef struct {
                                 STAGED: consumer threads, 128 or 256 */
     int32_t grid;            /* CTAs to launch (rounded to the cluster size) */
     int32_t vec_bytes;       /* 16, 8, 4 or 2 (bf16 only); must suit the alignment */
-    int32_t chunk_bytes;     /* STAGED: bytes per bulk copy (multiple of 16) */
+    int32_t chunk_bytes;     /* STAGED: bytes per bulk copy (multiple of 16); RINGREG: see
+                                RMSNORM_PATH_RINGREG */
     int32_t stages;          /* STAGED: chunk slots in the shared-memory ring (>= chunks per
-                                row slice, <= 32) */
+                                row slice, <= 32); RINGREG: ring slots (2..32) */
     int32_t weights;         /* STAGED: 1 = weight slice copied to shared memory once,
                                 2 = weights read through L1/L2 every row */
-    int32_t fault_inject;    /* failure-detection tests only: 1 = the staged kernel's
-                                producer withholds its first copy, 2 = one CTA of a
+    int32_t fault_inject;    /* failure-detection tests only: 1 = the bulk-copy producer
+                                (STAGED, RINGREG) withholds its first copy, 2 = one CTA of a
                                 split-row cluster withholds its partial sum.  Honoured
                                 only by the test build of the library (compiled with
                                 RMSNORM_FAULT_INJECT); the product library returns
