@@ -78,10 +78,11 @@ def check_bf16(bits_gpu: np.ndarray, bits_ref: np.ndarray, what: str = ""):
             f"ref 0x{int(bits_ref[ok][i]):04x} ({int(d[i])} ulp)")
 
 
-def compare_every_row(x_dev: torch.Tensor, y_dev: torch.Tensor, w_cpu: torch.Tensor,
-                      eps: float, what: str = "", chunk_rows: int = 16384,
-                      piece_elems: int = 1 << 20, threads: int = 0):
-    """Check every row of a full-size GPU result against the oracle.
+def compare_every_row(x_dev: torch.Tensor, y_dev: torch.Tensor, w_cpu, eps: float,
+                      what: str = "", chunk_rows: int = 16384, piece_elems: int = 1 << 20,
+                      threads: int = 0, op: str = "rmsnorm"):
+    """Check every row of a full-size GPU result against the oracle (op
+    "rmsnorm", or "softmax" with w_cpu and eps unused).
 
     Rows are copied to the host in chunks of ``chunk_rows``; each chunk is cut
     into pieces of about ``piece_elems`` elements that host threads run
@@ -98,7 +99,9 @@ def compare_every_row(x_dev: torch.Tensor, y_dev: torch.Tensor, w_cpu: torch.Ten
     piece_rows = max(1, piece_elems // hidden)
     threads = threads or max(1, len(os.sched_getaffinity(0)))
     f32 = x_dev.dtype == torch.float32
-    w_host = w_cpu.numpy() if f32 else workloads.bf16_bits(w_cpu)
+    w_host = None
+    if op == "rmsnorm":
+        w_host = w_cpu.numpy() if f32 else workloads.bf16_bits(w_cpu)
     local = threading.local()
 
     def piece(args):
@@ -109,7 +112,13 @@ def compare_every_row(x_dev: torch.Tensor, y_dev: torch.Tensor, w_cpu: torch.Ten
         if bufs is None or bufs[0].shape != tuple(xs.shape):
             bufs = (np.zeros(tuple(xs.shape), np.float64), np.zeros(tuple(xs.shape), np.uint16))
             local.bufs = bufs
-        if f32:
+        if op == "softmax":
+            if f32:
+                ref = oracle.rowsoftmax_f32(xs.numpy(), out=bufs[0])
+            else:
+                _, ref = oracle.rowsoftmax_bf16(workloads.bf16_bits(xs), out64=bufs[0],
+                                                out16=bufs[1])
+        elif f32:
             ref = oracle.rmsnorm_f32(xs.numpy(), w_host, eps, out=bufs[0])
         else:
             _, ref = oracle.rmsnorm_bf16(workloads.bf16_bits(xs), w_host, eps,

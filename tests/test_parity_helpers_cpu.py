@@ -40,3 +40,19 @@ def test_every_row_finds_one_bad_element(dtype, row):
     lo = int(str(e.value).split("rows ")[1].split("..")[0])
     hi = int(str(e.value).split("..")[1].split(":")[0])
     assert lo <= row <= hi
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_every_row_softmax_mode(dtype):
+    x = workloads.make_random((300, 257), dtype, 5, ("normal", 0.0, 3.0))
+    if dtype == "f32":
+        y = torch.from_numpy(oracle.rowsoftmax_f32(x.numpy()).astype(np.float32))
+    else:
+        _, y16 = oracle.rowsoftmax_bf16(workloads.bf16_bits(x))
+        y = workloads.from_bf16_bits(y16)
+    compare_every_row(x, y, None, 0.0, "clean", chunk_rows=128, piece_elems=40 * 257,
+                      threads=3, op="softmax")
+    y[131, 7] = y[131, 7] * 1.5 + 0.01
+    with pytest.raises(AssertionError):
+        compare_every_row(x, y, None, 0.0, "planted", chunk_rows=128, piece_elems=40 * 257,
+                          threads=3, op="softmax")
