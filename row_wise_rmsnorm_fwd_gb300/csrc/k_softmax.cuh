@@ -120,17 +120,18 @@ constexpr int softmax_max_threads() { return NV >= 4 ? 512 : 1024; }
 // PF: the next row's loads are issued before this row's two reductions
 // (register double buffer), doubling the bytes in flight per thread.
 // CL: a thread-block cluster of p.cluster CTAs shares each row: every CTA
-// holds a slice, and the row maximum and the row sum are each combined across
-// the cluster through distributed shared memory (bounded waits).  A compile-
-// time switch, so that the plain instances carry none of the cluster code
-// (measured: with the cluster branches present but idle, 1 KB bf16 rows ran
-// about 8% slower).
+// holds a slice, computes exponentials and their sum relative to its slice's
+// maximum, and one exchange of the (maximum, sum) pair through distributed
+// shared memory (bounded wait) gives the row's, with which each CTA rescales
+// its slice.  A compile-time switch, so that the plain instances carry none of
+// the cluster code (measured: with the cluster branches present but idle, 1 KB
+// bf16 rows ran about 8% slower).
 template <typename T, int VB, int NV, bool PF, bool CL>
 __global__ void __launch_bounds__(softmax_max_threads<NV>())
 softmax_rowreg_kernel(const Params p) {
     constexpr int EPV = VecTraits<T, VB>::kElems;
     __shared__ float red[2][2][32];      // [max | sum][double buffer][warp]
-    __shared__ ClusterExchange exmax, exsum;
+    __shared__ PairExchange ex;        // cluster split only
 
     const int G = p.group;
     const int tid = threadIdx.x;
@@ -147,7 +148,13 @@ softmax_rowreg_kernel(const Params p) {
         rank = cluster_ctarank();
         unit = cluster_id_x();
         nunits = cluster_count_x();
-        cluster_exchange_init(&exmax, ncta, &exsum);
+        if (tid == 0) {
+            mbar_init(smem_addr(&ex.bar[0]), ncta);
+            mbar_init(smem_addr(&ex.bar[1]), ncta);
+            fence_mbarrier_init_cluster();
+        }
+        __syncthreads();
+        cluster_sync_all();        // no peer arrives before the barriers exist
     }
     const int vbase = CL ? static_cast<int>(rank) * p.slice_vecs : 0;
     const int vlim = CL ? min(p.nvec, vbase + p.slice_vecs) : p.nvec;
@@ -207,14 +214,9 @@ softmax_rowreg_kernel(const Params p) {
             m = -INFINITY;
             for (int k = 0; k < wpg; ++k) m = fmaxf(m, red[0][b][gw0 + k]);
         }
-        if (CL) {
-            float cm;
-            const bool ok = cluster_allreduce<true>(&exmax, m, ncta, rank, it, p, &cm, tid);
-            m = cm;
-            if (__syncthreads_or(!ok)) break;   // uniform: stop, then leave cleanly
-        }
-        // exponentials and their sum
-        const float c = row_exp_bias<T>() - m * kLog2e;
+        // exponentials and their sum, relative to this CTA's maximum when a
+        // cluster splits the row (a slice of -inf keeps -inf: exp(-inf) = 0)
+        const float c = (CL && m == -INFINITY) ? -INFINITY : row_exp_bias<T>() - m * kLog2e;
         float sk[4] = {0.f, 0.f, 0.f, 0.f};
         if (row_ok) {
 #pragma unroll
@@ -236,13 +238,14 @@ softmax_rowreg_kernel(const Params p) {
             s = 0.f;
             for (int k = 0; k < wpg; ++k) s += red[1][b][gw0 + k];
         }
+        float inv = 1.0f / s;
         if (CL) {
-            float cs;
-            const bool ok = cluster_allreduce(&exsum, s, ncta, rank, it, p, &cs, tid);
-            s = cs;
-            if (__syncthreads_or(!ok)) break;
+            // one exchange of the (maximum, sum) pair gives the row's
+            float M, S;
+            const bool ok = cluster_pair_allreduce(&ex, m, s, ncta, rank, it, p, &M, &S, tid);
+            if (__syncthreads_or(!ok)) break;   // uniform: stop, then leave cleanly
+            inv = exp2f((m - M) * kLog2e) / S;   // rescale this slice to the row's maximum
         }
-        const float inv = 1.0f / s;
         if (row_ok) {
             char* dst = yb + row * row_bytes;
 #pragma unroll
