@@ -410,32 +410,26 @@ struct ClusterExchange {
     float slot[2][16];
 };
 
-// Initialise (thread 0) one or two exchanges, make the barriers visible
-// cluster-wide, and sync the cluster so no peer arrives before initialisation.
-__device__ __forceinline__ void cluster_exchange_init(ClusterExchange* ex, int ncta,
-                                                      ClusterExchange* ex2 = nullptr) {
+// Initialise (thread 0) the exchange, make its barriers visible cluster-wide,
+// and sync the cluster so no peer arrives before initialisation.
+__device__ __forceinline__ void cluster_exchange_init(ClusterExchange* ex, int ncta) {
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(&ex->bar[0]), ncta);
         mbar_init(smem_addr(&ex->bar[1]), ncta);
-        if (ex2) {
-            mbar_init(smem_addr(&ex2->bar[0]), ncta);
-            mbar_init(smem_addr(&ex2->bar[1]), ncta);
-        }
         fence_mbarrier_init_cluster();
     }
     __syncthreads();
     cluster_sync_all();
 }
 
-// Combine `part` (this CTA's value, identical in all participating threads)
-// over the cluster: the sum, or the maximum when kMax.  Every CTA combines
-// the C slots in rank order, so every CTA gets the bitwise same result.
+// Sum `part` (this CTA's value, identical in all participating threads) over
+// the cluster.  Every CTA adds the C slots in rank order, so every CTA gets
+// the bitwise same result.
 // `it` is this CTA's row iteration count and `lt` the caller's index among
 // the participating threads (the first `ncta` of them send).  Returns false
 // if the bounded wait expired (the status word is then set).  The caller
 // must pass a barrier over the participants after this returns and before
 // its next call on the same exchange (the slots are reused two rows on).
-template <bool kMax = false>
 __device__ __forceinline__ bool cluster_allreduce(ClusterExchange* ex, float part, int ncta,
                                                   uint32_t rank, uint32_t it,
                                                   const Params& p, float* total, int lt) {
@@ -453,10 +447,9 @@ __device__ __forceinline__ bool cluster_allreduce(ClusterExchange* ex, float par
     }
     const bool ok = mbar_wait_bounded<true>(smem_addr(&ex->bar[b]), (it >> 1) & 1u,
                                             p.timeout_ns);
-    float s = kMax ? -INFINITY : 0.f;
+    float s = 0.f;
     if (ok) {
-        for (int c = 0; c < ncta; ++c)
-            s = kMax ? fmaxf(s, ex->slot[b][c]) : s + ex->slot[b][c];
+        for (int c = 0; c < ncta; ++c) s += ex->slot[b][c];
     } else if (lt == 0) {
         report_timeout(p.status, kSiteClusterExchange);
     }
