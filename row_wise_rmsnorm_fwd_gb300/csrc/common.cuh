@@ -291,12 +291,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
 }
 
-// Arrive on the mbarrier at the same offset in CTA `rank` of this cluster.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
-                 :: "r"(bar_cluster_addr) : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -388,8 +382,19 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
+// Asynchronous stores into the shared memory of a CTA of this cluster (addr
+// and bar are shared::cluster addresses in the same CTA): the stored bytes
+// complete transaction count on that CTA's mbarrier `bar`, whose phase
+// completion releases them at cluster scope.  One one-way trip, no fence.
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];"
+                 :: "r"(addr), "f"(v), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void st_async_v2_f32(uint32_t addr, float a, float b, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+        :: "r"(addr), "f"(a), "f"(b), "r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -405,17 +410,21 @@ __device__ __forceinline__ void fence_mbarrier_init_cluster() {
 
 // Shared-memory state of the DSMEM exchange: two slot sets and two mbarriers,
 // used alternately by consecutive rows (a peer can be at most one row ahead).
+// Each barrier phase takes one local arrival, which also expects the bytes of
+// the C slots; every CTA's st.async completes its share.  A peer's bytes may
+// land before the local arrival (the transaction count then dips below zero,
+// which the mbarrier allows); the phase completes only once both happened.
 struct ClusterExchange {
     alignas(8) unsigned long long bar[2];
     float slot[2][16];
 };
 
 // Initialise (thread 0) the exchange, make its barriers visible cluster-wide,
-// and sync the cluster so no peer arrives before initialisation.
-__device__ __forceinline__ void cluster_exchange_init(ClusterExchange* ex, int ncta) {
+// and sync the cluster so no peer stores before initialisation.
+__device__ __forceinline__ void cluster_exchange_init(ClusterExchange* ex) {
     if (threadIdx.x == 0) {
-        mbar_init(smem_addr(&ex->bar[0]), ncta);
-        mbar_init(smem_addr(&ex->bar[1]), ncta);
+        mbar_init(smem_addr(&ex->bar[0]), 1);
+        mbar_init(smem_addr(&ex->bar[1]), 1);
         fence_mbarrier_init_cluster();
     }
     __syncthreads();
@@ -434,19 +443,18 @@ __device__ __forceinline__ bool cluster_allreduce(ClusterExchange* ex, float par
                                                   uint32_t rank, uint32_t it,
                                                   const Params& p, float* total, int lt) {
     const uint32_t b = it & 1u;
+    const uint32_t bar = smem_addr(&ex->bar[b]);
+    if (lt == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ncta) * 4u);
     bool send = lt < ncta;
 #if RMSNORM_FAULT_INJECT
     if (p.fault == kFaultClusterWithholdPartial && rank == 0 && it == 0) send = false;
 #endif
     if (send) {
         const uint32_t peer = static_cast<uint32_t>(lt);
-        const uint32_t slot = map_to_rank(smem_addr(&ex->slot[b][rank]), peer);
-        const uint32_t bar = map_to_rank(smem_addr(&ex->bar[b]), peer);
-        st_cluster_f32(slot, part);
-        mbar_arrive_remote(bar);   // release.cluster orders the store before it
+        st_async_f32(map_to_rank(smem_addr(&ex->slot[b][rank]), peer), part,
+                     map_to_rank(bar, peer));
     }
-    const bool ok = mbar_wait_bounded<true>(smem_addr(&ex->bar[b]), (it >> 1) & 1u,
-                                            p.timeout_ns);
+    const bool ok = mbar_wait_bounded<true>(bar, (it >> 1) & 1u, p.timeout_ns);
     float s = 0.f;
     if (ok) {
         for (int c = 0; c < ncta; ++c) s += ex->slot[b][c];

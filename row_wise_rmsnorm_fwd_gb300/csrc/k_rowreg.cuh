@@ -60,7 +60,7 @@ rowreg_kernel(const Params p) {
         rank = cluster_ctarank();
         unit = cluster_id_x();
         nunits = cluster_count_x();
-        cluster_exchange_init(&ex, ncta);
+        cluster_exchange_init(&ex);
     }
 
     // Vector indices this thread owns inside the row (or the CTA's slice).

@@ -92,15 +92,14 @@ __device__ __forceinline__ bool cluster_pair_allreduce(PairExchange* ex, float m
                                                        const Params& p, float* M, float* S,
                                                        int lt) {
     const uint32_t b = it & 1u;
+    const uint32_t bar = smem_addr(&ex->bar[b]);
+    if (lt == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ncta) * 8u);
     if (lt < ncta) {
         const uint32_t peer = static_cast<uint32_t>(lt);
-        const uint32_t slot = map_to_rank(smem_addr(&ex->slot[b][rank]), peer);
-        asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" :: "r"(slot), "f"(m), "f"(s)
-                     : "memory");
-        mbar_arrive_remote(map_to_rank(smem_addr(&ex->bar[b]), peer));
+        st_async_v2_f32(map_to_rank(smem_addr(&ex->slot[b][rank]), peer), m, s,
+                        map_to_rank(bar, peer));
     }
-    const bool ok = mbar_wait_bounded<true>(smem_addr(&ex->bar[b]), (it >> 1) & 1u,
-                                            p.timeout_ns);
+    const bool ok = mbar_wait_bounded<true>(bar, (it >> 1) & 1u, p.timeout_ns);
     float mx = -INFINITY, sum = 0.f;
     if (ok) {
         for (int c = 0; c < ncta; ++c) mx = fmaxf(mx, ex->slot[b][c].x);
@@ -149,8 +148,8 @@ softmax_rowreg_kernel(const Params p) {
         unit = cluster_id_x();
         nunits = cluster_count_x();
         if (tid == 0) {
-            mbar_init(smem_addr(&ex.bar[0]), ncta);
-            mbar_init(smem_addr(&ex.bar[1]), ncta);
+            mbar_init(smem_addr(&ex.bar[0]), 1);
+            mbar_init(smem_addr(&ex.bar[1]), 1);
             fence_mbarrier_init_cluster();
         }
         __syncthreads();
@@ -335,8 +334,8 @@ __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kerne
     }
     if (CL) {
         if (tid == 0) {
-            mbar_init(smem_addr(&ex->bar[0]), ncta);
-            mbar_init(smem_addr(&ex->bar[1]), ncta);
+            mbar_init(smem_addr(&ex->bar[0]), 1);
+            mbar_init(smem_addr(&ex->bar[1]), 1);
             fence_mbarrier_init_cluster();
         }
         __syncthreads();

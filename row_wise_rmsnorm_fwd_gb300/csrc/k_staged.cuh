@@ -69,8 +69,8 @@ __global__ void __maxnreg__(96) staged_kernel(const Params p) {
         ring_init(ring, NCW);
         mbar_init(smem_addr(wbar), 1);
         if (ncta > 1) {
-            mbar_init(smem_addr(&ex->bar[0]), ncta);
-            mbar_init(smem_addr(&ex->bar[1]), ncta);
+            mbar_init(smem_addr(&ex->bar[0]), 1);   // one local arrival per phase
+            mbar_init(smem_addr(&ex->bar[1]), 1);
         }
         fence_mbarrier_init_cluster();
     }
