@@ -141,6 +141,11 @@ def test_staged_ring_shapes(dtype, rows, cols, chunk, stages, grid, threads):
     (50, 1928, 16, 64, 0, 0),          # 16-CTA clusters; the last slice is short, so
                                        # some of its chunks are empty
     (5, 8200, 8, 1024, 0, 0),
+    (41, 32808, 2, 0, 0, 4),           # two clusters of 20 and 21 rows: odd and even
+                                       # row counts through the double-buffered exchange
+    (7, 128256, 4, 0, 3, 8),           # clusters of 4 and 3 rows
+    (64, 100000, 8, 16384, 0, 8),      # one cluster, 64 rows, two chunks per slice;
+                                       # short last slice
 ])
 def test_staged_cluster_split(dtype, rows, cols, cluster, chunk, stages, grid):
     """Rows split over a cluster of CTAs, each staging its slice through its
