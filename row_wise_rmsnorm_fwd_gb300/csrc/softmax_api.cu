@@ -19,6 +19,7 @@ constexpr int64_t kSoftmaxStagedChunk = 65536;          // bytes per bulk copy (
 constexpr int64_t kSoftmaxStagedMinCols = 8192;         // wider fp32 rows go to the staged kernel
 constexpr int64_t kSoftmaxStagedMinColsBf16 = 16384;    // wider bf16 rows go to the staged kernel
 constexpr int kSoftmaxMaxStagedCluster = 8;             // portable cluster sizes only
+constexpr int64_t kSoftmaxSplitStagedMinRowBytes = 240 << 10;  // narrower: three-pass (sm_make_plan)
 
 struct SmCall {
     int dtype;
@@ -345,14 +346,28 @@ rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
     if (c.cols > (c.dtype == RMSNORM_DTYPE_BF16 ? kSoftmaxStagedMinColsBf16 : kSoftmaxStagedMinCols)) {
         st = sm_plan_staged(c, 1, P);
         if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
-        // fp32 rows too wide for one CTA's registers: split each over the
-        // smallest cluster whose slices fit (up to 8 CTAs).  Measured on
-        // prefill logits (rows of 128256): fp32 69% of the HBM roofline split
-        // against 50% for the three-pass kernel; bf16 59% split against 65%,
-        // so bf16 rows stay with the three-pass kernel.
-        for (int cl = 2; c.dtype == RMSNORM_DTYPE_F32 && cl <= kSoftmaxMaxStagedCluster; cl <<= 1) {
-            st = sm_plan_staged(c, cl, P);
-            if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+        // Rows too wide for one CTA's registers: split each over the smallest
+        // cluster whose slices fit (up to 8 CTAs), where that beats the
+        // three-pass kernel.  Measured on 1 GB inputs (% of the HBM roofline,
+        // split / three-pass): the three-pass kernel holds up while 304 rows
+        // fit L2 for its re-reads (rows of 128-200 KB: 70-80%) and falls to
+        // 48-55% on rows of 400 KB and more; the split runs at 54-84% for fp32
+        // rows (65536 elements 84 / 69, 100000 64 / 55, 128256 78 / 51,
+        // 262144 67 / 49; 48000 72 / 80), and for bf16 rows only when the
+        // slices fill the CTAs' registers (128256 elements, 98% full: 72 /
+        // 67; 262144, full: 60 / 51; 100000 and 200000, 76% full: 60 / 70
+        // and 49 / 54).
+        if (row_bytes >= kSoftmaxSplitStagedMinRowBytes) {
+            for (int cl = 2; cl <= kSoftmaxMaxStagedCluster; cl <<= 1) {
+                st = sm_plan_staged(c, cl, P);
+                if (st == RMSNORM_ERR_CUDA) return st;
+                if (st != RMSNORM_OK) continue;
+                const int64_t capacity = static_cast<int64_t>(softmax_staged_max_threads()) * 8 * 16;
+                if (c.dtype == RMSNORM_DTYPE_F32 ||
+                    16 * static_cast<int64_t>(P->slice_vecs) * 16 >= 15 * capacity)
+                    return RMSNORM_OK;
+                break;             // bf16 slices not full enough: three-pass
+            }
         }
     }
     st = sm_plan_rowreg(c, 1, P);

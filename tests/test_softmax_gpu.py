@@ -265,7 +265,12 @@ def test_guards_and_determinism(dtype):
     ((8192, 32000), "bf16", "softmax_staged"),
     ((16384, 16384), "bf16", "softmax_rowreg"),          # eight vectors per thread
     ((1024, 128256), "f32", "softmax_cluster_staged"),   # prefill logits, fp32
-    ((2048, 128256), "bf16", "softmax_threepass"),       # prefill logits, bf16
+    ((2048, 128256), "bf16", "softmax_cluster_staged"),  # prefill logits, bf16: slices 98% full
+    ((2048, 262144), "bf16", "softmax_cluster_staged"),  # full slices over 8 CTAs
+    ((5368, 100000), "bf16", "softmax_threepass"),       # slices 76% full
+    ((8192, 65536), "bf16", "softmax_threepass"),        # rows of 128 KB: L2 serves the re-reads
+    ((5592, 48000), "f32", "softmax_threepass"),         # rows of 188 KB
+    ((4096, 65536), "f32", "softmax_cluster_staged"),    # rows of 256 KB
     ((8, 128256), "f32", "softmax_cluster_rowreg"),      # decode logits
 ])
 def test_automatic_choice(shape, dtype, kernel):
