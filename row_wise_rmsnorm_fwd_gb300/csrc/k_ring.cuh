@@ -98,22 +98,32 @@ struct RingCursor {
 };
 
 // Issue the chunk at `c` (byte range [sbeg, sbeg + my_bytes) of row c.row,
-// chunk c.k) into its slot and advance `c`.  A chunk past the end of a short
-// slice completes its slot's phase with a plain arrive and no copy.  The
-// caller guarantees that the slot's previous chunk has been read by every
-// thread.  Returns false, issuing nothing, when the stream has no more rows.
+// chunk c.k; number `seq` of the CTA's stream) into its slot and advance `c`.
+// A chunk past the end of a short slice completes its slot's phase with a
+// plain arrive and no copy.  The caller guarantees that the slot's previous
+// chunk has been read by every thread.  Returns false, issuing nothing, when
+// the stream has no more rows.
 __device__ __forceinline__ bool ring_issue_next(const Params& p, const SlotRing& r, RingCursor& c,
                                                int64_t nunits, int64_t row_bytes, int64_t sbeg,
-                                               uint64_t policy) {
+                                               uint64_t policy, int64_t seq) {
     if (c.row >= p.rows) return false;
     const int len = r.chunk_len(c.k);
     const uint32_t fb = smem_addr(&r.full[c.slot]);
+#if RMSNORM_FAULT_INJECT
+    // Test build: the first copy is withheld, its barrier armed for bytes
+    // that never come, so every wait on that phase must run out.
+    const bool withhold = p.fault == kFaultStagedWithholdCopy && seq == 0;
+#else
+    const bool withhold = false;
+    (void)seq;
+#endif
     if (len > 0) {
         mbar_arrive_expect_tx(fb, static_cast<uint32_t>(len));
-        bulk_g2s(smem_addr(r.slots + static_cast<int64_t>(c.slot) * r.CB),
-                 static_cast<const char*>(p.x) + c.row * row_bytes + sbeg +
-                     static_cast<int64_t>(c.k) * r.CB,
-                 static_cast<uint32_t>(len), fb, policy);
+        if (!withhold)
+            bulk_g2s(smem_addr(r.slots + static_cast<int64_t>(c.slot) * r.CB),
+                     static_cast<const char*>(p.x) + c.row * row_bytes + sbeg +
+                         static_cast<int64_t>(c.k) * r.CB,
+                     static_cast<uint32_t>(len), fb, policy);
     } else {
         mbar_arrive(fb);
     }

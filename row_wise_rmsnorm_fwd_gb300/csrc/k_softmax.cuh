@@ -247,7 +247,11 @@ __device__ __forceinline__ bool cluster_pair_allreduce(PairExchange* ex, float m
     const uint32_t b = it & 1u;
     const uint32_t bar = smem_addr(&ex->bar[b]);
     if (lt == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ncta) * 8u);
-    if (lt < ncta) {
+    bool send = lt < ncta;
+#if RMSNORM_FAULT_INJECT
+    if (p.fault == kFaultClusterWithholdPartial && rank == 0 && it == 0) send = false;
+#endif
+    if (send) {
         const uint32_t peer = static_cast<uint32_t>(lt);
         st_async_v2_f32(map_to_rank(smem_addr(&ex->slot[b][rank]), peer), m, s,
                         map_to_rank(bar, peer));
@@ -461,7 +465,7 @@ __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kerne
     if (tid == 0) {
         for (int k = 0; k < S; ++k) mbar_init(smem_addr(&full[k]), 1);
         fence_mbarrier_init_cluster();
-        while (issued < S && ring_issue_next(p, ring, cur, nunits, row_bytes, sbeg, policy))
+        while (issued < S && ring_issue_next(p, ring, cur, nunits, row_bytes, sbeg, policy, issued))
             ++issued;
     }
     if (CL) {
@@ -530,7 +534,7 @@ __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kerne
         // every thread holds its part of the row: refill the row's slots
         if (tid == 0)
             while (issued < base + NCH + S &&
-                   ring_issue_next(p, ring, cur, nunits, row_bytes, sbeg, policy))
+                   ring_issue_next(p, ring, cur, nunits, row_bytes, sbeg, policy, issued))
                 ++issued;
         slot0 += NCH;              // NCH <= S: one wrap at most
         if (slot0 >= S) {

@@ -73,8 +73,16 @@ rmsnorm_status_t sm_validate(int32_t dtype, const void* x, const void* y, int64_
     if (opt) {
         c->opt = *opt;
         const rmsnorm_options_t& o = *opt;
-        if (o.weights || o.fault_inject || o.reserved || o.epilogue)
+        if (o.weights || o.reserved || o.epilogue || o.fault_inject < 0 || o.fault_inject > 2)
             return RMSNORM_ERR_INVALID_ARG;
+        // fault injection: test build only, and only where its site exists
+        // (1: the staged ring's first copy; 2: a split row's first pair)
+        if (o.fault_inject != 0 &&
+            (!RMSNORM_FAULT_INJECT ||
+             (o.fault_inject == 1 && o.path != RMSNORM_PATH_STAGED) ||
+             (o.fault_inject == 2 && o.path != RMSNORM_PATH_CLUSTER &&
+              !(o.path == RMSNORM_PATH_STAGED && o.cluster > 1))))
+            return RMSNORM_ERR_UNSUPPORTED;
         if (o.path != RMSNORM_PATH_AUTO && o.path != RMSNORM_PATH_ROWREG &&
             o.path != RMSNORM_PATH_TWOPASS && o.path != RMSNORM_PATH_CLUSTER &&
             o.path != RMSNORM_PATH_STAGED)
@@ -400,6 +408,7 @@ rmsnorm_status_t sm_run(int32_t dtype, const void* x, void* y, int64_t rows, int
     p.nchunks = P.nchunks;
     p.nslots = P.nslots;
     p.status = c.dv.status;
+    p.fault = c.opt.fault_inject;
     p.timeout_ns = c.opt.wait_timeout_ns ? c.opt.wait_timeout_ns : kDefaultTimeoutNs;
     LaunchShape s{P.grid, P.block, P.cluster, P.smem};
     if (ensure_prepared(c.dv.dev, P.fn, c.dv.smem_optin) != cudaSuccess) return RMSNORM_ERR_CUDA;

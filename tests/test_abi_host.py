@@ -110,10 +110,27 @@ def test_softmax_rejects_bad_arguments_before_launch(lib, fn):
 
 def test_softmax_ex_rejects_rmsnorm_only_options(lib):
     for field, value in (("cluster", 2), ("chunk_bytes", 4096), ("stages", 3), ("weights", 1),
-                         ("epilogue", 1), ("fault_inject", 1), ("path", 5), ("path", 6)):
+                         ("epilogue", 1), ("path", 5), ("path", 6)):
         o = binding.make_options()
         setattr(o, field, value)
         assert binding.raw.rowsoftmax_fwd_ex(0, A, B, 4, 8, o) == INVALID, field
+
+
+def test_softmax_fault_injection_is_test_build_only(lib):
+    """The product library refuses fault injection at every site (1: the
+    staged ring's first copy, 2: a split row's first pair) and where no site
+    exists; values outside 0..2 are invalid.  No CUDA call is made."""
+    unsupported = binding.RMSNORM_ERR_UNSUPPORTED
+    for opts in (dict(path="staged", fault_inject=1), dict(path="staged", cluster=2, fault_inject=1),
+                 dict(path="staged", cluster=2, fault_inject=2),
+                 dict(path="cluster", cluster=2, fault_inject=2),
+                 dict(fault_inject=1), dict(path="rowreg", fault_inject=2),
+                 dict(path="twopass", fault_inject=1)):
+        o = binding.make_options(**opts)
+        assert binding.raw.rowsoftmax_fwd_ex(0, A, B, 4, 8, o) == unsupported, opts
+    for v in (-1, 3):
+        o = binding.make_options(path="staged", fault_inject=v)
+        assert binding.raw.rowsoftmax_fwd_ex(0, A, B, 4, 8, o) == INVALID, v
 
 
 def test_softmax_ex_staged_shape_options_are_checked(lib):

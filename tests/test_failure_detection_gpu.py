@@ -2,9 +2,10 @@
 
 Every device-side wait of the library is bounded.  The test build of the
 library (compiled with RMSNORM_FAULT_INJECT, loaded here from
-librmsnorm_faultinject.so) can be told to withhold one bulk copy of the staged
+librmsnorm_faultinject.so) can be told to withhold one bulk copy of a staged
 kernel (its mbarrier is armed for bytes that never arrive) or one CTA's
-partial sum in a split-row cluster (its peers' barrier never completes).  The
+partial sum -- or (maximum, sum) pair, for the row softmax -- in a split-row
+cluster (its peers' barrier never completes).  The
 waits then run out after a short limit, the kernel records
 RMSNORM_ERR_TIMEOUT in the device status word, leaves cleanly, and the CUDA
 context stays usable: a following clean call must be exact and report OK.
@@ -16,7 +17,8 @@ import time
 import pytest
 import torch
 
-from _parity import compare, oracle_for
+import oracle
+from _parity import check_bf16, check_f32, compare, oracle_for
 from row_wise_rmsnorm_fwd_gb300 import binding, build, workloads
 
 pytestmark = pytest.mark.gpu
@@ -90,5 +92,55 @@ def test_bounded_wait_expires_and_context_survives(flib, what, opts, shape, dtyp
     compare(y, oracle_for(x.cpu(), w.cpu(), 1e-6), f"{what}: clean call after timeout")
     # and so does the product library
     y2 = binding.rmsnorm_fwd_ex(x, w, eps=1e-6, options=clean)
+    torch.cuda.synchronize()
+    assert torch.equal(y2, y)
+
+
+def sm_call(lib, x, y, **opts):
+    o = binding.make_options(**opts)
+    dt = binding.RMSNORM_DTYPE_F32 if x.dtype == torch.float32 else binding.RMSNORM_DTYPE_BF16
+    rows, cols = x.shape
+    return lib.rowsoftmax_fwd_ex(dt, x.data_ptr(), y.data_ptr(), rows, cols, ctypes.byref(o),
+                                 torch.cuda.current_stream().cuda_stream)
+
+
+def sm_compare(y, x, what):
+    x, y = x.cpu(), y.cpu()
+    if x.dtype == torch.float32:
+        check_f32(y.numpy(), oracle.rowsoftmax_f32(x.numpy()), what)
+    else:
+        _, ref16 = oracle.rowsoftmax_bf16(workloads.bf16_bits(x))
+        check_bf16(workloads.bf16_bits(y), ref16, what)
+
+
+SOFTMAX_CASES = [
+    ("softmax staged withholds a copy", dict(path="staged", fault_inject=1), (64, 32000)),
+    ("softmax staged cluster withholds a copy", dict(path="staged", cluster=4, fault_inject=1),
+     (16, 128256)),
+    ("softmax cluster withholds a pair", dict(path="cluster", cluster=4, fault_inject=2),
+     (8, 65536)),
+    ("softmax staged cluster withholds a pair", dict(path="staged", cluster=4, fault_inject=2),
+     (16, 128256)),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("what,opts,shape", SOFTMAX_CASES, ids=[c[0] for c in SOFTMAX_CASES])
+def test_softmax_bounded_wait_expires_and_context_survives(flib, what, opts, shape, dtype):
+    x = workloads.make_random(shape, dtype, 7, ("normal", 0.0, 3.0)).cuda()
+    y = torch.empty_like(x)
+    assert status(flib) == binding.RMSNORM_OK
+    t0 = time.monotonic()
+    assert sm_call(flib, x, y, wait_timeout_ns=LIMIT_NS, **opts) == binding.RMSNORM_OK
+    st = status(flib)
+    elapsed = time.monotonic() - t0
+    assert st == binding.RMSNORM_ERR_TIMEOUT, f"{what}: status {st}"
+    assert elapsed < 30.0, f"{what}: took {elapsed:.1f} s"
+    assert status(flib) == binding.RMSNORM_OK
+    clean = {k: v for k, v in opts.items() if k != "fault_inject"}
+    assert sm_call(flib, x, y, wait_timeout_ns=LIMIT_NS, **clean) == binding.RMSNORM_OK
+    assert status(flib) == binding.RMSNORM_OK
+    sm_compare(y, x, f"{what}: clean call after timeout")
+    y2 = binding.rowsoftmax_fwd_ex(x, options=clean)
     torch.cuda.synchronize()
     assert torch.equal(y2, y)
