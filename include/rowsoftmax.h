@@ -54,8 +54,15 @@ rmsnorm_status_t rowsoftmax_fwd_bf16(const uint16_t* x, uint16_t* y, int64_t row
  * RMSNORM_PATH_TWOPASS (the wide-row kernel:
  * reads each row three times, the repeats normally from L2); opt->threads,
  * opt->grid, opt->vec_bytes and opt->wait_timeout_ns as for rmsnorm_fwd_ex.
- * chunk_bytes and stages with any other path, and the other option fields,
- * must be zero (else RMSNORM_ERR_INVALID_ARG).  `opt` may be NULL.
+ * opt->fault_inject (failure-detection tests, test build of the library
+ * only): 1 = STAGED withholds each CTA's first bulk copy, 2 = a split row
+ * (CLUSTER, or STAGED with cluster > 1) has CTA rank 0 withhold its first
+ * (maximum, sum) pair; the bounded waits then expire (see
+ * rmsnorm_last_device_status).  The product library, and any path without
+ * that site, return RMSNORM_ERR_UNSUPPORTED; values outside 0..2 are
+ * RMSNORM_ERR_INVALID_ARG.  chunk_bytes and stages with any other path, and
+ * the other option fields, must be zero (else RMSNORM_ERR_INVALID_ARG).
+ * `opt` may be NULL.
  */
 rmsnorm_status_t rowsoftmax_fwd_ex(int32_t dtype, const void* x, void* y, int64_t rows,
                                    int64_t cols, const rmsnorm_options_t* opt,
