@@ -21,9 +21,11 @@
 //
 // softmax_staged_kernel brings rows in through the bulk-copy slot ring
 // (k_ring.cuh) and holds each in registers, so that the next rows are already
-// in flight while a row's reductions run; softmax_threepass_kernel serves
-// rows too wide for registers: one CTA per row reads x three times (max, sum,
-// write), the second and third reads normally served by L2.
+// in flight while a row's reductions run; rows too wide for one CTA's
+// registers are split over a thread-block cluster of such CTAs.
+// softmax_threepass_kernel serves the wide rows where that split loses: one
+// CTA per row reads x three times (max, sum, write), the second and third
+// reads normally served by L2.
 #pragma once
 #include <type_traits>
 
@@ -150,12 +152,19 @@ struct RowPairs {
     using Sums = PairSums;
     uint64_t e[kPairs];
 
-    __device__ __forceinline__ void load(const Vec<VB>& v, float (&)[4], uint32_t (&mw)[2]) {
+    static __device__ __forceinline__ void fold_max(const Vec<VB>& v, float (&)[4],
+                                                    uint32_t (&mw)[2]) {
 #pragma unroll
-        for (int j = 0; j < kPairs; ++j) {
-            mw[j & 1] = max_bf16x2(mw[j & 1], v.u[j]);
+        for (int j = 0; j < kPairs; ++j) mw[j & 1] = max_bf16x2(mw[j & 1], v.u[j]);
+    }
+    __device__ __forceinline__ void widen(const Vec<VB>& v) {
+#pragma unroll
+        for (int j = 0; j < kPairs; ++j)
             e[j] = pack_x2(get<T, VB>(v, 2 * j), get<T, VB>(v, 2 * j + 1));
-        }
+    }
+    __device__ __forceinline__ void load(const Vec<VB>& v, float (&mk)[4], uint32_t (&mw)[2]) {
+        fold_max(v, mk, mw);
+        widen(v);
     }
     // e = 2^(e*log2e + c) in place; the sums take the exponentials.
     __device__ __forceinline__ void exp(float c, Sums& s) {
@@ -176,6 +185,19 @@ struct RowPairs {
         for (int j = 0; j < kPairs; ++j) unpack_x2(mul_x2(e[j], inv2), o[2 * j], o[2 * j + 1]);
         return pack<T, VB>(o);
     }
+    // The outputs 2^(e*log2e + c) * inv of widened inputs, packed for the store.
+    __device__ __forceinline__ Vec<VB> exp_scaled(float c, float inv) const {
+        const uint64_t l2 = pack_x2(kLog2e, kLog2e), c2 = pack_x2(c, c), inv2 = pack_x2(inv, inv);
+        float o[kElems];
+#pragma unroll
+        for (int j = 0; j < kPairs; ++j) {
+            float a0, a1;
+            unpack_x2(fma_x2(e[j], l2, c2), a0, a1);
+            unpack_x2(mul_x2(pack_x2(row_exp_arg<T>(a0), row_exp_arg<T>(a1)), inv2), o[2 * j],
+                      o[2 * j + 1]);
+        }
+        return pack<T, VB>(o);
+    }
 };
 
 // The same passes in scalar fp32 arithmetic (fp32 rows, and bf16 vectors of
@@ -186,6 +208,15 @@ struct RowScalars {
     using Sums = ScalarSums;
     float e[kElems];
 
+    static __device__ __forceinline__ void fold_max(const Vec<VB>& v, float (&mk)[4],
+                                                    uint32_t (&)[2]) {
+#pragma unroll
+        for (int k = 0; k < kElems; ++k) mk[k & 3] = fmaxf(mk[k & 3], get<T, VB>(v, k));
+    }
+    __device__ __forceinline__ void widen(const Vec<VB>& v) {
+#pragma unroll
+        for (int k = 0; k < kElems; ++k) e[k] = get<T, VB>(v, k);
+    }
     __device__ __forceinline__ void load(const Vec<VB>& v, float (&mk)[4], uint32_t (&)[2]) {
 #pragma unroll
         for (int k = 0; k < kElems; ++k) {
@@ -204,6 +235,12 @@ struct RowScalars {
         float o[kElems];
 #pragma unroll
         for (int k = 0; k < kElems; ++k) o[k] = e[k] * inv;
+        return pack<T, VB>(o);
+    }
+    __device__ __forceinline__ Vec<VB> exp_scaled(float c, float inv) const {
+        float o[kElems];
+#pragma unroll
+        for (int k = 0; k < kElems; ++k) o[k] = row_exp<T>(e[k], c) * inv;
         return pack<T, VB>(o);
     }
 };
@@ -580,7 +617,13 @@ constexpr int kSoftmaxWideThreads = 1024;
 
 template <typename T, int VB>
 __global__ void __launch_bounds__(kSoftmaxWideThreads) softmax_threepass_kernel(const Params p) {
+    // bf16 vectors of two or more elements: the packed-pair passes; fp32 (and
+    // one-element) vectors: scalar code with one maximum chain and two sums,
+    // which keeps the kernel at 32 registers and two 1024-thread CTAs per SM
+    // (four chains took the fp32 instance to 44 registers, one CTA per SM).
+    constexpr bool kPairs = sizeof(T) == 2 && VecTraits<T, VB>::kElems >= 2;
     constexpr int EPV = VecTraits<T, VB>::kElems;
+    using RV = RowVec<T, VB>;
     __shared__ float red[2][2][32];
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
@@ -595,10 +638,18 @@ __global__ void __launch_bounds__(kSoftmaxWideThreads) softmax_threepass_kernel(
         const int b = it & 1;
         const char* src = xb + row * row_bytes;
         float m = -INFINITY;
-        for (int v = tid; v < p.nvec; v += nthr) {
-            const Vec<VB> xv = ld_plain<VB>(src + static_cast<int64_t>(v) * VB);
+        if constexpr (kPairs) {
+            float mk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            uint32_t mw[2] = {kBf16x2NegInf, kBf16x2NegInf};
+            for (int v = tid; v < p.nvec; v += nthr)
+                RV::fold_max(ld_plain<VB>(src + static_cast<int64_t>(v) * VB), mk, mw);
+            m = running_max(mk, mw);
+        } else {
+            for (int v = tid; v < p.nvec; v += nthr) {
+                const Vec<VB> xv = ld_plain<VB>(src + static_cast<int64_t>(v) * VB);
 #pragma unroll
-            for (int k = 0; k < EPV; ++k) m = fmaxf(m, get<T, VB>(xv, k));
+                for (int k = 0; k < EPV; ++k) m = fmaxf(m, get<T, VB>(xv, k));
+            }
         }
         m = warp_allreduce_max(m);
         if (lane == 0) red[0][b][warp] = m;
@@ -607,16 +658,28 @@ __global__ void __launch_bounds__(kSoftmaxWideThreads) softmax_threepass_kernel(
         for (int k = 0; k < nwarps; ++k) m = fmaxf(m, red[0][b][k]);
         const float c = row_exp_bias<T>() - m * kLog2e;
 
-        float s0 = 0.f, s1 = 0.f;
-        for (int v = tid; v < p.nvec; v += nthr) {
-            const Vec<VB> xv = ld_plain<VB>(src + static_cast<int64_t>(v) * VB);
-#pragma unroll
-            for (int k = 0; k < EPV; ++k) {
-                const float ev = row_exp<T>(get<T, VB>(xv, k), c);
-                if (k & 1) s1 += ev; else s0 += ev;
+        float sl;
+        if constexpr (kPairs) {
+            PairSums sums;
+            for (int v = tid; v < p.nvec; v += nthr) {
+                RV e;
+                e.widen(ld_plain<VB>(src + static_cast<int64_t>(v) * VB));
+                e.exp(c, sums);
             }
+            sl = sums.total();
+        } else {
+            float s0 = 0.f, s1 = 0.f;
+            for (int v = tid; v < p.nvec; v += nthr) {
+                const Vec<VB> xv = ld_plain<VB>(src + static_cast<int64_t>(v) * VB);
+#pragma unroll
+                for (int k = 0; k < EPV; ++k) {
+                    const float ev = row_exp<T>(get<T, VB>(xv, k), c);
+                    if (k & 1) s1 += ev; else s0 += ev;
+                }
+            }
+            sl = s0 + s1;
         }
-        float s = warp_allreduce_sum(s0 + s1);
+        float s = warp_allreduce_sum(sl);
         if (lane == 0) red[1][b][warp] = s;
         __syncthreads();
         s = 0.f;
@@ -626,11 +689,9 @@ __global__ void __launch_bounds__(kSoftmaxWideThreads) softmax_threepass_kernel(
         char* dst = yb + row * row_bytes;
         for (int v = tid; v < p.nvec; v += nthr) {
             const int64_t off = static_cast<int64_t>(v) * VB;
-            const Vec<VB> xv = ld_stream<VB>(src + off);
-            float o[EPV];
-#pragma unroll
-            for (int k = 0; k < EPV; ++k) o[k] = row_exp<T>(get<T, VB>(xv, k), c) * inv;
-            st_stream<VB>(dst + off, pack<T, VB>(o));
+            RV e;
+            e.widen(ld_stream<VB>(src + off));
+            st_stream<VB>(dst + off, e.exp_scaled(c, inv));
         }
     }
 }

@@ -196,6 +196,7 @@ rmsnorm_status_t sm_plan_rowreg(const SmCall& c, int cluster, SmPlan* P) {
                                                  : (c.rows < occ ? c.rows : occ);
         grid = static_cast<int>(nclusters * cluster);
     }
+    *P = SmPlan{};             // every field this plan does not set keeps its default
     P->path = cluster == 1 ? RMSNORM_PATH_ROWREG : RMSNORM_PATH_CLUSTER;
     P->cluster = cluster;
     P->slice_vecs = static_cast<int>(per);
@@ -226,6 +227,7 @@ rmsnorm_status_t sm_plan_threepass(const SmCall& c, SmPlan* P) {
         return RMSNORM_ERR_CUDA;
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
     const int64_t resident = static_cast<int64_t>(c.dv.sms) * occ;
+    *P = SmPlan{};             // every field this plan does not set keeps its default
     P->path = RMSNORM_PATH_TWOPASS;
     P->group = block;
     P->block = block;
@@ -302,6 +304,7 @@ rmsnorm_status_t sm_plan_staged(const SmCall& c, int cluster, SmPlan* P) {
                                                  : (c.rows < occ ? c.rows : occ);
         grid = static_cast<int>(nclusters * cluster);
     }
+    *P = SmPlan{};             // every field this plan does not set keeps its default
     P->path = RMSNORM_PATH_STAGED;
     P->cluster = cluster;
     P->slice_vecs = static_cast<int>(per);
@@ -367,13 +370,16 @@ rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
         // and 49 / 54).
         if (row_bytes >= kSoftmaxSplitStagedMinRowBytes) {
             for (int cl = 2; cl <= kSoftmaxMaxStagedCluster; cl <<= 1) {
-                st = sm_plan_staged(c, cl, P);
+                SmPlan Q;          // P stays untouched unless the split is taken
+                st = sm_plan_staged(c, cl, &Q);
                 if (st == RMSNORM_ERR_CUDA) return st;
                 if (st != RMSNORM_OK) continue;
                 const int64_t capacity = static_cast<int64_t>(softmax_staged_max_threads()) * 8 * 16;
                 if (c.dtype == RMSNORM_DTYPE_F32 ||
-                    16 * static_cast<int64_t>(P->slice_vecs) * 16 >= 15 * capacity)
+                    16 * static_cast<int64_t>(Q.slice_vecs) * 16 >= 15 * capacity) {
+                    *P = Q;
                     return RMSNORM_OK;
+                }
                 break;             // bf16 slices not full enough: three-pass
             }
         }
