@@ -468,6 +468,9 @@ rmsnorm_status_t rowsoftmax_plan(int32_t dtype, const void* x, const void* y, in
     plan->grid = P.grid;
     plan->vec_bytes = P.vb;
     plan->vecs_per_thread = P.nv;
+    plan->smem_bytes = P.smem;
+    plan->chunk_bytes = P.chunk;
+    plan->stages = P.nslots;
     std::snprintf(plan->kernel, sizeof(plan->kernel), "%s", P.name);
     return RMSNORM_OK;
 }

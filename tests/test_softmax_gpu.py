@@ -280,6 +280,19 @@ def test_automatic_choice(shape, dtype, kernel):
     assert p["kernel"] == kernel, p
 
 
+def test_rejected_split_leaves_no_trace_in_the_plan():
+    """bf16 rows whose cluster split is planned and then rejected (slices too
+    empty) launch the three-pass kernel as a plain launch: no cluster and no
+    shared-memory reservation left over from the split."""
+    x = torch.empty((3533, 151936), dtype=torch.bfloat16, device="cuda")
+    p = binding.rowsoftmax_plan(x, torch.empty_like(x))
+    assert p["kernel"] == "softmax_threepass", p
+    assert p["cluster"] == 1 and p["smem_bytes"] == 0 and p["stages"] == 0, p
+    # the split itself, forced, reports its ring
+    q = binding.rowsoftmax_plan(x, torch.empty_like(x), options={"path": "staged", "cluster": 8})
+    assert q["cluster"] == 8 and q["smem_bytes"] > 0 and q["stages"] >= 1, q
+
+
 def test_rows_sum_to_one_and_match_torch():
     x = case(1000, 512, "f32", 5).cuda()
     y = run(x)
