@@ -366,7 +366,7 @@ def run_ours(args, wl):
         staged = args.path == "staged"
         options = binding.make_options(
             path=args.path if args.path in ("rowreg", "twopass", "cluster", "staged") else "auto",
-            cluster=args.cluster if args.path in ("cluster", "staged") else 0,
+            cluster=args.cluster if args.path in ("cluster", "staged", "twopass") else 0,
             grid=args.grid, threads=args.threads,
             chunk_bytes=args.chunk if staged else 0, stages=args.stages if staged else 0)
         dt_code = binding.RMSNORM_DTYPE_BF16 if wl.dtype == "bf16" else binding.RMSNORM_DTYPE_F32

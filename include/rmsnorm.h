@@ -67,7 +67,13 @@ typedef enum {
                                   (cp.async.bulk + mbarrier), multi-stage prefetch    */
     RMSNORM_PATH_CLUSTER = 3,  /* split row: a thread-block cluster per row, slices in
                                   registers, partial sums exchanged through DSMEM     */
-    RMSNORM_PATH_TWOPASS = 4,  /* generic fallback: read x twice (any width/alignment) */
+    RMSNORM_PATH_TWOPASS = 4,  /* generic fallback: read x twice (any width/alignment);
+                                  opt->cluster = 2..16 (any size) splits each row over
+                                  a thread-block cluster (partial sums through DSMEM),
+                                  which the automatic choice does for few rows too
+                                  wide for every other family.  Unsplit (cluster 0
+                                  or 1): rows of at most 2^31 - 1025 vectors, else
+                                  RMSNORM_ERR_UNSUPPORTED */
     RMSNORM_PATH_PAGE = 5,     /* comparison only, never automatic: the compiler write-up's
                                   schedule (one 256-thread CTA per row, whole row staged
                                   in shared memory, 4-byte accesses, 3-level tree); rows
@@ -84,7 +90,8 @@ typedef enum {
  * need; every zero field means "automatic". */
 typedef struct {
     int32_t path;            /* rmsnorm_path_t */
-    int32_t cluster;         /* CTAs per row for CLUSTER (2..16) or STAGED (1..16) */
+    int32_t cluster;         /* CTAs per row for CLUSTER (2, 4, 8, 16), STAGED (1..16)
+                                or TWOPASS (1..16) */
     int32_t threads;         /* threads per row group (multiple of 32, <= 1024, or
                                 1, 2, 4, 8, 16 for ROWREG: several rows per warp);
                                 STAGED: consumer threads, 128 or 256 */

@@ -52,11 +52,16 @@ rmsnorm_status_t rowsoftmax_fwd_bf16(const uint16_t* x, uint16_t* y, int64_t row
  * to 512; opt->cluster = 2..16 splits each row over a thread-block cluster,
  * maximum and sum combined through distributed shared memory) or
  * RMSNORM_PATH_TWOPASS (the wide-row kernel:
- * reads each row three times, the repeats normally from L2); opt->threads,
+ * reads each row three times, the repeats normally from L2; opt->cluster =
+ * 2..16 (any size; the other paths take powers of two) splits each row over
+ * a thread-block cluster with one (maximum, sum) exchange per row, which the
+ * automatic choice does for few rows too wide for every other kernel;
+ * unsplit, rows of at most 2^31 - 1025 vectors, else
+ * RMSNORM_ERR_UNSUPPORTED); opt->threads,
  * opt->grid, opt->vec_bytes and opt->wait_timeout_ns as for rmsnorm_fwd_ex.
  * opt->fault_inject (failure-detection tests, test build of the library
  * only): 1 = STAGED withholds each CTA's first bulk copy, 2 = a split row
- * (CLUSTER, or STAGED with cluster > 1) has CTA rank 0 withhold its first
+ * (CLUSTER, or STAGED or TWOPASS with cluster > 1) has CTA rank 0 withhold its first
  * (maximum, sum) pair; the bounded waits then expire (see
  * rmsnorm_last_device_status).  The product library, and any path without
  * that site, return RMSNORM_ERR_UNSUPPORTED; values outside 0..2 are

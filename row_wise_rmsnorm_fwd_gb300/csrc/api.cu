@@ -42,6 +42,7 @@ constexpr int64_t kSplitMinBytes = 16 << 20;    // auto: split narrow few-row in
 constexpr int kRingregSlots = 3;                 // ring-to-register kernel: ring slots
 constexpr int64_t kRingregLowMaxRowBytes = 57344;    // auto: ringreg for rows above 32 KB to here
 constexpr int64_t kRingregHighMinRowBytes = 114688;  // auto: and above this (to 128 KB)
+constexpr int64_t kUnsplitMaxVecs = 0x7FFFFFFFll - 1024;  // two-pass, one CTA per row: up to here
 
 struct Call {
     int dtype;
@@ -71,6 +72,7 @@ struct Plan {
     int w_staged = 0;
     int nvec = 0;
     int slice_vecs = 0;
+    int resident = 0;       // resident CTAs per SM, or resident clusters (split rows)
     KernelFn fn = nullptr;
     const char* name = "";
 };
@@ -375,34 +377,51 @@ rmsnorm_status_t plan_ringreg(const Call& c, Plan* P) {
 }
 
 // Generic fallback: any width and alignment.
-rmsnorm_status_t plan_twopass(const Call& c, Plan* P) {
+// Two-pass kernel; cluster > 1 splits each row over a thread-block cluster
+// (slices of whole 32-vector groups, CTA totals combined through DSMEM).
+rmsnorm_status_t plan_twopass(const Call& c, int cluster, Plan* P) {
     int vb;
     rmsnorm_status_t st = pick_vb(c, &vb);
     if (st != RMSNORM_OK) return st;
-    KernelFn fn = twopass_kernel_ptr(c.dtype, vb, c.opt.epilogue);
+    KernelFn fn = cluster > 1 ? twopass_cluster_kernel_ptr(c.dtype, vb, c.opt.epilogue)
+                              : twopass_kernel_ptr(c.dtype, vb, c.opt.epilogue);
     if (!fn) return RMSNORM_ERR_UNSUPPORTED;
     const int64_t nvec = c.hidden / (vb / c.sz);
-    int block = c.opt.threads > 0 ? c.opt.threads
-                                  : (nvec >= twopass_block() ? twopass_block()
-                                                             : round_up(nvec, 32));
-    if (block % 32 != 0 || block > twopass_block()) return RMSNORM_ERR_INVALID_ARG;
+    const int maxb = cluster > 1 ? split_block() : twopass_block();
+    // The unsplit kernel's 32-bit vector index must not pass 2^31 - 1 one
+    // stride after the row's last vector: rows of 2^31 - 1024 vectors or
+    // more (widths near 2^31 elements with one-element vectors) are split.
+    if (cluster == 1 && nvec > kUnsplitMaxVecs) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t slice = cluster > 1 ? round_up(ceil_div(nvec, cluster), 32) : nvec;
+    int block = c.opt.threads > 0 ? c.opt.threads : (slice >= maxb ? maxb : round_up(slice, 32));
+    if (block % 32 != 0 || block > maxb) return RMSNORM_ERR_INVALID_ARG;
     int occ = 0;
-    if (cached_occupancy(c.dev, c.info->smem_optin, fn, block, 0, 1, &occ) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (cached_occupancy(c.dev, c.info->smem_optin, fn, block, 0, cluster, &occ) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
-    const int64_t resident = static_cast<int64_t>(c.info->sms) * occ;
+    int grid;
+    if (cluster == 1) {
+        const int64_t resident = static_cast<int64_t>(c.info->sms) * occ;
+        grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
+                                               : (c.rows < resident ? c.rows : resident));
+    } else {
+        const int64_t nclusters = c.opt.grid > 0 ? (c.opt.grid + cluster - 1) / cluster
+                                                 : (c.rows < occ ? c.rows : occ);
+        grid = static_cast<int>(nclusters * cluster);
+    }
+    P->resident = occ;
     P->path = RMSNORM_PATH_TWOPASS;
-    P->cluster = 1;
+    P->cluster = cluster;
     P->group = block;
     P->block = block;
     P->rpc = 1;
-    P->grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
-                                              : (c.rows < resident ? c.rows : resident));
+    P->grid = grid;
     P->vb = vb;
     P->nv = 0;
     P->nvec = static_cast<int>(nvec);
-    P->slice_vecs = static_cast<int>(nvec);
+    P->slice_vecs = static_cast<int>(slice);
     P->fn = fn;
-    P->name = "twopass";
+    P->name = cluster == 1 ? "twopass" : "twopass_cluster";
     return RMSNORM_OK;
 }
 
@@ -446,6 +465,33 @@ rmsnorm_status_t plan_page(const Call& c, Plan* P) {
 //  - wider rows (and bf16 rows above 32 KB): two-pass, the second read served
 //    by L2 (81-95%).
 // Each choice falls through to the next family if it cannot serve the call.
+// The two-pass kernel with each row over a cluster of C CTAs (one CTA per
+// row would leave the row's whole traffic to a single SM).  C (2..16, any
+// size) minimises the row time waves(C) / C, waves(C) = rows / resident
+// clusters of C, rounded up: resident clusters are limited by the SMs of a
+// GPC, so for eight rows of 16-byte vectors (one 1024-thread CTA per SM) 16
+// CTAs per row take two waves where 12 take one (measured on eight fp32 rows
+// of 64 MiB: 409 us with 16, 303 us with 12, 355 us with 8).  Ties go to the
+// smaller cluster.
+rmsnorm_status_t plan_twopass_split(const Call& c, Plan* P) {
+    Plan best;
+    int64_t best_waves = 0;
+    for (int cl = 2; cl <= 16; ++cl) {
+        Plan Q;
+        const rmsnorm_status_t st = plan_twopass(c, cl, &Q);
+        if (st == RMSNORM_ERR_CUDA) return st;
+        if (st != RMSNORM_OK) continue;
+        const int64_t waves = (c.rows + Q.resident - 1) / Q.resident;
+        if (best_waves == 0 || waves * best.cluster < best_waves * cl) {
+            best = Q;
+            best_waves = waves;
+        }
+    }
+    if (best_waves == 0) return RMSNORM_ERR_UNSUPPORTED;
+    *P = best;
+    return RMSNORM_OK;
+}
+
 rmsnorm_status_t plan_auto(const Call& c, Plan* P) {
     const int64_t row_bytes = c.hidden * c.sz;
     rmsnorm_status_t st;
@@ -467,7 +513,10 @@ rmsnorm_status_t plan_auto(const Call& c, Plan* P) {
             st = plan_staged(c, cl, P);
             if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
         }
-        return plan_twopass(c, P);
+        // Rows too wide for any cluster's registers or shared memory.
+        st = plan_twopass_split(c, P);
+        if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+        return plan_twopass(c, 1, P);
     }
     if (row_bytes <= kRowregMaxRowBytes) {
         st = plan_rowreg(c, 1, P);
@@ -491,7 +540,9 @@ rmsnorm_status_t plan_auto(const Call& c, Plan* P) {
         st = plan_staged(c, 1, P);
         if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
     }
-    return plan_twopass(c, P);
+    st = plan_twopass(c, 1, P);
+    if (st != RMSNORM_ERR_UNSUPPORTED) return st;
+    return plan_twopass_split(c, P);   // rows too wide for one CTA's 32-bit index
 }
 
 rmsnorm_status_t make_plan(const Call& c, Plan* P) {
@@ -517,8 +568,7 @@ rmsnorm_status_t make_plan(const Call& c, Plan* P) {
         case RMSNORM_PATH_STAGED:
             return plan_staged(c, cl == 0 ? 1 : cl, P);
         case RMSNORM_PATH_TWOPASS:
-            if (cl > 1) return RMSNORM_ERR_INVALID_ARG;
-            return plan_twopass(c, P);
+            return plan_twopass(c, cl == 0 ? 1 : cl, P);
         case RMSNORM_PATH_PAGE:
             return plan_page(c, P);
         case RMSNORM_PATH_RINGREG:
@@ -700,7 +750,7 @@ int32_t rmsnorm_last_cuda_error(char* msg, size_t len) {
     return static_cast<int32_t>(e);
 }
 
-int32_t rmsnorm_abi_version(void) { return 10100; }
+int32_t rmsnorm_abi_version(void) { return 10200; }
 
 // Present in every build; non-zero only in the failure-injection test build.
 int32_t rmsnorm_fault_injection_enabled(void) { return RMSNORM_FAULT_INJECT; }

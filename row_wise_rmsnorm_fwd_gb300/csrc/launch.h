@@ -35,6 +35,13 @@ KernelFn softmax_rowreg_ptr(int dtype, int vb, int nv, bool cluster);
 int softmax_rowreg_max_block(int nv);
 KernelFn softmax_threepass_ptr(int dtype, int vb);
 int softmax_threepass_block();
+// Few rows too wide for every other kernel: the two-pass (RMSNorm) and
+// three-pass (softmax) kernels with each row split over a thread-block
+// cluster of 2..16 CTAs (slices of Params.slice_vecs vectors, totals combined
+// through DSMEM); up to split_block() threads per CTA.
+KernelFn twopass_cluster_kernel_ptr(int dtype, int vb, int epi);
+KernelFn softmax_threepass_cluster_ptr(int dtype, int vb);
+int split_block();
 // Row softmax staged in shared memory and held in registers: up to 512
 // threads of nv 16-byte vectors each (fp32: 4, 8 or 16; bf16: 2, 4 or 8);
 // cluster = rows split over a thread-block cluster; dynamic shared memory =

@@ -20,6 +20,7 @@ constexpr int64_t kSoftmaxStagedMinCols = 8192;         // wider fp32 rows go to
 constexpr int64_t kSoftmaxStagedMinColsBf16 = 16384;    // wider bf16 rows go to the staged kernel
 constexpr int kSoftmaxMaxStagedCluster = 8;             // portable cluster sizes only
 constexpr int64_t kSoftmaxSplitStagedMinRowBytes = 240 << 10;  // narrower: three-pass (sm_make_plan)
+constexpr int64_t kSoftmaxUnsplitMaxVecs = 0x7FFFFFFFll - 1024;  // three-pass, one CTA per row
 
 struct SmCall {
     int dtype;
@@ -45,6 +46,7 @@ struct SmPlan {
     int chunk = 0;         // staged path: bytes per bulk copy
     int nchunks = 0;       // staged path: copies per row
     int nslots = 0;        // staged path: ring slots
+    int resident = 0;      // three-pass split: resident clusters
     KernelFn fn = nullptr;
     const char* name = "";
 };
@@ -81,7 +83,8 @@ rmsnorm_status_t sm_validate(int32_t dtype, const void* x, const void* y, int64_
             (!RMSNORM_FAULT_INJECT ||
              (o.fault_inject == 1 && o.path != RMSNORM_PATH_STAGED) ||
              (o.fault_inject == 2 && o.path != RMSNORM_PATH_CLUSTER &&
-              !(o.path == RMSNORM_PATH_STAGED && o.cluster > 1))))
+              !((o.path == RMSNORM_PATH_STAGED || o.path == RMSNORM_PATH_TWOPASS) &&
+                o.cluster > 1))))
             return RMSNORM_ERR_UNSUPPORTED;
         if (o.path != RMSNORM_PATH_AUTO && o.path != RMSNORM_PATH_ROWREG &&
             o.path != RMSNORM_PATH_TWOPASS && o.path != RMSNORM_PATH_CLUSTER &&
@@ -92,9 +95,12 @@ rmsnorm_status_t sm_validate(int32_t dtype, const void* x, const void* y, int64_
             return RMSNORM_ERR_INVALID_ARG;
         if (o.chunk_bytes < 0 || o.chunk_bytes % 16 != 0 || o.stages < 0)
             return RMSNORM_ERR_INVALID_ARG;
-        if (o.cluster < 0 || o.cluster > 16 || (o.cluster & (o.cluster - 1)) != 0)
+        // cluster sizes: powers of two, or any size up to 16 for TWOPASS
+        if (o.cluster < 0 || o.cluster > 16 ||
+            ((o.cluster & (o.cluster - 1)) != 0 && o.path != RMSNORM_PATH_TWOPASS))
             return RMSNORM_ERR_INVALID_ARG;
-        if (o.cluster > 1 && o.path != RMSNORM_PATH_CLUSTER && o.path != RMSNORM_PATH_STAGED)
+        if (o.cluster > 1 && o.path != RMSNORM_PATH_CLUSTER && o.path != RMSNORM_PATH_STAGED &&
+            o.path != RMSNORM_PATH_TWOPASS)
             return RMSNORM_ERR_INVALID_ARG;
         const bool sub_warp = o.threads > 0 && o.threads < 32 && (o.threads & (o.threads - 1)) == 0;
         if (o.threads < 0 || (o.threads % 32 != 0 && !sub_warp) || o.threads > 1024 || o.grid < 0)
@@ -212,33 +218,73 @@ rmsnorm_status_t sm_plan_rowreg(const SmCall& c, int cluster, SmPlan* P) {
     return RMSNORM_OK;
 }
 
-rmsnorm_status_t sm_plan_threepass(const SmCall& c, SmPlan* P) {
+// Three-pass kernel; cluster > 1 splits each row over a thread-block cluster
+// (slices of whole 32-vector groups, one (maximum, sum) exchange per row).
+rmsnorm_status_t sm_plan_threepass(const SmCall& c, int cluster, SmPlan* P) {
     int vb;
     rmsnorm_status_t st = sm_pick_vb(c, &vb);
     if (st != RMSNORM_OK) return st;
-    KernelFn fn = softmax_threepass_ptr(c.dtype, vb);
+    KernelFn fn = cluster > 1 ? softmax_threepass_cluster_ptr(c.dtype, vb)
+                              : softmax_threepass_ptr(c.dtype, vb);
     if (!fn) return RMSNORM_ERR_UNSUPPORTED;
     const int64_t nvec = c.cols / (vb / c.sz);
-    const int maxb = softmax_threepass_block();
+    // The unsplit kernel's 32-bit vector index must not pass 2^31 - 1 one
+    // stride after the row's last vector: such rows are split.
+    if (cluster == 1 && nvec > kSoftmaxUnsplitMaxVecs) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t slice = cluster > 1 ? sm_round_up((nvec + cluster - 1) / cluster, 32) : nvec;
+    const int maxb = cluster > 1 ? split_block() : softmax_threepass_block();
     const int block = c.opt.threads > 0 ? c.opt.threads
-                                        : (nvec >= maxb ? maxb : sm_round_up(nvec, 32));
+                                        : (slice >= maxb ? maxb : sm_round_up(slice, 32));
     int occ = 0;
-    if (cached_occupancy(c.dv.dev, c.dv.smem_optin, fn, block, 0, 1, &occ) != cudaSuccess)
+    if (cached_occupancy(c.dv.dev, c.dv.smem_optin, fn, block, 0, cluster, &occ) != cudaSuccess)
         return RMSNORM_ERR_CUDA;
     if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
-    const int64_t resident = static_cast<int64_t>(c.dv.sms) * occ;
+    int64_t grid;
+    if (cluster == 1) {
+        const int64_t resident = static_cast<int64_t>(c.dv.sms) * occ;
+        grid = c.opt.grid > 0 ? c.opt.grid : (c.rows < resident ? c.rows : resident);
+    } else {
+        const int64_t nclusters = c.opt.grid > 0 ? (c.opt.grid + cluster - 1) / cluster
+                                                 : (c.rows < occ ? c.rows : occ);
+        grid = nclusters * cluster;
+    }
     *P = SmPlan{};             // every field this plan does not set keeps its default
     P->path = RMSNORM_PATH_TWOPASS;
+    P->cluster = cluster;
+    P->slice_vecs = static_cast<int>(slice);
     P->group = block;
     P->block = block;
     P->rpc = 1;
-    P->grid = static_cast<int>(c.opt.grid > 0 ? c.opt.grid
-                                              : (c.rows < resident ? c.rows : resident));
+    P->grid = static_cast<int>(grid);
     P->vb = vb;
     P->nv = 0;
     P->nvec = static_cast<int>(nvec);
     P->fn = fn;
-    P->name = "softmax_threepass";
+    P->resident = occ;
+    P->name = cluster == 1 ? "softmax_threepass" : "softmax_cluster_threepass";
+    return RMSNORM_OK;
+}
+
+// The three-pass kernel with each row over a cluster of C CTAs (one CTA per
+// row would leave the row's whole traffic to one SM).  C (2..16, any size)
+// minimises the row time waves(C) / C, waves(C) = rows / resident clusters
+// of C, rounded up; ties go to the smaller cluster.
+rmsnorm_status_t sm_plan_threepass_split(const SmCall& c, SmPlan* P) {
+    SmPlan best;
+    int64_t best_waves = 0;
+    for (int cl = 2; cl <= 16; ++cl) {
+        SmPlan Q;
+        const rmsnorm_status_t st = sm_plan_threepass(c, cl, &Q);
+        if (st == RMSNORM_ERR_CUDA) return st;
+        if (st != RMSNORM_OK) continue;
+        const int64_t waves = (c.rows + Q.resident - 1) / Q.resident;
+        if (best_waves == 0 || waves * best.cluster < best_waves * cl) {
+            best = Q;
+            best_waves = waves;
+        }
+    }
+    if (best_waves == 0) return RMSNORM_ERR_UNSUPPORTED;
+    *P = best;
     return RMSNORM_OK;
 }
 
@@ -338,7 +384,8 @@ rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
     switch (c.opt.path) {
         case RMSNORM_PATH_ROWREG: return sm_plan_rowreg(c, 1, P);
         case RMSNORM_PATH_CLUSTER: return sm_plan_rowreg(c, c.opt.cluster ? c.opt.cluster : 2, P);
-        case RMSNORM_PATH_TWOPASS: return sm_plan_threepass(c, P);
+        case RMSNORM_PATH_TWOPASS:
+            return sm_plan_threepass(c, c.opt.cluster ? c.opt.cluster : 1, P);
         case RMSNORM_PATH_STAGED: return sm_plan_staged(c, c.opt.cluster ? c.opt.cluster : 1, P);
         default: break;
     }
@@ -386,7 +433,15 @@ rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
     }
     st = sm_plan_rowreg(c, 1, P);
     if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
-    return sm_plan_threepass(c, P);
+    // Few rows too wide for any of the above: the three-pass kernel, each row
+    // over a cluster.
+    if (c.rows < c.dv.sms) {
+        st = sm_plan_threepass_split(c, P);
+        if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+    }
+    st = sm_plan_threepass(c, 1, P);
+    if (st != RMSNORM_ERR_UNSUPPORTED) return st;
+    return sm_plan_threepass_split(c, P);   // rows too wide for one CTA's 32-bit index
 }
 
 rmsnorm_status_t sm_run(int32_t dtype, const void* x, void* y, int64_t rows, int64_t cols,

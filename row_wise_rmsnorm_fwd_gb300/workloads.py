@@ -24,12 +24,14 @@ c5b        (8, 262144)              bf16   N(0,2)            N(1,0.1)         1e
 w16k       (16384, 16384)           f32    N(0,1)            N(1,0.1)         1e-6
 w32k       (8192, 32768)            f32    N(0,1)            N(1,0.1)         1e-6
 w64k       (16384, 65536)           bf16   N(0,2)            N(1,0.1)         1e-6
+w16m       (8, 16777216)            f32    N(0,1)            N(1,0.1)         1e-6
 =========  =======================  =====  ================  ===============  ======
 
 c1..c5b are the measured workloads; w16k (64 KiB rows) and w32k, w64k
 (128 KiB rows) are extra wide-row cases, too wide for the register-resident
 kernel's sweet spot, used to measure the shared-memory staged, cluster and
-two-pass kernels on HBM-sized inputs.  MODEL_SWEEP
+two-pass kernels on HBM-sized inputs; w16m (eight rows of 64 MiB) is the
+few-rows case too wide for any kernel but the two-pass one.  MODEL_SWEEP
 adds the model-shaped batch x seq grid (see below).
 
 Readings: "N(0,2)" is mean 0, standard deviation 2; the Qwen-shaped case's
@@ -126,6 +128,9 @@ WORKLOADS = {
         Workload("w64k", 6, (16384, 65536), "bf16", ("normal", 0.0, 2.0),
                  ("normal", 1.0, 0.1), 1e-6,
                  description="wide bf16 rows (16384,65536), 128 KiB per row"),
+        Workload("w16m", 9, (8, 1 << 24), "f32", ("normal", 0.0, 1.0),
+                 ("normal", 1.0, 0.1), 1e-6,
+                 description="few very wide fp32 rows (8,16777216), 64 MiB per row"),
     ]
 }
 
@@ -147,8 +152,9 @@ WORKLOADS.update(MODEL_SWEEP)
 
 # Row softmax on the same skeleton: attention-score rows (batch 8 x 32 heads x
 # seq 512 rows of 512 columns, N(0,2) scores), vocabulary logits (rows of
-# 32000, N(0,4)), decode-step logits (few rows of a 128256 vocabulary) and
-# prefill logits (many rows of a 128256 vocabulary); x only, no weight.
+# 32000, N(0,4)), decode-step logits (few rows of a 128256 vocabulary),
+# prefill logits (many rows of a 128256 vocabulary) and few rows of 2^24
+# columns (too wide for any kernel but the three-pass one); x only, no weight.
 SOFTMAX_WORKLOADS = {
     w.name: w for w in [
         Workload("sm_attn_f32", 40, (8 * 32 * 512, 512), "f32", ("normal", 0.0, 2.0),
@@ -175,6 +181,9 @@ SOFTMAX_WORKLOADS = {
         Workload("sm_prefill_bf16", 47, (2048, 128256), "bf16", ("normal", 0.0, 4.0),
                  ("normal", 1.0, 0.0), 0.0, op="softmax",
                  description="prefill logits, 2048 tokens x 128256 vocabulary, bf16"),
+        Workload("sm_wide_f32", 48, (8, 1 << 24), "f32", ("normal", 0.0, 4.0),
+                 ("normal", 1.0, 0.0), 0.0, op="softmax",
+                 description="few very wide rows (8, 16777216) fp32, 64 MiB per row"),
     ]
 }
 WORKLOADS.update(SOFTMAX_WORKLOADS)
@@ -239,6 +248,25 @@ def make_random(shape, dtype: str, seed: int, dist=("normal", 0.0, 1.0),
     """A seeded tensor of any shape (for sweeps over widths and row counts)."""
     g = _generator(seed, device)
     return _draw(tuple(shape), dist, g, device).to(_torch_dtype(dtype))
+
+
+def make_sign_row(n: int, dtype: str, seed: int, device: str = "cuda",
+                  w_dist=("normal", 1.0, 0.1), chunk: int = 1 << 27):
+    """One row of n entries +1 or -1 (each sign with probability 1/2) and a
+    weight vector of n entries from ``w_dist``, drawn chunk by chunk from
+    generators seeded with ``seed`` (x) and ``seed + 1`` (w), so rows of up to
+    2^31 - 1 entries need no full-size temporaries.  Returns (x of shape
+    (1, n), w of shape (n,))."""
+    gx, gw = _generator(seed, device), _generator(seed + 1, device)
+    x = torch.empty((1, n), dtype=_torch_dtype(dtype), device=device)
+    w = torch.empty((n,), dtype=_torch_dtype(dtype), device=device)
+    for a in range(0, n, chunk):
+        b = min(n, a + chunk)
+        u = torch.rand(b - a, generator=gx, device=device)
+        x[0, a:b] = torch.where(u < 0.5, -1.0, 1.0).to(x.dtype)
+        del u
+        w[a:b] = _draw((b - a,), w_dist, gw, device).to(w.dtype)
+    return x, w
 
 
 def bf16_bits(t: torch.Tensor):

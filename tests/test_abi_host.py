@@ -39,7 +39,7 @@ def test_status_strings(lib):
         s = binding.rmsnorm_status_string(code)
         assert isinstance(s, str) and s
     assert binding.rmsnorm_status_string(99) == "unknown status"
-    assert binding.rmsnorm_abi_version() == 10100
+    assert binding.rmsnorm_abi_version() == 10200
 
 
 def test_struct_sizes_match_header():

@@ -67,6 +67,8 @@ CASES = [
     ("staged cluster withholds a partial", dict(path="staged", cluster=2, fault_inject=2),
      (16, 8192)),
     ("ring-to-register withholds a copy", dict(path="ringreg", fault_inject=1), (64, 16384)),
+    ("two-pass cluster withholds a partial", dict(path="twopass", cluster=4, fault_inject=2),
+     (8, 65536)),
 ]
 
 
@@ -121,6 +123,8 @@ SOFTMAX_CASES = [
      (8, 65536)),
     ("softmax staged cluster withholds a pair", dict(path="staged", cluster=4, fault_inject=2),
      (16, 128256)),
+    ("softmax three-pass cluster withholds a pair",
+     dict(path="twopass", cluster=4, fault_inject=2), (8, 65536)),
 ]
 
 

@@ -74,7 +74,7 @@ def test_workload_page_schedule(name):
     check_case(x.reshape(-1, wl.hidden), w, wl.eps, f"page schedule {name}", path="page")
 
 
-@pytest.mark.parametrize("name", ["c4", "c5a"])
+@pytest.mark.parametrize("name", ["c4", "c5a", "w16m"])
 def test_workload_full_size_every_row(name):
     """Full-size workload in the bench's launch configuration (automatic
     path, current stream, inputs drawn on the device); every row is checked
@@ -113,10 +113,50 @@ def test_row_sweep(dtype, hidden):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("rows,hidden", [(1, 262144), (8, 262144), (3, 100000), (2, 1 << 20)])
+@pytest.mark.parametrize("rows,hidden", [(1, 262144), (8, 262144), (3, 100000), (2, 1 << 20),
+                                         (1, (1 << 22) + 3), (3, 3 << 20)])
 def test_wide_rows(dtype, rows, hidden):
     x, w = rand_case(rows, hidden, dtype, seed=rows + hidden, xdist=("normal", 0.0, 2.0))
     check_case(x, w, 1e-6, f"{dtype} {rows}x{hidden}")
+
+
+MAX_HIDDEN = (1 << 31) - 1      # the widest row the ABI accepts
+
+
+@pytest.mark.parametrize("dtype,opts", [("f32", {}), ("bf16", {}),
+                                        ("bf16", {"path": "twopass", "cluster": 2})],
+                         ids=["f32-auto", "bf16-auto", "bf16-twopass-cluster-2"])
+def test_maximum_row_width(dtype, opts):
+    """One row of 2^31 - 1 elements.  The width is odd, so every vector is a
+    single element and the row holds 2^31 - 1 of them: the vector indices
+    reach the top of their range.  x is +-1 with random signs, so the row's
+    mean square is exactly 1 whatever its length, and any contiguous piece of
+    the row has the same mean square: the oracle, run on the row piece by
+    piece (each piece as a row of its own), gives every element's expected
+    value.  The automatic choice splits the row over a cluster of two-pass
+    CTAs (of the size that fills the most SMs), the forced one over two; the
+    unsplit two-pass kernel refuses a row this wide without launching."""
+    import concurrent.futures as cf
+    import os
+
+    x, w = workloads.make_sign_row(MAX_HIDDEN, dtype, seed=4242)
+    with pytest.raises(binding.RmsnormError) as ei:
+        binding.rmsnorm_plan(x, w, options={"path": "twopass"})
+    assert ei.value.status == binding.RMSNORM_ERR_UNSUPPORTED
+    y = run(x, w, 1e-6, **opts)
+    plan = binding.rmsnorm_plan(x, w, y, options=opts or None)
+    assert plan["vec_bytes"] == x.element_size(), plan
+    piece = 1 << 22
+
+    def check(a):
+        b = min(MAX_HIDDEN, a + piece)
+        xs, ws = x[:, a:b].cpu(), w[a:b].cpu()
+        compare(y[:, a:b], oracle_for(xs, ws, 1e-6), f"{dtype} {opts} elements {a}..{b - 1}")
+
+    with cf.ThreadPoolExecutor(max(1, min(8, len(os.sched_getaffinity(0))))) as ex:
+        list(ex.map(check, range(0, MAX_HIDDEN, piece)))
+    del x, w, y
+    torch.cuda.empty_cache()
 
 
 # ----------------------------------------------------------- forced paths --
@@ -129,6 +169,9 @@ FORCED = [
     ("cluster", {"cluster": 2}), ("cluster", {"cluster": 4}), ("cluster", {"cluster": 8}),
     ("cluster", {"cluster": 16}), ("page", {}), ("ringreg", {}), ("ringreg", {"stages": 2}),
     ("ringreg", {"threads": 256}), ("ringreg", {"grid": 2}),
+    ("twopass", {"cluster": 2}), ("twopass", {"cluster": 16}),
+    ("twopass", {"cluster": 4, "threads": 96}), ("twopass", {"cluster": 3}),
+    ("twopass", {"cluster": 12}),
 ]
 
 
@@ -342,6 +385,7 @@ def test_plan_reports_families():
     ((1024, 32768), "f32", "ringreg", 512, 16),      # fp32 rows of 128 KB
     ((1024, 24576), "f32", "twopass", 1024, 0),      # fp32 rows of 96 KB
     ((8, 262144), "bf16", "cluster_rowreg", 512, 8), # c5b: few wide rows
+    ((2, 1 << 20), "f32", "twopass_cluster", 1024, 0),   # few rows of 4 MB
 ])
 def test_automatic_choice(shape, dtype, kernel, lanes, nv):
     """The automatic kernel choice for representative shapes (a guard on the
@@ -351,6 +395,19 @@ def test_automatic_choice(shape, dtype, kernel, lanes, nv):
     p = binding.rmsnorm_plan(x, w)
     assert p["kernel"] == kernel, p
     assert p["threads_per_row"] == lanes and p["vecs_per_thread"] == nv, p
+
+
+def test_few_very_wide_rows_split_over_clusters():
+    """Rows too wide for any cluster's registers or shared memory still spread
+    over rows x 16 SMs: the two-pass kernel, each row over a cluster."""
+    x = torch.empty(2, 1 << 20, device="cuda")
+    w = torch.empty(1 << 20, device="cuda")
+    p = binding.rmsnorm_plan(x, w)
+    assert p["kernel"] == "twopass_cluster" and p["cluster"] >= 8, p
+    assert p["grid"] == 2 * p["cluster"], p
+    x = torch.empty(300, 1 << 20, device="cuda")   # many rows: one CTA per row
+    p = binding.rmsnorm_plan(x, w)
+    assert p["kernel"] == "twopass" and p["cluster"] == 1, p
 
 
 def test_row_kernel_grid_has_about_three_row_blocks_per_cta():

@@ -78,7 +78,8 @@ def test_width_sweep(dtype, cols):
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("path,cluster", [("rowreg", 0), ("twopass", 0), ("staged", 0),
                                           ("cluster", 2), ("cluster", 4), ("cluster", 8),
-                                          ("cluster", 16)])
+                                          ("cluster", 16), ("twopass", 2), ("twopass", 16),
+                                          ("twopass", 5), ("twopass", 12)])
 @pytest.mark.parametrize("rows,cols", [(300, 512), (7, 4096), (3, 32000), (64, 1000),
                                        (5, 128256), (2, 262144)])
 def test_forced_paths(dtype, path, cluster, rows, cols):
@@ -93,18 +94,33 @@ def test_forced_paths(dtype, path, cluster, rows, cols):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_cluster_special_values(dtype):
-    """Masked, fully masked, NaN and +inf rows through the cluster split (the
-    maximum and the sum cross the cluster)."""
+@pytest.mark.parametrize("path", ["cluster", "twopass"])
+def test_cluster_special_values(dtype, path):
+    """Masked, fully masked, NaN and +inf rows through the cluster splits of
+    the register and the three-pass kernels (the maximum and the sum cross
+    the cluster); row 4 has one slice of -inf and finite slices elsewhere."""
     cols = 65536
-    x = case(4, cols, "f32", 19)
+    x = case(5, cols, "f32", 19)
     x[0, ::7] = -float("inf")
     x[1] = -float("inf")
     x[2, 60000] = float("nan")
     x[3, 3] = float("inf")
+    x[4, :cols // 8] = -float("inf")
     x = x.to(DT[dtype])
-    y = run(x.cuda(), path="cluster", cluster=8)
-    compare(y, ref_for(x), f"cluster special {dtype}")
+    y = run(x.cuda(), path=path, cluster=8)
+    compare(y, ref_for(x), f"{path} cluster special {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols", [(1, (1 << 22) + 3), (3, 3 << 20), (2, 1 << 20)])
+def test_few_very_wide_rows(dtype, rows, cols):
+    """Rows too wide for the register and staged kernels, few of them: the
+    automatic choice splits each over a cluster of three-pass CTAs."""
+    x = case(rows, cols, dtype, rows * 7 + cols)
+    xd = x.cuda()
+    p = binding.rowsoftmax_plan(xd, torch.empty_like(xd))
+    assert p["kernel"] == "softmax_cluster_threepass" and p["cluster"] >= 8, p
+    compare(run(xd), ref_for(x), f"{dtype} {rows}x{cols}")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -272,6 +288,7 @@ def test_guards_and_determinism(dtype):
     ((5592, 48000), "f32", "softmax_threepass"),         # rows of 188 KB
     ((4096, 65536), "f32", "softmax_cluster_staged"),    # rows of 256 KB
     ((8, 128256), "f32", "softmax_cluster_rowreg"),      # decode logits
+    ((2, 1 << 20), "f32", "softmax_cluster_threepass"),  # few rows of 4 MB
 ])
 def test_automatic_choice(shape, dtype, kernel):
     """The automatic kernel choice for representative shapes (no launch)."""
