@@ -56,3 +56,27 @@ def test_every_row_softmax_mode(dtype):
     with pytest.raises(AssertionError):
         compare_every_row(x, y, None, 0.0, "planted", chunk_rows=128, piece_elems=40 * 257,
                           threads=3, op="softmax")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sign_row_pieces_reproduce_the_whole_row(dtype):
+    """The widest-row parity test checks a row of 2^31 - 1 elements piece by
+    piece, running the oracle on each piece as a row of its own.  That is
+    exact only because every entry is +1 or -1: the mean square of the row
+    and of any piece is then exactly 1.  Checked here on a small row drawn by
+    the same generator: the entries are +-1 with both signs present, and the
+    oracle's per-piece outputs equal its whole-row outputs bit for bit."""
+    n, piece = 10_007, 1_000
+    x, w = workloads.make_sign_row(n, dtype, seed=4242, device="cpu", chunk=3_000)
+    xf = x.float()
+    assert bool((xf.abs() == 1).all()) and 0 < int((xf > 0).sum()) < n
+    if dtype == "f32":
+        whole = oracle.rmsnorm_f32(x.numpy(), w.numpy(), 1e-6)
+        parts = [oracle.rmsnorm_f32(x[:, a:a + piece].numpy(), w[a:a + piece].numpy(), 1e-6)
+                 for a in range(0, n, piece)]
+    else:
+        xb, wb = workloads.bf16_bits(x), workloads.bf16_bits(w)
+        _, whole = oracle.rmsnorm_bf16(xb, wb, 1e-6)
+        parts = [oracle.rmsnorm_bf16(xb[:, a:a + piece], wb[a:a + piece], 1e-6)[1]
+                 for a in range(0, n, piece)]
+    assert np.array_equal(np.concatenate(parts, axis=1), whole)
