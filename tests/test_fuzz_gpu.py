@@ -54,7 +54,7 @@ def _rms_case(rng: random.Random):
         ("auto", {}), ("rowreg", {}), ("rowreg", {"grid": rng.randint(1, 400)}),
         ("staged", {}), ("staged", {"cluster": rng.choice([2, 4])}), ("ringreg", {}),
         ("ringreg", {"stages": rng.randint(2, 6)}), ("cluster", {"cluster": rng.choice([2, 4, 8, 16])}),
-        ("twopass", {}), ("page", {}),
+        ("twopass", {}), ("page", {}), ("twopass", {"cluster": rng.randint(2, 16)}),
     ])
     epi = rng.choice(["none", "none", "scale", "relu"])
     return dtype, rows, hidden, offs, path, extra, epi
@@ -101,7 +101,7 @@ def test_softmax_random_case(seed):
     path, extra = rng.choice([
         ("auto", {}), ("rowreg", {}), ("staged", {}), ("staged", {"cluster": rng.choice([2, 4, 8])}),
         ("staged", {"stages": rng.randint(1, 6)}), ("cluster", {"cluster": rng.choice([2, 4, 8, 16])}),
-        ("twopass", {}),
+        ("twopass", {}), ("twopass", {"cluster": rng.randint(2, 16)}),
     ])
     x = workloads.make_random((rows, cols), dtype, seed, ("normal", 0.0, rng.choice([1.0, 4.0, 40.0])))
     xd = _placed(x, offs[0])
