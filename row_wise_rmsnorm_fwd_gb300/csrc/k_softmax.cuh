@@ -68,6 +68,20 @@ __device__ __forceinline__ float row_exp(float v, float c) {
     return row_exp_arg<T>(fmaf(v, kLog2e, c));
 }
 
+// A split row's slices each form their exponentials with their own offset
+// c = bias - m*log2(e), m the slice's maximum, rounded to fp32.  That rounding
+// (up to half an ulp of |m|*log2(e): 7.6e-6 for |m| near 100) is a factor
+// common to the slice, not to the row, so unlike a whole row's offset it does
+// not cancel in e / sum.  This returns 2^-eps, eps = c - (bias - m*log2(e))
+// recovered with one fma; the split kernels multiply the slice sum they
+// exchange and the slice's output scale by it.  1 for a slice whose maximum
+// is not finite (c = -inf, or a NaN row).
+template <typename T>
+__device__ __forceinline__ float slice_offset_correction(float m, float c) {
+    if (!(fabsf(m) < INFINITY)) return 1.0f;
+    return exp2f(-fmaf(m, kLog2e, c - row_exp_bias<T>()));
+}
+
 // Packed fp32 pairs: the f32x2 forms of fma, add and mul (sm_100 and later)
 // do two lanes in one instruction, each lane rounded exactly as the scalar
 // fmaf / + / * would be, so a kernel that pairs its elements computes the
@@ -420,10 +434,13 @@ softmax_rowreg_kernel(const Params p) {
         float inv = 1.0f / s;
         if (CL) {
             // one exchange of the (maximum, sum) pair gives the row's
+            const float corr = slice_offset_correction<T>(m, c);
             float M, S;
-            const bool ok = cluster_pair_allreduce(&ex, m, s, ncta, rank, it, p, &M, &S, tid);
+            const bool ok =
+                cluster_pair_allreduce(&ex, m, s * corr, ncta, rank, it, p, &M, &S, tid);
             if (__syncthreads_or(!ok)) break;   // uniform: stop, then leave cleanly
-            inv = exp2f((m - M) * kLog2e) / S;   // rescale this slice to the row's maximum
+            // rescale this slice to the row's maximum
+            inv = exp2f((m - M) * kLog2e) * corr / S;
         }
         if (row_ok) {
             char* dst = yb + row * row_bytes;
@@ -594,10 +611,13 @@ __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kerne
         for (int k = 0; k < NW; ++k) sum += red[32 + b * 16 + k];
         float inv = 1.0f / sum;
         if (CL) {
+            const float corr = slice_offset_correction<T>(m, c);
             float M, S;
-            const bool cok = cluster_pair_allreduce(ex, m, sum, ncta, rank, it, p, &M, &S, tid);
+            const bool cok =
+                cluster_pair_allreduce(ex, m, sum * corr, ncta, rank, it, p, &M, &S, tid);
             if (__syncthreads_or(!cok)) break;   // uniform: stop, then leave cleanly
-            inv = exp2f((m - M) * kLog2e) / S;    // rescale this slice to the row's maximum
+            // rescale this slice to the row's maximum
+            inv = exp2f((m - M) * kLog2e) * corr / S;
         }
         char* dst = yb + row * row_bytes + sbeg;
 #pragma unroll

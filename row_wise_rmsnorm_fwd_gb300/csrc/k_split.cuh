@@ -249,13 +249,16 @@ __global__ void __launch_bounds__(kSplitThreads, 1) softmax_threepass_cluster_ke
         __syncthreads();
         s = 0.f;
         for (int k = 0; k < nwarps; ++k) s += red[1][b][k];
-        // one exchange of the (maximum, sum) pair gives the row's
+        // one exchange of the (maximum, sum) pair gives the row's; the slice
+        // sum and pass 3's offset are both corrected for the rounding of
+        // their offsets (slice_offset_correction)
         float M, S;
-        const bool ok = cluster_pair_allreduce(&ex, m, s, p.cluster, rank, it, p, &M, &S,
+        const bool ok = cluster_pair_allreduce(&ex, m, s * slice_offset_correction<T>(m, c),
+                                               p.cluster, rank, it, p, &M, &S,
                                                static_cast<int>(tid));
         if (__syncthreads_or(!ok)) break;   // uniform: stop, then leave cleanly
         const float c3 = row_exp_bias<T>() - M * kLog2e;
-        const float inv = 1.0f / S;
+        const float inv = slice_offset_correction<T>(M, c3) / S;
 
         // pass 3, forward: exp(x - M) / S
         char* dst = yb + soff;

@@ -253,19 +253,20 @@ def make_random(shape, dtype: str, seed: int, dist=("normal", 0.0, 1.0),
 def make_sign_row(n: int, dtype: str, seed: int, device: str = "cuda",
                   w_dist=("normal", 1.0, 0.1), chunk: int = 1 << 27):
     """One row of n entries +1 or -1 (each sign with probability 1/2) and a
-    weight vector of n entries from ``w_dist``, drawn chunk by chunk from
-    generators seeded with ``seed`` (x) and ``seed + 1`` (w), so rows of up to
-    2^31 - 1 entries need no full-size temporaries.  Returns (x of shape
-    (1, n), w of shape (n,))."""
+    weight vector of n entries from ``w_dist`` (none if ``w_dist`` is None),
+    drawn chunk by chunk from generators seeded with ``seed`` (x) and
+    ``seed + 1`` (w), so rows of up to 2^31 - 1 entries need no full-size
+    temporaries.  Returns (x of shape (1, n), w of shape (n,) or None)."""
     gx, gw = _generator(seed, device), _generator(seed + 1, device)
     x = torch.empty((1, n), dtype=_torch_dtype(dtype), device=device)
-    w = torch.empty((n,), dtype=_torch_dtype(dtype), device=device)
+    w = None if w_dist is None else torch.empty((n,), dtype=_torch_dtype(dtype), device=device)
     for a in range(0, n, chunk):
         b = min(n, a + chunk)
         u = torch.rand(b - a, generator=gx, device=device)
         x[0, a:b] = torch.where(u < 0.5, -1.0, 1.0).to(x.dtype)
         del u
-        w[a:b] = _draw((b - a,), w_dist, gw, device).to(w.dtype)
+        if w is not None:
+            w[a:b] = _draw((b - a,), w_dist, gw, device).to(w.dtype)
     return x, w
 
 

@@ -1,12 +1,13 @@
 """GPU parity of the row-wise softmax against the fp64 CPU oracle (C ABI via
-the ctypes binding).  Tolerances as for RMSNorm (tests/_parity.py): fp32
-|d| <= max(1e-5 |ref|, 1e-6); bf16 within 1 ulp of the single rounding."""
+the ctypes binding).  Tolerances (tests/_parity.py): fp32 |d| <= max(1e-5
+|ref|, 1e-35), a relative bound down to outputs near the subnormal range;
+bf16 within 1 ulp of the single rounding."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from _parity import check_bf16, check_f32, compare_every_row
+from _parity import SOFTMAX_F32_ATOL, check_bf16, check_f32, compare_every_row
 from row_wise_rmsnorm_fwd_gb300 import binding, build, workloads
 
 pytestmark = pytest.mark.gpu
@@ -32,7 +33,7 @@ def ref_for(x_cpu):
 def compare(y, ref, what):
     y = y.detach().cpu().contiguous()
     if y.dtype == torch.float32:
-        check_f32(y.numpy(), ref, what)
+        check_f32(y.numpy(), ref, what, atol=SOFTMAX_F32_ATOL)
     else:
         check_bf16(workloads.bf16_bits(y), ref, what)
 
@@ -109,6 +110,50 @@ def test_cluster_special_values(dtype, path):
     x = x.to(DT[dtype])
     y = run(x.cuda(), path=path, cluster=8)
     compare(y, ref_for(x), f"{path} cluster special {dtype}")
+
+
+MAX_COLS = (1 << 31) - 1      # the widest row the ABI accepts
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_maximum_row_width(dtype):
+    """One row of 2^31 - 1 columns (odd: one-element vectors, so the vector
+    indices reach the top of their range), split over a cluster of three-pass
+    CTAs; the unsplit three-pass kernel refuses it without launching.  x is
+    +-1 with random signs, so by the definition every output is one of two
+    values, v+ = e / S and v- = e^-1 / S with S = n+ e + n- e^-1 (n+, n- the
+    counts of each sign), evaluated in binary64 (and rounded once to bf16);
+    every element is compared against its value, piece by piece."""
+    import concurrent.futures as cf
+    import math
+    import os
+
+    x, _ = workloads.make_sign_row(MAX_COLS, dtype, seed=4343, w_dist=None)
+    y = torch.empty_like(x)
+    with pytest.raises(binding.RmsnormError) as ei:
+        binding.rowsoftmax_plan(x, y, options={"path": "twopass"})
+    assert ei.value.status == binding.RMSNORM_ERR_UNSUPPORTED
+    p = binding.rowsoftmax_plan(x, y)
+    assert p["kernel"] == "softmax_cluster_threepass" and p["vec_bytes"] == x.element_size(), p
+    run(x, y=y)
+    n_pos = int((x > 0).sum())
+    n_neg = MAX_COLS - n_pos
+    assert 0 < n_pos < MAX_COLS
+    s = n_pos * math.e + n_neg / math.e
+    v = np.array([math.e / s, 1.0 / (math.e * s)])          # v+, v-
+    ref_vals = v if dtype == "f32" else oracle.f64_to_bf16(v)
+    piece = 1 << 22
+
+    def check(a):
+        b = min(MAX_COLS, a + piece)
+        pos = (x[0, a:b] > 0).cpu().numpy()
+        ref = np.where(pos, ref_vals[0], ref_vals[1])
+        compare(y[:, a:b], ref[None, :], f"{dtype} softmax columns {a}..{b - 1}")
+
+    with cf.ThreadPoolExecutor(max(1, min(8, len(os.sched_getaffinity(0))))) as ex:
+        list(ex.map(check, range(0, MAX_COLS, piece)))
+    del x, y
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
