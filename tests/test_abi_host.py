@@ -145,3 +145,14 @@ def test_softmax_ex_staged_shape_options_are_checked(lib):
         o = binding.make_options(path="staged")
         setattr(o, field, value)
         assert binding.raw.rowsoftmax_fwd_ex(0, A, B, 4, 8, o) == INVALID, (field, value)
+
+
+def test_softmax_cluster_sizes_are_checked(lib):
+    """A split over a cluster takes 2..16 CTAs: any size for the three-pass
+    kernel (RMSNORM_PATH_TWOPASS), powers of two for the register and staged
+    kernels; anything else is refused before any CUDA call."""
+    for path, cluster in (("cluster", 3), ("cluster", 12), ("staged", 6), ("twopass", 17),
+                          ("twopass", -1), ("rowreg", 2), ("auto", 2)):
+        o = binding.make_options(path=path)
+        o.cluster = cluster
+        assert binding.raw.rowsoftmax_fwd_ex(0, A, B, 4, 8, o) == INVALID, (path, cluster)
