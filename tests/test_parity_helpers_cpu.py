@@ -80,3 +80,26 @@ def test_sign_row_pieces_reproduce_the_whole_row(dtype):
         parts = [oracle.rmsnorm_bf16(xb[:, a:a + piece], wb[a:a + piece], 1e-6)[1]
                  for a in range(0, n, piece)]
     assert np.array_equal(np.concatenate(parts, axis=1), whole)
+
+
+def test_sign_row_softmax_closed_form_matches_the_oracle():
+    """The widest-row softmax test compares every output against
+    v+ = e / S or v- = e^-1 / S, S = n+ e + n- e^-1, instead of running the
+    oracle over 2^31 - 1 columns.  That formula is the definition for a row
+    of +-1 entries; checked here against the oracle on a small row drawn by
+    the same generator, in binary64 and after the single bf16 rounding."""
+    import math
+
+    n = 10_007
+    x, _ = workloads.make_sign_row(n, "f32", seed=4343, device="cpu", w_dist=None, chunk=3_000)
+    xs = x.numpy()
+    n_pos = int((xs > 0).sum())
+    s = n_pos * math.e + (n - n_pos) / math.e
+    v = np.array([math.e / s, 1.0 / (math.e * s)])
+    closed = np.where(xs > 0, v[0], v[1])
+    ref = oracle.rowsoftmax_f64(xs.astype(np.float64))
+    assert np.allclose(ref, closed, rtol=1e-13, atol=0)
+    xb = workloads.bf16_bits(x.to(torch.bfloat16))
+    _, ref16 = oracle.rowsoftmax_bf16(xb)
+    assert np.array_equal(ref16, np.where(xs > 0, oracle.f64_to_bf16(v)[0],
+                                          oracle.f64_to_bf16(v)[1]))
