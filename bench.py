@@ -28,6 +28,13 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
+# GB300 datasheet HBM3e bandwidth, reported beside the measured copy peak.
+NOMINAL_HBM_GBS = 7900.0
+L2_BYTES = 129e6
+# Timed after the main region of the default run, same method and clocks: the
+# other graded RMSNorm config, the few-row split-row config, the few very wide
+# rows, and the prefill-logit row softmax.
+SECONDARY_DEFAULT = ("c4", "c5b", "w16m", "sm_prefill_f32", "sm_prefill_bf16", "sm_wide_f32")
 METRIC = "RMSNorm GB/s and rows/s on 1 GB300; % of HBM roofline"
 METRIC_SOFTMAX = "row softmax GB/s and rows/s on 1 GB300; % of HBM roofline"
 
@@ -140,6 +147,20 @@ class ClockSampler:
         sm.sort()
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def roofline_block(achieved, peak, peak_src, traffic=None):
+    """The roofline object: `frac` is of the measured copy peak (a torch
+    copy's read+write rate, so a kernel that streams reads and writes
+    separately can sit a little above 1); `frac_of_nominal` is of the
+    datasheet HBM3e bandwidth."""
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak,
+            "peak_source": (f"{peak_src} copy peak (MEASURED_PEAKS.json hbm_gbs: torch "
+                            "b.copy_(a), read+write bytes)" if peak_src == "measured"
+                            else f"{peak_src} copy peak"),
+            "nominal_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+            "traffic": traffic}
 
 
 def max_over_ranks(values, device="cpu"):
@@ -467,6 +488,16 @@ def run_ours(args, wl):
 
     del x, y
     torch.cuda.empty_cache()
+    secondary = None
+    names = secondary_names(args) if world == 1 else []
+    if names:
+        secondary = {}
+        with ClockSampler(local) as clocks2:
+            time.sleep(0.3)
+            for name in names:
+                secondary[name] = time_secondary(workloads.WORKLOADS[name], 50, binding,
+                                                 workloads, peak, peak_src)
+        secondary["clocks"] = clocks2.summary()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_line(wl)
@@ -492,11 +523,10 @@ def run_ours(args, wl):
                        "launch_ms_p90": per_launch_sorted[(9 * len(per_launch_sorted)) // 10],
                        "launch_ms_min": per_launch_sorted[0],
                        "launch_ms_max": per_launch_sorted[-1]},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_source": f"{peak_src} (hbm_gbs)",
-                         "traffic": traffic},
+            "roofline": roofline_block(achieved, peak, peak_src, traffic),
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "secondary": secondary,
             "gpu_launches": args.steps,
             "timed_region_ms": region_ms,
             "device": device_info(dev),
@@ -506,6 +536,87 @@ def run_ours(args, wl):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def secondary_names(args):
+    """Workloads timed after the main region: by default only on the default
+    run (the headline workload, nothing forced, all rows); --secondary
+    overrides the list, --secondary none switches it off."""
+    if args.secondary is not None:
+        return [n for n in args.secondary.split(",") if n and n != "none"]
+    if args.workload != "c5a" or args.rows or forced(args):
+        return []
+    return list(SECONDARY_DEFAULT)
+
+
+def time_secondary(wl, steps, binding, workloads, peak, peak_src):
+    """One secondary workload through its automatic entry point, timed with
+    CUDA events on the launching stream.  Inputs larger than 4x L2 run back to
+    back (one event pair around all launches); smaller inputs rotate through
+    enough copies of x and y (more than 3x L2 in rotation) that every launch
+    finds its input and output out of L2, and one event pair times the
+    launches back to back (single launches of a few microseconds are below
+    the event timer's resolution)."""
+    import torch
+
+    softmax = wl.op == "softmax"
+    x = workloads.make_x(wl, device="cuda")
+    w = torch.empty(0, device="cuda") if softmax else workloads.make_w(wl, device="cuda")
+    io_bytes = 2 * x.numel() * x.element_size()
+    rotate = wl.bytes_per_call <= 4 * L2_BYTES
+    nbuf = int(3.2 * L2_BYTES // io_bytes) + 1 if rotate else 1
+    xs = [x] + [x.clone() for _ in range(nbuf - 1)]
+    ys = [torch.empty_like(x) for _ in range(nbuf)]
+    stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream
+    bf16 = wl.dtype == "bf16"
+    rows, hidden = wl.rows, wl.hidden
+    if softmax:
+        fn = binding.raw.rowsoftmax_fwd_bf16 if bf16 else binding.raw.rowsoftmax_fwd_f32
+
+        def launch(i):
+            return fn(xs[i % nbuf].data_ptr(), ys[i % nbuf].data_ptr(), rows, hidden, handle)
+        plan = binding.rowsoftmax_plan(x, ys[0])
+    else:
+        fn = binding.raw.rmsnorm_fwd_bf16 if bf16 else binding.raw.rmsnorm_fwd_f32
+
+        def launch(i):
+            return fn(xs[i % nbuf].data_ptr(), w.data_ptr(), ys[i % nbuf].data_ptr(), rows,
+                      hidden, wl.eps, handle)
+        plan = binding.rmsnorm_plan(x, w, ys[0])
+    n = max(steps, 2 * nbuf) if rotate else steps
+    for i in range(max(3, nbuf)):
+        st = launch(i)
+        if st != 0:
+            raise RuntimeError(f"{wl.name}: {binding.rmsnorm_status_string(st)}")
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(n):
+        launch(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if binding.rmsnorm_last_device_status() != binding.RMSNORM_OK:
+        raise RuntimeError(f"{wl.name}: device status word set")
+    ms = t0.elapsed_time(t1) / n
+    achieved = wl.bytes_per_call / (ms / 1e3) / 1e9
+    del xs, ys, x, w
+    torch.cuda.empty_cache()
+    return {
+        "workload": f"{wl.name}: {wl.description}", "shape": list(wl.shape),
+        "io_dtype": wl.dtype, "op": wl.op, "bytes_per_launch": wl.bytes_per_call,
+        "ms_per_launch": ms, "value": achieved, "unit": "GB/s",
+        "rows_per_s": rows / (ms / 1e3), "launches": n,
+        "kernel": {"name": plan["kernel"], "grid": plan["grid"], "block": plan["block_threads"],
+                   "cluster": plan["cluster"]},
+        "timing": (f"{n} launches back to back rotating over {nbuf} copies of x and y "
+                   f"({nbuf * io_bytes / 1e6:.0f} MB, more than 3x L2), one event pair"
+                   if rotate else f"{n} launches back to back (inputs larger than L2), "
+                                  "one event pair"),
+        "roofline": roofline_block(achieved, peak, peak_src,
+                                   profiled_traffic(wl.name, plan["kernel"])),
+    }
 
 
 def measure_e2e(args, wl, x_dev, w_dev, y_dev, fwd, binding, world):
@@ -599,6 +710,9 @@ def main():
                          "that fit L2; hot: no flush, for the L2-resident figure")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--secondary", default=None,
+                    help="comma-separated workloads timed after the main region (default: "
+                         + ",".join(SECONDARY_DEFAULT) + " on the default run; 'none' = off)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

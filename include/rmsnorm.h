@@ -136,6 +136,10 @@ typedef struct {
 
 /*
  * rmsnorm_fwd_f32 -- y = RMSNorm(x) * w for fp32 tensors.
+ * Defined by: page "A hackable Python ML compiler, part 2", the RMSNorm
+ * Loop-IR listing (the reduce axis summing x^2, the free axis scaling by the
+ * reciprocal root and then by the weight) and the epilogue of the CUDA kernel
+ * it generates (rsqrt of sum * (1/H) + eps).
  * x, y: rows*hidden floats (device); w: hidden floats (device);
  * rows >= 0; 1 <= hidden <= 2^31-1; eps finite and >= 0.
  * Returns RMSNORM_OK once launched; RMSNORM_ERR_INVALID_ARG for NULL pointers,
@@ -148,7 +152,9 @@ rmsnorm_status_t rmsnorm_fwd_f32(const float* x, const float* w, float* y,
 
 /*
  * rmsnorm_fwd_bf16 -- the same for bfloat16 tensors, passed as raw 16-bit
- * patterns.  Accumulation, rstd and the products are fp32; each output is
+ * patterns.  Defined by: the same Loop-IR listing and kernel epilogue as
+ * rmsnorm_fwd_f32; the page is fp32 only, so the bf16 rounding below is this
+ * library's reading, not a passage.  Accumulation, rstd and the products are fp32; each output is
  * rounded once to bfloat16 (round-to-nearest-even).  Arguments and errors as
  * for rmsnorm_fwd_f32.
  */
@@ -157,7 +163,9 @@ rmsnorm_status_t rmsnorm_fwd_bf16(const uint16_t* x, const uint16_t* w, uint16_t
                                   rmsnorm_stream_t stream);
 
 /*
- * rmsnorm_fwd_ex -- either dtype, with explicit options (forced kernel family,
+ * rmsnorm_fwd_ex -- the operation of rmsnorm_fwd_f32 / rmsnorm_fwd_bf16 (same
+ * passages); the options have no counterpart in the page: they choose among
+ * this library's kernels.  Either dtype, with explicit options (forced kernel family,
  * cluster size, launch shape, wait limit).  `opt` may be NULL (= automatic).
  * Returns RMSNORM_ERR_UNSUPPORTED when a forced option cannot serve the call
  * (e.g. STAGED on a row pitch that is not a multiple of 16 bytes); nothing is
@@ -168,7 +176,8 @@ rmsnorm_status_t rmsnorm_fwd_ex(int32_t dtype, const void* x, const void* w, voi
                                 const rmsnorm_options_t* opt, rmsnorm_stream_t stream);
 
 /*
- * rmsnorm_plan -- fill *plan with what rmsnorm_fwd_ex(dtype, x, w, y, rows,
+ * rmsnorm_plan -- no passage of the page: a query of this library's launch
+ * heuristics.  Fill *plan with what rmsnorm_fwd_ex(dtype, x, w, y, rows,
  * hidden, ., opt, .) would launch on the current device, without launching.
  * Pointers are used only for their alignment (they may be any non-NULL values).
  */
@@ -177,18 +186,19 @@ rmsnorm_status_t rmsnorm_plan(int32_t dtype, const void* x, const void* w, const
                               const rmsnorm_options_t* opt, rmsnorm_plan_t* plan);
 
 /*
- * rmsnorm_last_device_status -- synchronise `stream`, then read and clear the
+ * rmsnorm_last_device_status -- no passage of the page defines it: it reports
+ * this library's own failure detection (bounded device waits).  Synchronise `stream`, then read and clear the
  * current device's status word.  RMSNORM_OK if no kernel's bounded wait has
  * expired since the last read; RMSNORM_ERR_TIMEOUT otherwise (outputs of the
  * affected call are undefined); RMSNORM_ERR_CUDA if synchronisation failed.
  */
 rmsnorm_status_t rmsnorm_last_device_status(rmsnorm_stream_t stream);
 
-/* Static English text for a status code (never NULL). */
+/* Static English text for a status code (never NULL).  No passage: diagnostics. */
 const char* rmsnorm_status_string(rmsnorm_status_t status);
 
 /*
- * rmsnorm_last_cuda_error -- the cudaError_t of the last CUDA runtime call of
+ * rmsnorm_last_cuda_error -- (no passage: diagnostics) the cudaError_t of the last CUDA runtime call of
  * this library that failed on the calling host thread (0 if none), and clears
  * it.  If msg != NULL and len > 0, writes "<name>: <description>" there
  * (truncated, NUL-terminated).  The library links the CUDA runtime

@@ -30,11 +30,16 @@
 extern "C" {
 #endif
 
-/* y = softmax(x) along the last axis, fp32 tensors. */
+/* y = softmax(x) along the last axis, fp32 tensors.  Defined by: page "A
+ * hackable Python ML compiler, part 2", the opening benchmark paragraph
+ * (softmax-style small reductions among the generated kernels' wins); the page
+ * prints no formula, so the definition above is the plain one. */
 rmsnorm_status_t rowsoftmax_fwd_f32(const float* x, float* y, int64_t rows, int64_t cols,
                                     rmsnorm_stream_t stream);
 
-/* The same for bfloat16 tensors (raw 16-bit patterns), fp32 arithmetic. */
+/* The same for bfloat16 tensors (raw 16-bit patterns), fp32 arithmetic; same
+ * passage (the page is fp32 only: the single output rounding is this library's
+ * reading). */
 rmsnorm_status_t rowsoftmax_fwd_bf16(const uint16_t* x, uint16_t* y, int64_t rows,
                                      int64_t cols, rmsnorm_stream_t stream);
 

@@ -1,76 +1,105 @@
-// k_page.cuh -- the schedule of the generated kernel in the compiler write-up
-// ("A hackable Python ML compiler, part 2": the Tile IR after stage_inputs and
-// the CUDA kernel it emits for torch.nn.RMSNorm(2048)), rebuilt from its
-// description as an in-library comparison point.  It is never chosen
-// automatically; it exists to measure what the other kernels' design choices buy.
+// k_page.cuh -- comparison kernel with the schedule of the compiler write-up
+// ("A hackable Python ML compiler, part 2"), rebuilt from the way the page
+// describes its lowering of torch.nn.RMSNorm(2048), not from the kernel text
+// it prints.  Never chosen automatically: it measures what the library's own
+// kernels gain over that schedule on the same GPU.
 //
-// The schedule, as the page describes it:
-//   - one CTA per row, 256 threads (Tile axes a0:256=THREAD, a1:rows=BLOCK);
-//   - stage_inputs: the whole row is copied once from global memory into
-//     shared memory, element by element (4-byte accesses, stride 256), then a
-//     barrier;
-//   - each thread sums the squares of its strided elements from shared memory;
-//   - a butterfly shuffle reduces each warp; lane 0 of each of the 8 warps
-//     writes its sum to shared memory; a tree halves the 8 partials in three
-//     levels (4, 2, 1) with a barrier per level; every thread reads slot 0;
-//   - rstd = rsqrt(sum * (1/H) + eps);
-//   - each thread normalises its strided elements from shared memory, reads
-//     the weight from global memory and stores, element by element.
-// Generalised only as far as needed to run on any H that fits shared memory
-// (the page hard-codes H = 2048 and has no tail) and on bf16 (widened on load).
+// What the page's schedule fixes, and how it is met here:
+//   - Tile IR: one CTA per row (the row axis bound to the grid), 256 threads
+//     on the hidden axis -> grid = rows, block = kPageThreads;
+//   - the stage_inputs pass: the input row is copied once into shared memory
+//     before any arithmetic, in element-sized (4-byte fp32) accesses strided
+//     by the thread count -> stage_row, then one barrier;
+//   - the reduce axis: every thread sums the squares of its strided elements
+//     of the staged copy -> sum_staged_squares;
+//   - the cooperative reduction: a shuffle butterfly inside each warp, the 8
+//     warp totals parked in shared memory and halved in a three-level tree
+//     with a barrier after the parking and after each level -> tree_total;
+//   - the epilogue: rsqrt of the mean plus eps, then (x * rstd) * w element
+//     by element from the staged copy, the weight read from global memory ->
+//     write_normalised_row.
+// Generalised only as far as the library's interface needs: any H whose fp32
+// copy fits shared memory (the page hard-codes H = 2048 with no tail), and
+// bf16 (widened when staged, rounded once when written).
 #pragma once
 #include "common.cuh"
 
 namespace rmsnorm {
 
 constexpr int kPageThreads = 256;
+constexpr int kPageWarps = kPageThreads / 32;
 
 template <typename T>
-__device__ __forceinline__ float load_elem(const T* p) {
+__device__ __forceinline__ float page_widen(T v) {
     if constexpr (sizeof(T) == 4) {
-        return *reinterpret_cast<const float*>(p);
+        return v;
     } else {
-        return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
+        return __bfloat162float(v);
     }
 }
 
 template <typename T>
-__device__ __forceinline__ void store_elem(T* p, float v) {
+__device__ __forceinline__ T page_narrow(float v) {
     if constexpr (sizeof(T) == 4) {
-        *reinterpret_cast<float*>(p) = v;
+        return v;
     } else {
-        *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
+        return __float2bfloat16_rn(v);
     }
+}
+
+// stage_inputs: the row, widened to fp32, into shared memory.
+template <typename T>
+__device__ __forceinline__ void stage_row(float* staged, const T* row, int n) {
+    for (int j = threadIdx.x; j < n; j += kPageThreads) staged[j] = page_widen(row[j]);
+}
+
+__device__ __forceinline__ float sum_staged_squares(const float* staged, int n) {
+    float acc = 0.f;
+    for (int j = threadIdx.x; j < n; j += kPageThreads) acc = fmaf(staged[j], staged[j], acc);
+    return acc;
+}
+
+// Halving tree over `slots` (kWidth * 2 entries): each level folds the upper
+// half onto the lower half and ends in a block barrier.
+template <int kWidth>
+__device__ __forceinline__ void halve_slots(float* slots) {
+    if constexpr (kWidth >= 1) {
+        if (threadIdx.x < kWidth) slots[threadIdx.x] += slots[threadIdx.x + kWidth];
+        __syncthreads();
+        halve_slots<kWidth / 2>(slots);
+    }
+}
+
+// Block total of `v`: warp butterfly, one slot per warp, barrier, tree.
+__device__ __forceinline__ float tree_total(float v, float* slots) {
+    v = warp_allreduce_sum(v);
+    if ((threadIdx.x & 31) == 0) slots[threadIdx.x >> 5] = v;
+    __syncthreads();
+    halve_slots<kPageWarps / 2>(slots);
+    return slots[0];
+}
+
+template <typename T>
+__device__ __forceinline__ void write_normalised_row(T* out, const float* staged, const T* w,
+                                                     int n, float rstd) {
+    for (int j = threadIdx.x; j < n; j += kPageThreads)
+        out[j] = page_narrow<T>((staged[j] * rstd) * page_widen(w[j]));
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kPageThreads) page_kernel(const Params p) {
-    extern __shared__ float x_smem[];            // the staged row (fp32)
-    __shared__ float acc_smem[kPageThreads / 32];
-    const int a0 = threadIdx.x;
-    const int lane = a0 & 31, warp = a0 >> 5;
-    const int H = p.hidden;
-    const int64_t row = blockIdx.x;
-    const T* x = static_cast<const T*>(p.x) + row * H;
-    const T* w = static_cast<const T*>(p.w);
-    T* y = static_cast<T*>(p.y) + row * H;
+    extern __shared__ float staged[];            // the whole row, fp32
+    __shared__ float slots[kPageWarps];
+    const int n = p.hidden;
+    const int64_t r = blockIdx.x;
+    const T* row = static_cast<const T*>(p.x) + r * n;
+    T* out = static_cast<T*>(p.y) + r * n;
 
-    for (int j = a0; j < H; j += kPageThreads) x_smem[j] = load_elem(x + j);
+    stage_row(staged, row, n);
     __syncthreads();
-
-    float acc = 0.f;
-    for (int j = a0; j < H; j += kPageThreads) acc += x_smem[j] * x_smem[j];
-    acc = warp_allreduce_sum(acc);
-    if (lane == 0) acc_smem[warp] = acc;
-    __syncthreads();
-    for (int s = kPageThreads / 64; s > 0; s >>= 1) {
-        if (warp < s && lane == 0) acc_smem[warp] = acc_smem[warp] + acc_smem[warp + s];
-        __syncthreads();
-    }
-    const float rstd = rsqrtf(acc_smem[0] * p.inv_hidden + p.eps);
-
-    for (int j = a0; j < H; j += kPageThreads)
-        store_elem(y + j, (x_smem[j] * rstd) * load_elem(w + j));
+    const float total = tree_total(sum_staged_squares(staged, n), slots);
+    const float rstd = rsqrtf(fmaf(total, p.inv_hidden, p.eps));
+    write_normalised_row(out, staged, static_cast<const T*>(p.w), n, rstd);
 }
 
 }  // namespace rmsnorm

@@ -68,6 +68,34 @@ __device__ __forceinline__ float row_exp(float v, float c) {
     return row_exp_arg<T>(fmaf(v, kLog2e, c));
 }
 
+// Whether a row (or slice) whose maximum is m may form its exponent
+// arguments as v*log2e + c with the one rounded offset c = bias - m*log2e.
+// That offset's rounding (half an ulp of |m|*log2e) is a factor common to
+// the row, so it cancels in e / sum -- but only while it is small: for |m|
+// near 1e10 it is hundreds, every exponential of the row underflows and the
+// row turns into 0/0; for |m| above FLT_MAX / log2(e) the offset itself
+// overflows.  |m| < 2^21 keeps it below 2^-4.  Other rows (and rows whose
+// maximum is not finite) take the exact form (v - m)*log2e + bias: for every
+// element that can contribute (v within about 130 of m) the difference v - m
+// is exact (Sterbenz), so that form has the single rounding of the fused
+// one, for one more instruction per element.
+constexpr float kRowExpOffsetMax = 2097152.0f;   // 2^21
+
+__device__ __forceinline__ bool row_exp_offset_ok(float m) {
+    return fabsf(m) < kRowExpOffsetMax;
+}
+
+// One exponential with the row's offset: F = the fused form (c), else the
+// exact form relative to the maximum m.
+template <typename T, bool F>
+__device__ __forceinline__ float row_exp_sel(float v, float c, float m) {
+    if constexpr (F) {
+        return row_exp_arg<T>(fmaf(v, kLog2e, c));
+    } else {
+        return row_exp_arg<T>(fmaf(v - m, kLog2e, row_exp_bias<T>()));
+    }
+}
+
 // A split row's slices each form their exponentials with their own offset
 // c = bias - m*log2(e), m the slice's maximum, rounded to fp32.  That rounding
 // (up to half an ulp of |m|*log2(e): 7.6e-6 for |m| near 100) is a factor
@@ -180,13 +208,25 @@ struct RowPairs {
         fold_max(v, mk, mw);
         widen(v);
     }
-    // e = 2^(e*log2e + c) in place; the sums take the exponentials.
-    __device__ __forceinline__ void exp(float c, Sums& s) {
-        const uint64_t l2 = pack_x2(kLog2e, kLog2e), c2 = pack_x2(c, c);
+    // The exponent arguments of pair j: e*log2e + c (F), or (e - m)*log2e +
+    // bias (the exact form, see row_exp_offset_ok).
+    template <bool F>
+    __device__ __forceinline__ void args(int j, float c, float m, float& a0, float& a1) const {
+        const uint64_t l2 = pack_x2(kLog2e, kLog2e);
+        if constexpr (F) {
+            unpack_x2(fma_x2(e[j], l2, pack_x2(c, c)), a0, a1);
+        } else {
+            const float b = row_exp_bias<T>();
+            unpack_x2(fma_x2(add_x2(e[j], pack_x2(-m, -m)), l2, pack_x2(b, b)), a0, a1);
+        }
+    }
+    // e = 2^(argument) in place; the sums take the exponentials.
+    template <bool F = true>
+    __device__ __forceinline__ void exp(float c, Sums& s, float m = 0.f) {
 #pragma unroll
         for (int j = 0; j < kPairs; ++j) {
             float a0, a1;
-            unpack_x2(fma_x2(e[j], l2, c2), a0, a1);
+            args<F>(j, c, m, a0, a1);
             e[j] = pack_x2(row_exp_arg<T>(a0), row_exp_arg<T>(a1));
             s.s2[j & 1] = add_x2(s.s2[j & 1], e[j]);
         }
@@ -199,14 +239,15 @@ struct RowPairs {
         for (int j = 0; j < kPairs; ++j) unpack_x2(mul_x2(e[j], inv2), o[2 * j], o[2 * j + 1]);
         return pack<T, VB>(o);
     }
-    // The outputs 2^(e*log2e + c) * inv of widened inputs, packed for the store.
-    __device__ __forceinline__ Vec<VB> exp_scaled(float c, float inv) const {
-        const uint64_t l2 = pack_x2(kLog2e, kLog2e), c2 = pack_x2(c, c), inv2 = pack_x2(inv, inv);
+    // The outputs 2^(argument) * inv of widened inputs, packed for the store.
+    template <bool F = true>
+    __device__ __forceinline__ Vec<VB> exp_scaled(float c, float inv, float m = 0.f) const {
+        const uint64_t inv2 = pack_x2(inv, inv);
         float o[kElems];
 #pragma unroll
         for (int j = 0; j < kPairs; ++j) {
             float a0, a1;
-            unpack_x2(fma_x2(e[j], l2, c2), a0, a1);
+            args<F>(j, c, m, a0, a1);
             unpack_x2(mul_x2(pack_x2(row_exp_arg<T>(a0), row_exp_arg<T>(a1)), inv2), o[2 * j],
                       o[2 * j + 1]);
         }
@@ -238,10 +279,11 @@ struct RowScalars {
             mk[k & 3] = fmaxf(mk[k & 3], e[k]);
         }
     }
-    __device__ __forceinline__ void exp(float c, Sums& s) {
+    template <bool F = true>
+    __device__ __forceinline__ void exp(float c, Sums& s, float m = 0.f) {
 #pragma unroll
         for (int k = 0; k < kElems; ++k) {
-            e[k] = row_exp<T>(e[k], c);
+            e[k] = row_exp_sel<T, F>(e[k], c, m);
             s.sk[k & 3] += e[k];
         }
     }
@@ -251,10 +293,11 @@ struct RowScalars {
         for (int k = 0; k < kElems; ++k) o[k] = e[k] * inv;
         return pack<T, VB>(o);
     }
-    __device__ __forceinline__ Vec<VB> exp_scaled(float c, float inv) const {
+    template <bool F = true>
+    __device__ __forceinline__ Vec<VB> exp_scaled(float c, float inv, float m = 0.f) const {
         float o[kElems];
 #pragma unroll
-        for (int k = 0; k < kElems; ++k) o[k] = row_exp<T>(e[k], c) * inv;
+        for (int k = 0; k < kElems; ++k) o[k] = row_exp_sel<T, F>(e[k], c, m) * inv;
         return pack<T, VB>(o);
     }
 };
@@ -416,12 +459,19 @@ softmax_rowreg_kernel(const Params p) {
         }
         // exponentials and their sum, relative to this CTA's maximum when a
         // cluster splits the row (a slice of -inf keeps -inf: exp(-inf) = 0)
+        const bool fast = row_exp_offset_ok(m) || (CL && m == -INFINITY);
         const float c = (CL && m == -INFINITY) ? -INFINITY : row_exp_bias<T>() - m * kLog2e;
         typename RowVec<T, VB>::Sums sums;
         if (row_ok) {
+            if (fast) {
 #pragma unroll
-            for (int i = 0; i < NV; ++i)
-                if (valid[i]) e[i].exp(c, sums);
+                for (int i = 0; i < NV; ++i)
+                    if (valid[i]) e[i].exp(c, sums);
+            } else {
+#pragma unroll
+                for (int i = 0; i < NV; ++i)
+                    if (valid[i]) e[i].template exp<false>(c, sums, m);
+            }
         }
         const float sl = sums.total();
         float s = G >= 32 ? warp_allreduce_sum(sl) : group_allreduce_sum(sl, G);
@@ -434,7 +484,7 @@ softmax_rowreg_kernel(const Params p) {
         float inv = 1.0f / s;
         if (CL) {
             // one exchange of the (maximum, sum) pair gives the row's
-            const float corr = slice_offset_correction<T>(m, c);
+            const float corr = fast ? slice_offset_correction<T>(m, c) : 1.0f;
             float M, S;
             const bool ok =
                 cluster_pair_allreduce(&ex, m, s * corr, ncta, rank, it, p, &M, &S, tid);
@@ -599,11 +649,18 @@ __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kerne
         for (int k = 0; k < NW; ++k) m = fmaxf(m, red[b * 16 + k]);
         // exponentials relative to this CTA's maximum: the whole row's when
         // the row is not split; a slice of -inf keeps -inf (exp(-inf) = 0)
+        const bool fast = row_exp_offset_ok(m) || (CL && m == -INFINITY);
         const float c = (CL && m == -INFINITY) ? -INFINITY : row_exp_bias<T>() - m * kLog2e;
         typename RowVec<T, 16>::Sums sums;
+        if (fast) {
 #pragma unroll
-        for (int i = 0; i < NV; ++i)
-            if (valid[i]) e[i].exp(c, sums);
+            for (int i = 0; i < NV; ++i)
+                if (valid[i]) e[i].exp(c, sums);
+        } else {
+#pragma unroll
+            for (int i = 0; i < NV; ++i)
+                if (valid[i]) e[i].template exp<false>(c, sums, m);
+        }
         float sum = warp_allreduce_sum(sums.total());
         if (lane == 0) red[32 + b * 16 + warp] = sum;
         __syncthreads();
@@ -611,7 +668,7 @@ __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kerne
         for (int k = 0; k < NW; ++k) sum += red[32 + b * 16 + k];
         float inv = 1.0f / sum;
         if (CL) {
-            const float corr = slice_offset_correction<T>(m, c);
+            const float corr = fast ? slice_offset_correction<T>(m, c) : 1.0f;
             float M, S;
             const bool cok =
                 cluster_pair_allreduce(ex, m, sum * corr, ncta, rank, it, p, &M, &S, tid);
@@ -677,28 +734,33 @@ __global__ void __launch_bounds__(kSoftmaxWideThreads) softmax_threepass_kernel(
         m = -INFINITY;
         for (int k = 0; k < nwarps; ++k) m = fmaxf(m, red[0][b][k]);
         const float c = row_exp_bias<T>() - m * kLog2e;
+        const bool fast = row_exp_offset_ok(m);
 
-        float sl;
-        if constexpr (kPairs) {
-            PairSums sums;
-            for (int v = tid; v < p.nvec; v += nthr) {
-                RV e;
-                e.widen(ld_plain<VB>(src + static_cast<int64_t>(v) * VB));
-                e.exp(c, sums);
-            }
-            sl = sums.total();
-        } else {
-            float s0 = 0.f, s1 = 0.f;
-            for (int v = tid; v < p.nvec; v += nthr) {
-                const Vec<VB> xv = ld_plain<VB>(src + static_cast<int64_t>(v) * VB);
-#pragma unroll
-                for (int k = 0; k < EPV; ++k) {
-                    const float ev = row_exp<T>(get<T, VB>(xv, k), c);
-                    if (k & 1) s1 += ev; else s0 += ev;
+        // pass 2: the sum of exponentials (F: fused offset, else exact form)
+        auto pass2 = [&](auto ftag) -> float {
+            constexpr bool F = decltype(ftag)::value;
+            if constexpr (kPairs) {
+                PairSums sums;
+                for (int v = tid; v < p.nvec; v += nthr) {
+                    RV e;
+                    e.widen(ld_plain<VB>(src + static_cast<int64_t>(v) * VB));
+                    e.template exp<F>(c, sums, m);
                 }
+                return sums.total();
+            } else {
+                float s0 = 0.f, s1 = 0.f;
+                for (int v = tid; v < p.nvec; v += nthr) {
+                    const Vec<VB> xv = ld_plain<VB>(src + static_cast<int64_t>(v) * VB);
+#pragma unroll
+                    for (int k = 0; k < EPV; ++k) {
+                        const float ev = row_exp_sel<T, F>(get<T, VB>(xv, k), c, m);
+                        if (k & 1) s1 += ev; else s0 += ev;
+                    }
+                }
+                return s0 + s1;
             }
-            sl = s0 + s1;
-        }
+        };
+        const float sl = fast ? pass2(std::true_type{}) : pass2(std::false_type{});
         float s = warp_allreduce_sum(sl);
         if (lane == 0) red[1][b][warp] = s;
         __syncthreads();
@@ -706,13 +768,18 @@ __global__ void __launch_bounds__(kSoftmaxWideThreads) softmax_threepass_kernel(
         for (int k = 0; k < nwarps; ++k) s += red[1][b][k];
         const float inv = 1.0f / s;
 
+        // pass 3: the outputs
         char* dst = yb + row * row_bytes;
-        for (int v = tid; v < p.nvec; v += nthr) {
-            const int64_t off = static_cast<int64_t>(v) * VB;
-            RV e;
-            e.widen(ld_stream<VB>(src + off));
-            st_stream<VB>(dst + off, e.exp_scaled(c, inv));
-        }
+        auto pass3 = [&](auto ftag) {
+            constexpr bool F = decltype(ftag)::value;
+            for (int v = tid; v < p.nvec; v += nthr) {
+                const int64_t off = static_cast<int64_t>(v) * VB;
+                RV e;
+                e.widen(ld_stream<VB>(src + off));
+                st_stream<VB>(dst + off, e.template exp_scaled<F>(c, inv, m));
+            }
+        };
+        if (fast) pass3(std::true_type{}); else pass3(std::false_type{});
     }
 }
 

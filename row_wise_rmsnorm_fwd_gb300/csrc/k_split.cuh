@@ -213,37 +213,45 @@ __global__ void __launch_bounds__(kSplitThreads, 1) softmax_threepass_cluster_ke
         for (int k = 0; k < nwarps; ++k) m = fmaxf(m, red[0][b][k]);
         // pass 2, backward: exponentials relative to the slice's maximum (a
         // slice of -inf keeps -inf: exp(-inf) = 0)
+        // (the fused offset for slices of moderate maximum, else the exact
+        // form: row_exp_offset_ok)
+        const bool fast = row_exp_offset_ok(m) || m == -INFINITY;
         const float c = m == -INFINITY ? -INFINITY : row_exp_bias<T>() - m * kLog2e;
-        float sl = 0.f;
-        for (uint32_t q = nblocks; q-- > 0;) {
-            const uint32_t jb = q * B;
-            const uint32_t je = J - jb > B ? jb + B : J;
-            typename RV::Sums sums;
-            float s0 = 0.f, s1 = 0.f;
-            for (uint32_t j0 = jb; j0 < je; j0 += U) {
-                Vec<VB> xv[U];
+        auto pass2 = [&](auto ftag) -> float {
+            constexpr bool F = decltype(ftag)::value;
+            float sl = 0.f;
+            for (uint32_t q = nblocks; q-- > 0;) {
+                const uint32_t jb = q * B;
+                const uint32_t je = J - jb > B ? jb + B : J;
+                typename RV::Sums sums;
+                float s0 = 0.f, s1 = 0.f;
+                for (uint32_t j0 = jb; j0 < je; j0 += U) {
+                    Vec<VB> xv[U];
 #pragma unroll
-                for (uint32_t u = 0; u < U; ++u)
-                    if (j0 + u < je) xv[u] = ld_plain<VB>(src + (j0 + u) * stride);
+                    for (uint32_t u = 0; u < U; ++u)
+                        if (j0 + u < je) xv[u] = ld_plain<VB>(src + (j0 + u) * stride);
 #pragma unroll
-                for (uint32_t u = 0; u < U; ++u) {
-                    if (j0 + u < je) {
-                        if constexpr (kPairs) {
-                            RV e;
-                            e.widen(xv[u]);
-                            e.exp(c, sums);
-                        } else {
+                    for (uint32_t u = 0; u < U; ++u) {
+                        if (j0 + u < je) {
+                            if constexpr (kPairs) {
+                                RV e;
+                                e.widen(xv[u]);
+                                e.template exp<F>(c, sums, m);
+                            } else {
 #pragma unroll
-                            for (int k = 0; k < EPV; ++k) {
-                                const float ev = row_exp<T>(get<T, VB>(xv[u], k), c);
-                                if (k & 1) s1 += ev; else s0 += ev;
+                                for (int k = 0; k < EPV; ++k) {
+                                    const float ev = row_exp_sel<T, F>(get<T, VB>(xv[u], k), c, m);
+                                    if (k & 1) s1 += ev; else s0 += ev;
+                                }
                             }
                         }
                     }
                 }
+                if constexpr (kPairs) sl += sums.total(); else sl += s0 + s1;
             }
-            if constexpr (kPairs) sl += sums.total(); else sl += s0 + s1;
-        }
+            return sl;
+        };
+        const float sl = fast ? pass2(std::true_type{}) : pass2(std::false_type{});
         float s = warp_allreduce_sum(sl);
         if (lane == 0) red[1][b][warp] = s;
         __syncthreads();
@@ -253,29 +261,35 @@ __global__ void __launch_bounds__(kSplitThreads, 1) softmax_threepass_cluster_ke
         // sum and pass 3's offset are both corrected for the rounding of
         // their offsets (slice_offset_correction)
         float M, S;
-        const bool ok = cluster_pair_allreduce(&ex, m, s * slice_offset_correction<T>(m, c),
-                                               p.cluster, rank, it, p, &M, &S,
+        const float corr = fast ? slice_offset_correction<T>(m, c) : 1.0f;
+        const bool ok = cluster_pair_allreduce(&ex, m, s * corr, p.cluster, rank, it, p, &M, &S,
                                                static_cast<int>(tid));
         if (__syncthreads_or(!ok)) break;   // uniform: stop, then leave cleanly
+        const bool fast3 = row_exp_offset_ok(M);
         const float c3 = row_exp_bias<T>() - M * kLog2e;
-        const float inv = slice_offset_correction<T>(M, c3) / S;
+        const float inv = (fast3 ? slice_offset_correction<T>(M, c3) : 1.0f) / S;
 
         // pass 3, forward: exp(x - M) / S
         char* dst = yb + soff;
-        for (uint32_t j0 = 0; j0 < J; j0 += U2) {
-            Vec<VB> xv[U2];
+        auto pass3 = [&](auto ftag) {
+            constexpr bool F = decltype(ftag)::value;
+            for (uint32_t j0 = 0; j0 < J; j0 += U2) {
+                Vec<VB> xv[U2];
 #pragma unroll
-            for (uint32_t u = 0; u < U2; ++u)
-                if (j0 + u < J) xv[u] = ld_stream<VB>(src + (j0 + u) * stride);
+                for (uint32_t u = 0; u < U2; ++u)
+                    if (j0 + u < J) xv[u] = ld_stream<VB>(src + (j0 + u) * stride);
 #pragma unroll
-            for (uint32_t u = 0; u < U2; ++u) {
-                if (j0 + u < J) {
-                    RV e;
-                    e.widen(xv[u]);
-                    st_stream<VB>(dst + (j0 + u) * stride, e.exp_scaled(c3, inv));
+                for (uint32_t u = 0; u < U2; ++u) {
+                    if (j0 + u < J) {
+                        RV e;
+                        e.widen(xv[u]);
+                        st_stream<VB>(dst + (j0 + u) * stride,
+                                      e.template exp_scaled<F>(c3, inv, M));
+                    }
                 }
             }
-        }
+        };
+        if (fast3) pass3(std::true_type{}); else pass3(std::false_type{});
     }
     // Keep this CTA's shared memory alive until every peer is done with it.
     cluster_sync_all();

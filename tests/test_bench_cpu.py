@@ -67,3 +67,32 @@ def test_committed_profiles_parse():
         t = bench.profiled_traffic(workload, kernel)
         assert t is None or t > 0
     assert found >= 6
+
+
+def _args(**kw):
+    import argparse
+    base = dict(workload="c5a", rows=0, secondary=None, path="auto", cluster=0, grid=0,
+                threads=0, chunk=0, stages=0, epilogue="none")
+    base.update(kw)
+    return argparse.Namespace(**base)
+
+
+def test_secondary_workloads_only_on_the_default_run():
+    from row_wise_rmsnorm_fwd_gb300 import workloads
+    names = bench.secondary_names(_args())
+    assert names == list(bench.SECONDARY_DEFAULT)
+    assert {"c4", "c5b"} <= set(names)
+    assert all(n in workloads.WORKLOADS for n in names)
+    assert bench.secondary_names(_args(workload="c4")) == []
+    assert bench.secondary_names(_args(rows=1024)) == []
+    assert bench.secondary_names(_args(path="twopass")) == []
+    assert bench.secondary_names(_args(secondary="none")) == []
+    assert bench.secondary_names(_args(workload="c1", secondary="c4,c5b")) == ["c4", "c5b"]
+
+
+def test_roofline_block_labels_the_copy_peak_and_the_nominal_fraction():
+    r = bench.roofline_block(6000.0, 6768.8, "measured", None)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["frac"] - 6000.0 / 6768.8) < 1e-12
+    assert abs(r["frac_of_nominal"] - 6000.0 / bench.NOMINAL_HBM_GBS) < 1e-12
+    assert "copy peak" in r["peak_source"]

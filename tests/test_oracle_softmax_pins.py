@@ -97,3 +97,28 @@ def test_f32_and_bf16_entries():
     y64, y16 = oracle.rowsoftmax_bf16(bits)
     np.testing.assert_array_equal(y64, oracle.rowsoftmax_f64(xb.double().numpy()))
     np.testing.assert_array_equal(y16, oracle.f64_to_bf16(y64))
+
+
+def test_large_magnitude_rows_closed_forms():
+    """Rows far from zero: softmax depends only on differences, so 2^24 + k
+    (exact in binary32 and binary64 for small integers k) gives softmax(k);
+    entries near +-FLT_MAX give 1/count at the maxima and exact zeros
+    elsewhere (their differences, up to 6.8e38, underflow exp); two equal
+    maxima of any magnitude share 1/2 each."""
+    k = np.array([0.0, -1.0, -2.0, -3.0])
+    e = np.exp(k)
+    y = oracle.rowsoftmax_f32(np.array([2.0 ** 24 + k], dtype=np.float32))
+    np.testing.assert_allclose(y[0], e / e.sum(), rtol=1e-15)
+    fmax = float(np.finfo(np.float32).max)
+    x = np.array([[fmax, -fmax, fmax, 0.0],
+                  [-fmax, -fmax, -3.0e38, -fmax],
+                  [1.0e10, 1.0e10 - 1024.0, -1.0e10, 1.0e10]], dtype=np.float32)
+    y = oracle.rowsoftmax_f32(x)
+    np.testing.assert_array_equal(y[0], [0.5, 0.0, 0.5, 0.0])
+    np.testing.assert_array_equal(y[1], [0.0, 0.0, 1.0, 0.0])
+    np.testing.assert_array_equal(y[2], [0.5, 0.0, 0.0, 0.5])
+    # bf16: the largest finite bf16 twice -> 0.5 each (bf16 0x3F00)
+    bits = np.array([[0x7F7F, 0x7F7F, 0xFF7F]], dtype=np.uint16)
+    y64, y16 = oracle.rowsoftmax_bf16(bits)
+    np.testing.assert_array_equal(y64[0], [0.5, 0.5, 0.0])
+    np.testing.assert_array_equal(y16[0], [0x3F00, 0x3F00, 0x0000])

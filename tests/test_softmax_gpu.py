@@ -112,6 +112,49 @@ def test_cluster_special_values(dtype, path):
     compare(y, ref_for(x), f"{path} cluster special {dtype}")
 
 
+def large_magnitude_rows(cols, seed):
+    """Rows whose maximum is far from zero, where an exponent offset
+    bias - m*log2(e) rounded to fp32 is off by more than exp2 can absorb
+    (hundreds at |m| = 1e10) or overflows (|m| > FLT_MAX / log2(e)):
+    0: 2^22 + multiples of 1/2 (exact in fp32; real spread of exponentials),
+    1: 1e10 + N(0, 3000), 2: -1e10 + N(0, 3000), 3: uniform in [3e38,
+    3.38e38], 4: its negation, 5: a mix of both, 6: 3e6 + N(0, 4) (just above
+    the fused form's bound), 7: 2e6 + N(0, 4) (just below it)."""
+    g = torch.Generator().manual_seed(seed)
+    n = lambda std: torch.randn(cols, generator=g, dtype=torch.float64) * std  # noqa: E731
+    u = torch.rand(cols, generator=g, dtype=torch.float64)
+    rows = [
+        2.0 ** 22 + torch.round(n(4.0) * 2) / 2,
+        1e10 + n(3000.0),
+        -1e10 + n(3000.0),
+        3.0e38 + u * 0.38e38,
+        -(3.0e38 + u * 0.38e38),
+        torch.where(torch.rand(cols, generator=g) < 0.5, 1.0, -1.0).double() * (3.0e38 + u * 0.38e38),
+        3e6 + n(4.0),
+        2e6 + n(4.0),
+    ]
+    return torch.stack(rows).float()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("path,cluster,cols", [
+    ("auto", 0, 4096), ("auto", 0, 32000), ("rowreg", 0, 4096), ("staged", 0, 32000),
+    ("cluster", 4, 65536), ("twopass", 0, 65536), ("twopass", 4, 65536),
+    ("staged", 2, 128256), ("staged", 4, 128256)])
+def test_large_magnitude_rows(dtype, path, cluster, cols):
+    """Rows with maxima from 2e6 to 3.38e38 (either sign) through every
+    softmax kernel: finite results equal to the oracle's, no NaN rows."""
+    x = large_magnitude_rows(cols, 50 + cols).to(DT[dtype])
+    try:
+        y = run(x.cuda(), **({} if path == "auto" else {"path": path, "cluster": cluster}))
+    except binding.RmsnormError as e:
+        if e.status == binding.RMSNORM_ERR_UNSUPPORTED:
+            pytest.skip("path cannot serve this shape")
+        raise
+    assert not torch.isnan(y.float()).any()
+    compare(y, ref_for(x), f"large magnitudes {path} C={cluster} {dtype} cols={cols}")
+
+
 MAX_COLS = (1 << 31) - 1      # the widest row the ABI accepts
 
 
