@@ -384,10 +384,11 @@ def run_ours(args, wl):
     handle = stream.cuda_stream
     options = None
     if softmax:
-        staged = args.path == "staged"
+        staged = args.path in ("staged", "stream")
         options = binding.make_options(
-            path=args.path if args.path in ("rowreg", "twopass", "cluster", "staged") else "auto",
-            cluster=args.cluster if args.path in ("cluster", "staged", "twopass") else 0,
+            path=args.path if args.path in ("rowreg", "twopass", "cluster", "staged", "stream")
+            else "auto",
+            cluster=args.cluster if args.path in ("cluster", "staged", "twopass", "stream") else 0,
             grid=args.grid, threads=args.threads,
             chunk_bytes=args.chunk if staged else 0, stages=args.stages if staged else 0)
         dt_code = binding.RMSNORM_DTYPE_BF16 if wl.dtype == "bf16" else binding.RMSNORM_DTYPE_F32
@@ -696,7 +697,8 @@ def main():
     ap.add_argument("--rows", type=int, default=0,
                     help="use only this many rows of the workload (small profiling cases)")
     ap.add_argument("--path", default="auto",
-                    choices=["auto", "rowreg", "staged", "cluster", "twopass", "page", "ringreg"],
+                    choices=["auto", "rowreg", "staged", "cluster", "twopass", "page", "ringreg",
+                             "stream"],
                     help="force a kernel family through rmsnorm_fwd_ex (evidence runs)")
     ap.add_argument("--cluster", type=int, default=0)
     ap.add_argument("--grid", type=int, default=0, help="force the CTA count")

@@ -78,12 +78,16 @@ typedef enum {
                                   schedule (one 256-thread CTA per row, whole row staged
                                   in shared memory, 4-byte accesses, 3-level tree); rows
                                   up to the shared-memory limit (about 56K elements) */
-    RMSNORM_PATH_RINGREG = 6   /* wide rows (up to 128 KB, 16-byte aligned x, w, y and
+    RMSNORM_PATH_RINGREG = 6,  /* wide rows (up to 128 KB, 16-byte aligned x, w, y and
                                   pitch): rows streamed through a shared-memory ring by
                                   bulk copies and held in registers, the weight row in
                                   shared memory; opt->threads = consumer threads,
                                   opt->chunk_bytes = 2 or 4 vectors per consumer thread
                                   (x 16 bytes x threads), opt->stages = ring slots */
+    RMSNORM_PATH_STREAM = 7    /* row softmax only (rowsoftmax_fwd_ex): each row streamed
+                                  twice through a shared-memory ring by bulk copies, the
+                                  first read from DRAM (online maximum and sum), the second
+                                  normally from L2 (outputs); one CTA per SM, no cluster */
 } rmsnorm_path_t;
 
 /* Options for rmsnorm_fwd_ex / rmsnorm_plan.  Zero-initialise, then set what you

@@ -140,18 +140,23 @@ __device__ __forceinline__ bool ring_issue_next(const Params& p, const SlotRing&
 // then wait (bounded) until every copy it issued has landed, so that no copy
 // is in flight when the CTA leaves.  A refill waits for its slot's release;
 // if that wait runs out the status word records `site` and no more copies
-// are issued.
+// are issued.  `passes` > 1 streams each row that many times in a row (the
+// row's chunks again after its last one), the first time with `policy`, the
+// later ones with `policy2`.
 __device__ __forceinline__ void ring_produce(const Params& p, const SlotRing& r, int64_t unit,
                                              int64_t nunits, int64_t row_bytes, int64_t sbeg,
-                                             uint64_t policy, unsigned site) {
+                                             uint64_t policy, unsigned site, int passes = 1,
+                                             uint64_t policy2 = 0) {
     const char* xb = static_cast<const char*>(p.x);
     int64_t seq = 0;       // chunks issued so far
     int slot = 0;          // seq % S
     uint32_t lap = 0;      // (seq / S) & 1
     bool reuse = false;    // seq >= S: the slot held an earlier chunk
     bool abort = false;
-    for (int64_t rb = unit; rb < p.rows && !abort; rb += nunits) {
+    for (int64_t rb = unit; rb < p.rows && !abort; rb += nunits)
+    for (int ps = 0; ps < passes && !abort; ++ps) {
         const char* src = xb + rb * row_bytes + sbeg;
+        const uint64_t pol = ps == 0 ? policy : policy2;
         for (int k = 0; k < r.NCH; ++k, ++seq) {
             if (reuse && !mbar_wait_bounded<false>(smem_addr(&r.empty[slot]), lap ^ 1u,
                                                    p.timeout_ns)) {
@@ -175,7 +180,7 @@ __device__ __forceinline__ void ring_produce(const Params& p, const SlotRing& r,
                     mbar_arrive_expect_tx(fb, static_cast<uint32_t>(len));
                     bulk_g2s(smem_addr(r.slots + static_cast<int64_t>(slot) * r.CB),
                              src + static_cast<int64_t>(k) * r.CB, static_cast<uint32_t>(len),
-                             fb, policy);
+                             fb, pol);
                 } else {
                     mbar_arrive(fb);
                 }

@@ -220,6 +220,31 @@ struct RowPairs {
             unpack_x2(fma_x2(add_x2(e[j], pack_x2(-m, -m)), l2, pack_x2(b, b)), a0, a1);
         }
     }
+    // e = 2^((e - ms)*log2e + cs) in place, the sums take the exponentials:
+    // one loop for both forms of the argument, (ms, cs) = (0, c) or (m, bias).
+    __device__ __forceinline__ void exp_shift(float ms, float cs, Sums& s) {
+        const uint64_t l2 = pack_x2(kLog2e, kLog2e), n2 = pack_x2(-ms, -ms), c2 = pack_x2(cs, cs);
+#pragma unroll
+        for (int j = 0; j < kPairs; ++j) {
+            float a0, a1;
+            unpack_x2(fma_x2(add_x2(e[j], n2), l2, c2), a0, a1);
+            e[j] = pack_x2(row_exp_arg<T>(a0), row_exp_arg<T>(a1));
+            s.s2[j & 1] = add_x2(s.s2[j & 1], e[j]);
+        }
+    }
+    __device__ __forceinline__ Vec<VB> exp_shift_scaled(float ms, float cs, float inv) const {
+        const uint64_t l2 = pack_x2(kLog2e, kLog2e), n2 = pack_x2(-ms, -ms), c2 = pack_x2(cs, cs);
+        const uint64_t inv2 = pack_x2(inv, inv);
+        float o[kElems];
+#pragma unroll
+        for (int j = 0; j < kPairs; ++j) {
+            float a0, a1;
+            unpack_x2(fma_x2(add_x2(e[j], n2), l2, c2), a0, a1);
+            unpack_x2(mul_x2(pack_x2(row_exp_arg<T>(a0), row_exp_arg<T>(a1)), inv2), o[2 * j],
+                      o[2 * j + 1]);
+        }
+        return pack<T, VB>(o);
+    }
     // e = 2^(argument) in place; the sums take the exponentials.
     template <bool F = true>
     __device__ __forceinline__ void exp(float c, Sums& s, float m = 0.f) {
@@ -298,6 +323,12 @@ struct RowScalars {
         float o[kElems];
 #pragma unroll
         for (int k = 0; k < kElems; ++k) o[k] = row_exp_sel<T, F>(e[k], c, m) * inv;
+        return pack<T, VB>(o);
+    }
+    __device__ __forceinline__ Vec<VB> exp_shift_scaled(float ms, float cs, float inv) const {
+        float o[kElems];
+#pragma unroll
+        for (int k = 0; k < kElems; ++k) o[k] = row_exp_arg<T>(fmaf(e[k] - ms, kLog2e, cs)) * inv;
         return pack<T, VB>(o);
     }
 };

@@ -214,44 +214,41 @@ __global__ void __launch_bounds__(kSplitThreads, 1) softmax_threepass_cluster_ke
         // pass 2, backward: exponentials relative to the slice's maximum (a
         // slice of -inf keeps -inf: exp(-inf) = 0)
         // (the fused offset for slices of moderate maximum, else the exact
-        // form: row_exp_offset_ok)
+        // form: row_exp_offset_ok), both as (x - ms)*log2e + cs in one loop
         const bool fast = row_exp_offset_ok(m) || m == -INFINITY;
         const float c = m == -INFINITY ? -INFINITY : row_exp_bias<T>() - m * kLog2e;
-        auto pass2 = [&](auto ftag) -> float {
-            constexpr bool F = decltype(ftag)::value;
-            float sl = 0.f;
-            for (uint32_t q = nblocks; q-- > 0;) {
-                const uint32_t jb = q * B;
-                const uint32_t je = J - jb > B ? jb + B : J;
-                typename RV::Sums sums;
-                float s0 = 0.f, s1 = 0.f;
-                for (uint32_t j0 = jb; j0 < je; j0 += U) {
-                    Vec<VB> xv[U];
+        const float ms = fast ? 0.f : m, cs = fast ? c : row_exp_bias<T>();
+        float sl = 0.f;
+        for (uint32_t q = nblocks; q-- > 0;) {
+            const uint32_t jb = q * B;
+            const uint32_t je = J - jb > B ? jb + B : J;
+            typename RV::Sums sums;
+            float s0 = 0.f, s1 = 0.f;
+            for (uint32_t j0 = jb; j0 < je; j0 += U) {
+                Vec<VB> xv[U];
 #pragma unroll
-                    for (uint32_t u = 0; u < U; ++u)
-                        if (j0 + u < je) xv[u] = ld_plain<VB>(src + (j0 + u) * stride);
+                for (uint32_t u = 0; u < U; ++u)
+                    if (j0 + u < je) xv[u] = ld_plain<VB>(src + (j0 + u) * stride);
 #pragma unroll
-                    for (uint32_t u = 0; u < U; ++u) {
-                        if (j0 + u < je) {
-                            if constexpr (kPairs) {
-                                RV e;
-                                e.widen(xv[u]);
-                                e.template exp<F>(c, sums, m);
-                            } else {
+                for (uint32_t u = 0; u < U; ++u) {
+                    if (j0 + u < je) {
+                        if constexpr (kPairs) {
+                            RV e;
+                            e.widen(xv[u]);
+                            e.exp_shift(ms, cs, sums);
+                        } else {
 #pragma unroll
-                                for (int k = 0; k < EPV; ++k) {
-                                    const float ev = row_exp_sel<T, F>(get<T, VB>(xv[u], k), c, m);
-                                    if (k & 1) s1 += ev; else s0 += ev;
-                                }
+                            for (int k = 0; k < EPV; ++k) {
+                                const float ev =
+                                    row_exp_arg<T>(fmaf(get<T, VB>(xv[u], k) - ms, kLog2e, cs));
+                                if (k & 1) s1 += ev; else s0 += ev;
                             }
                         }
                     }
                 }
-                if constexpr (kPairs) sl += sums.total(); else sl += s0 + s1;
             }
-            return sl;
-        };
-        const float sl = fast ? pass2(std::true_type{}) : pass2(std::false_type{});
+            if constexpr (kPairs) sl += sums.total(); else sl += s0 + s1;
+        }
         float s = warp_allreduce_sum(sl);
         if (lane == 0) red[1][b][warp] = s;
         __syncthreads();
@@ -268,28 +265,24 @@ __global__ void __launch_bounds__(kSplitThreads, 1) softmax_threepass_cluster_ke
         const bool fast3 = row_exp_offset_ok(M);
         const float c3 = row_exp_bias<T>() - M * kLog2e;
         const float inv = (fast3 ? slice_offset_correction<T>(M, c3) : 1.0f) / S;
+        const float ms3 = fast3 ? 0.f : M, cs3 = fast3 ? c3 : row_exp_bias<T>();
 
         // pass 3, forward: exp(x - M) / S
         char* dst = yb + soff;
-        auto pass3 = [&](auto ftag) {
-            constexpr bool F = decltype(ftag)::value;
-            for (uint32_t j0 = 0; j0 < J; j0 += U2) {
-                Vec<VB> xv[U2];
+        for (uint32_t j0 = 0; j0 < J; j0 += U2) {
+            Vec<VB> xv[U2];
 #pragma unroll
-                for (uint32_t u = 0; u < U2; ++u)
-                    if (j0 + u < J) xv[u] = ld_stream<VB>(src + (j0 + u) * stride);
+            for (uint32_t u = 0; u < U2; ++u)
+                if (j0 + u < J) xv[u] = ld_stream<VB>(src + (j0 + u) * stride);
 #pragma unroll
-                for (uint32_t u = 0; u < U2; ++u) {
-                    if (j0 + u < J) {
-                        RV e;
-                        e.widen(xv[u]);
-                        st_stream<VB>(dst + (j0 + u) * stride,
-                                      e.template exp_scaled<F>(c3, inv, M));
-                    }
+            for (uint32_t u = 0; u < U2; ++u) {
+                if (j0 + u < J) {
+                    RV e;
+                    e.widen(xv[u]);
+                    st_stream<VB>(dst + (j0 + u) * stride, e.exp_shift_scaled(ms3, cs3, inv));
                 }
             }
-        };
-        if (fast3) pass3(std::true_type{}); else pass3(std::false_type{});
+        }
     }
     // Keep this CTA's shared memory alive until every peer is done with it.
     cluster_sync_all();

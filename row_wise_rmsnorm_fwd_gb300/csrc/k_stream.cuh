@@ -1,0 +1,286 @@
+// k_stream.cuh -- row softmax for many rows too wide for one CTA's registers
+// (prefill logits of a large vocabulary: rows of 128256 elements), every row
+// streamed twice through the bulk-copy slot ring of k_ring.cuh.
+//
+// One CTA per SM, one row at a time, no cluster: warp 0's lane 0 produces
+// (ring_produce with two passes per row: the row's chunks, then the same
+// chunks again), the other warps consume.
+//   pass A: each consumer thread keeps an online pair (m_t, s_t): the
+//     maximum of the elements it has seen and the sum of their exponentials
+//     relative to it; a chunk that raises m_t first rescales s_t.  At the
+//     row's end the pairs are folded over the warp (butterfly) and over the
+//     warps (one slot per warp, one named barrier, a fixed-order fold in
+//     every thread), which is the online-softmax combine, and give the row's
+//     maximum M and sum S.
+//   pass B: the same chunks again, the outputs exp(x - M) / S stored from
+//     registers.
+// The first read comes from DRAM with an L2 keep policy, the second from L2
+// (the rows in flight on all SMs, 152 x 513 KB for fp32 prefill logits,
+// fit in L2), so DRAM moves x once and y once.  Unlike the register-resident
+// and cluster-split kernels no thread holds a row: the ring can take all of
+// shared memory, which keeps a row's worth of copies in flight per SM.
+//
+// Exponent arguments: pass A uses the exact form (x - m_t)*log2e + bias (the
+// maximum changes as the row goes by, so a rounded offset would differ from
+// thread to thread); pass B uses the fused form with the row's offset where
+// row_exp_offset_ok allows it, with the offset's rounding taken out of 1/S
+// (slice_offset_correction), else the exact form.  A thread that has seen
+// only -inf entries keeps (-inf, 0) and adds nothing; a row of -inf, or with
+// a NaN or +inf, ends with a NaN sum and a NaN row, as the definition gives.
+#pragma once
+#include "k_softmax.cuh"
+
+#ifndef RMSNORM_STREAM_FIRST_PASS_POLICY
+#define RMSNORM_STREAM_FIRST_PASS_POLICY 0   // L2 policy of pass A: 0 evict_last, 1 evict_normal
+#endif
+
+namespace rmsnorm {
+
+// 15 consumer warps + the producer: four warps per SM sub-partition, up to 128
+// registers a thread (a 17th warp would cap them at 96 and spill).
+constexpr int kStreamMaxThreads = 512;
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Fold the pair (mo, so) into (m, s): each sum is of exponentials relative
+// to its own maximum; the result is relative to max(m, mo).  A pair whose
+// maximum is the result's keeps its sum unscaled, so two empty pairs (-inf,
+// 0) give (-inf, 0) rather than 0 * 2^NaN.
+__device__ __forceinline__ void pair_fold(float& m, float& s, float mo, float so) {
+    const float M = fmaxf(m, mo);
+    const float a = m == M ? s : s * exp2f((m - M) * kLog2e);
+    const float b = mo == M ? so : so * exp2f((mo - M) * kLog2e);
+    m = M;
+    s = a + b;
+}
+
+// This thread's vectors of one chunk, raw (bf16: half the registers of the
+// widened pairs): src = its first vector in the slot, vstride = bytes to its
+// next one.  kFull: all V vectors are there (no bounds checks), else only
+// those below nv (q0 = this thread's first vector index, nc = vectors per
+// step).
+template <int V, bool kFull>
+__device__ __forceinline__ void stream_load(Vec<16> (&raw)[V], const unsigned char* src,
+                                            int64_t vstride, int q0, int nc, int nv) {
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+        if (kFull || q0 + i * nc < nv)
+            raw[i] = as_vec(*reinterpret_cast<const uint4*>(src + i * vstride));
+}
+
+// Pass A on one chunk: fold its maximum into the running pair (m, s), then
+// add its exponentials relative to the new maximum.
+template <typename T, int V, bool kFull>
+__device__ __forceinline__ float2 stream_fold(const Vec<16> (&raw)[V], int q0, int nc, int nv,
+                                              float2 ms) {
+    using RV = RowVec<T, 16>;
+    float mk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    uint32_t mw[2] = {kBf16x2NegInf, kBf16x2NegInf};
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+        if (kFull || q0 + i * nc < nv) RV::fold_max(raw[i], mk, mw);
+    float mt = ms.x, st = ms.y;
+    const float mn = fmaxf(mt, running_max(mk, mw));
+    if (mn > mt) {
+        st *= exp2f((mt - mn) * kLog2e);       // 0 while mt was -inf
+        mt = mn;
+    }
+    const float mu = mt == -INFINITY ? 0.f : mt;   // -inf entries give 0, not NaN
+    typename RV::Sums sums;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        if (kFull || q0 + i * nc < nv) {
+            RV e;
+            e.widen(raw[i]);
+            e.template exp<false>(0.f, sums, mu);
+        }
+    }
+    return make_float2(mt, st + sums.total());
+}
+
+// Shared-memory header of the streamed kernel: full[32] | empty[32] |
+// red[2][32] pairs | the cluster pair exchange (split rows).
+constexpr int kStreamHeader = 2048;
+
+// V: 16-byte vectors per consumer thread per chunk (chunk_bytes = 16 * V *
+// consumer threads).  CL: each row is split over a thread-block cluster of
+// p.cluster CTAs, CTA rank r streaming slice r (p.slice_vecs vectors) of its
+// cluster's rows; the CTAs' (maximum, sum) pairs cross the cluster once per
+// row through distributed shared memory (cluster_pair_allreduce, bounded
+// wait).  Splitting halves (for two CTAs) the bytes of rows in flight, which
+// the second read needs to find in L2.
+template <typename T, int V, bool CL>
+__global__ void __launch_bounds__(kStreamMaxThreads, 1) softmax_stream_kernel(const Params p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kStagedMaxSlots;
+    float2* red = reinterpret_cast<float2*>(smem + 16 * kStagedMaxSlots);
+    PairExchange* ex = reinterpret_cast<PairExchange*>(smem + 16 * kStagedMaxSlots + 512);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int NCW = static_cast<int>(blockDim.x >> 5) - 1;   // consumer warps
+    const int NC = NCW * 32;
+    const int NCH = p.nchunks, S = p.nslots, CB = p.chunk_bytes;
+    const int64_t row_bytes = static_cast<int64_t>(p.hidden) * sizeof(T);
+    const int ncta = CL ? p.cluster : 1;
+    uint32_t rank = 0;
+    int64_t unit = blockIdx.x, nunits = gridDim.x;
+    if (CL) {
+        rank = cluster_ctarank();
+        unit = cluster_id_x();
+        nunits = cluster_count_x();
+    }
+    const int64_t slice_nom = CL ? static_cast<int64_t>(p.slice_vecs) * 16 : row_bytes;
+    const int64_t sbeg = static_cast<int64_t>(rank) * slice_nom;
+    const int64_t send = sbeg + slice_nom < row_bytes ? sbeg + slice_nom : row_bytes;
+    const int64_t my_bytes = send > sbeg ? send - sbeg : 0;
+    const SlotRing ring{full, empty, smem + kStreamHeader, S, NCH, CB, my_bytes};
+
+    if (tid == 0) {
+        ring_init(ring, NCW);
+        if (CL) {
+            mbar_init(smem_addr(&ex->bar[0]), 1);
+            mbar_init(smem_addr(&ex->bar[1]), 1);
+        }
+        fence_mbarrier_init_cluster();
+    }
+    __syncthreads();
+    if (CL) cluster_sync_all();        // no peer sends before the barriers exist
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer --
+        if (lane == 0) {
+            const uint64_t keep = RMSNORM_STREAM_FIRST_PASS_POLICY == 0 ? policy_evict_last()
+                                                                        : policy_evict_normal();
+            ring_produce(p, ring, unit, nunits, row_bytes, sbeg, keep, kSiteStagedEmpty, 2,
+                         policy_evict_first());
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------------- consumers --
+        const int ct = tid - 32;
+        const int cw = warp - 1;
+        char* yb = static_cast<char*>(p.y);
+        int slot = 0;            // the next chunk's slot
+        uint32_t lap = 0;        // its phase parity
+        bool ok = true;          // warp-uniform; false once a bounded wait expired
+        // Wait (bounded) for the next chunk; every lane of the warp agrees.
+        auto acquire = [&]() {
+            ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded<false>(smem_addr(&full[slot]),
+                                                                        lap, p.timeout_ns));
+            return ok;
+        };
+        // The warp has copied its vectors of the chunk: hand the slot back.
+        auto release = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&empty[slot]));
+            if (++slot == S) {
+                slot = 0;
+                lap ^= 1u;
+            }
+        };
+        // This thread's first vector in the current slot; vector i of a chunk
+        // is i * NC vectors further on.
+        auto slot_base = [&]() {
+            return ring.slots + static_cast<int64_t>(slot) * CB + static_cast<int64_t>(ct) * 16;
+        };
+        const int64_t vstride = static_cast<int64_t>(NC) * 16;
+        const int full_nv = V * NC;            // vectors of a full chunk
+
+        uint32_t it = 0;
+        for (int64_t row = unit; row < p.rows; row += nunits, ++it) {
+            // pass A: the online (maximum, sum) pair of this thread's elements
+            float2 ms = make_float2(-INFINITY, 0.f);
+#pragma unroll 1
+            for (int k = 0; k < NCH && acquire(); ++k) {
+                const int nv = ring.chunk_len(k) >> 4;
+                Vec<16> raw[V];
+                if (nv == full_nv) {
+                    stream_load<V, true>(raw, slot_base(), vstride, ct, NC, nv);
+                    release();
+                    ms = stream_fold<T, V, true>(raw, ct, NC, nv, ms);
+                } else {
+                    stream_load<V, false>(raw, slot_base(), vstride, ct, NC, nv);
+                    release();
+                    ms = stream_fold<T, V, false>(raw, ct, NC, nv, ms);
+                }
+            }
+            float mt = ms.x, st = ms.y;
+            // the CTA's pair: warp butterfly, one slot per warp, fixed-order fold
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float mo = __shfl_xor_sync(0xffffffffu, mt, o);
+                const float so = __shfl_xor_sync(0xffffffffu, st, o);
+                pair_fold(mt, st, mo, so);
+            }
+            const int b = it & 1;
+            if (lane == 0) red[b * 32 + cw] = make_float2(mt, st);
+            if (named_bar_or(1, NC, !ok)) {
+                if (ct == 0) report_timeout(p.status, kSiteStagedFull);
+                break;
+            }
+            float M = -INFINITY, Ssum = 0.f;
+            for (int w = 0; w < NCW; ++w)
+                pair_fold(M, Ssum, red[b * 32 + w].x, red[b * 32 + w].y);
+            if (CL) {
+                // the row's pair from the cluster's CTA pairs (one exchange)
+                float Mr, Sr;
+                const bool cok =
+                    cluster_pair_allreduce(ex, M, Ssum, ncta, rank, it, p, &Mr, &Sr, ct);
+                if (named_bar_or(1, NC, !cok)) break;   // uniform: stop, leave cleanly
+                M = Mr;
+                Ssum = Sr;
+            }
+
+            // pass B: exp(x - M) / S from the same chunks again
+            const bool fast = row_exp_offset_ok(M);
+            const float c = row_exp_bias<T>() - M * kLog2e;
+            const float Mu = M == -INFINITY ? 0.f : M;
+            const float inv = (fast ? slice_offset_correction<T>(M, c) : 1.0f) / Ssum;
+            char* dst = yb + row * row_bytes + sbeg + static_cast<int64_t>(ct) * 16;
+            auto pass_b_chunk = [&](auto ftag, auto full_tag, int k, int nv) {
+                constexpr bool F = decltype(ftag)::value;
+                constexpr bool kFull = decltype(full_tag)::value;
+                Vec<16> raw[V];
+                stream_load<V, kFull>(raw, slot_base(), vstride, ct, NC, nv);
+                release();
+                char* cdst = dst + static_cast<int64_t>(k) * CB;
+#pragma unroll
+                for (int i = 0; i < V; ++i) {
+                    if (kFull || ct + i * NC < nv) {
+                        RowVec<T, 16> e;
+                        e.widen(raw[i]);
+                        st_stream<16>(cdst + i * vstride, e.template exp_scaled<F>(c, inv, Mu));
+                    }
+                }
+            };
+            if (fast) {
+#pragma unroll 1
+                for (int k = 0; k < NCH && acquire(); ++k) {
+                    const int nv = ring.chunk_len(k) >> 4;
+                    if (nv == full_nv) pass_b_chunk(std::true_type{}, std::true_type{}, k, nv);
+                    else pass_b_chunk(std::true_type{}, std::false_type{}, k, nv);
+                }
+            } else {               // rows of large or non-finite maximum: rare
+#pragma unroll 1
+                for (int k = 0; k < NCH && acquire(); ++k)
+                    pass_b_chunk(std::false_type{}, std::false_type{}, k, ring.chunk_len(k) >> 4);
+            }
+        }
+    }
+    // Keep this CTA's shared memory alive until every peer is done with it.
+    if (CL) cluster_sync_all();
+}
+
+}  // namespace rmsnorm

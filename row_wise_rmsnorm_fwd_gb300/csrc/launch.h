@@ -48,6 +48,14 @@ int split_block();
 // kStagedHeaderHost + nslots * chunk bytes.
 KernelFn softmax_staged_ptr(int dtype, int nv, bool cluster);
 int softmax_staged_max_threads();
+// Row softmax streamed twice through the bulk-copy ring (online maximum and
+// sum, then the outputs): one producer warp plus consumer threads of v (2 or
+// 4) 16-byte vectors per chunk; dynamic shared memory = kStreamHeaderHost +
+// nslots * chunk bytes, chunk = 16 * v * consumer threads; cluster = rows
+// split over a thread-block cluster (slices of Params.slice_vecs vectors).
+constexpr int kStreamHeaderHost = 2048;
+KernelFn softmax_stream_ptr(int dtype, int v, bool cluster);
+int softmax_stream_max_threads();
 
 // Comparison kernel with the compiler write-up's schedule (one CTA per row).
 KernelFn page_kernel_ptr(int dtype);

@@ -21,6 +21,9 @@ constexpr int64_t kSoftmaxStagedMinColsBf16 = 16384;    // wider bf16 rows go to
 constexpr int kSoftmaxMaxStagedCluster = 8;             // portable cluster sizes only
 constexpr int64_t kSoftmaxSplitStagedMinRowBytes = 240 << 10;  // narrower: three-pass (sm_make_plan)
 constexpr int64_t kSoftmaxUnsplitMaxVecs = 0x7FFFFFFFll - 1024;  // three-pass, one CTA per row
+constexpr int64_t kSoftmaxStreamMinRowBytes = 128 << 10;   // streamed: rows of at least this
+constexpr int64_t kSoftmaxStreamMaxSlice = 400 << 10;      // streamed: split rows above this
+constexpr int kSoftmaxStreamMaxCluster = 8;
 
 struct SmCall {
     int dtype;
@@ -78,29 +81,33 @@ rmsnorm_status_t sm_validate(int32_t dtype, const void* x, const void* y, int64_
         if (o.weights || o.reserved || o.epilogue || o.fault_inject < 0 || o.fault_inject > 2)
             return RMSNORM_ERR_INVALID_ARG;
         // fault injection: test build only, and only where its site exists
-        // (1: the staged ring's first copy; 2: a split row's first pair)
+        // (1: the ring's first copy; 2: a split row's first pair)
         if (o.fault_inject != 0 &&
             (!RMSNORM_FAULT_INJECT ||
-             (o.fault_inject == 1 && o.path != RMSNORM_PATH_STAGED) ||
+             (o.fault_inject == 1 && o.path != RMSNORM_PATH_STAGED &&
+              o.path != RMSNORM_PATH_STREAM) ||
              (o.fault_inject == 2 && o.path != RMSNORM_PATH_CLUSTER &&
-              !((o.path == RMSNORM_PATH_STAGED || o.path == RMSNORM_PATH_TWOPASS) &&
+              !((o.path == RMSNORM_PATH_STAGED || o.path == RMSNORM_PATH_TWOPASS ||
+                 o.path == RMSNORM_PATH_STREAM) &&
                 o.cluster > 1))))
             return RMSNORM_ERR_UNSUPPORTED;
         if (o.path != RMSNORM_PATH_AUTO && o.path != RMSNORM_PATH_ROWREG &&
             o.path != RMSNORM_PATH_TWOPASS && o.path != RMSNORM_PATH_CLUSTER &&
-            o.path != RMSNORM_PATH_STAGED)
+            o.path != RMSNORM_PATH_STAGED && o.path != RMSNORM_PATH_STREAM)
             return RMSNORM_ERR_INVALID_ARG;
-        // chunk and ring sizes shape the staged kernel only
-        if ((o.chunk_bytes || o.stages) && o.path != RMSNORM_PATH_STAGED)
+        // chunk and ring sizes shape the ring kernels only
+        if ((o.chunk_bytes || o.stages) && o.path != RMSNORM_PATH_STAGED &&
+            o.path != RMSNORM_PATH_STREAM)
             return RMSNORM_ERR_INVALID_ARG;
         if (o.chunk_bytes < 0 || o.chunk_bytes % 16 != 0 || o.stages < 0)
             return RMSNORM_ERR_INVALID_ARG;
-        // cluster sizes: powers of two, or any size up to 16 for TWOPASS
+        // cluster sizes: powers of two, or any size up to 16 for TWOPASS and STREAM
         if (o.cluster < 0 || o.cluster > 16 ||
-            ((o.cluster & (o.cluster - 1)) != 0 && o.path != RMSNORM_PATH_TWOPASS))
+            ((o.cluster & (o.cluster - 1)) != 0 && o.path != RMSNORM_PATH_TWOPASS &&
+             o.path != RMSNORM_PATH_STREAM))
             return RMSNORM_ERR_INVALID_ARG;
         if (o.cluster > 1 && o.path != RMSNORM_PATH_CLUSTER && o.path != RMSNORM_PATH_STAGED &&
-            o.path != RMSNORM_PATH_TWOPASS)
+            o.path != RMSNORM_PATH_TWOPASS && o.path != RMSNORM_PATH_STREAM)
             return RMSNORM_ERR_INVALID_ARG;
         const bool sub_warp = o.threads > 0 && o.threads < 32 && (o.threads & (o.threads - 1)) == 0;
         if (o.threads < 0 || (o.threads % 32 != 0 && !sub_warp) || o.threads > 1024 || o.grid < 0)
@@ -370,6 +377,77 @@ rmsnorm_status_t sm_plan_staged(const SmCall& c, int cluster, SmPlan* P) {
     return RMSNORM_OK;
 }
 
+// Rows streamed twice through the ring (softmax_stream_kernel): 16-byte
+// vectors only; 480 consumer threads (or opt->threads, a multiple of 32 up
+// to 480) and a producer warp; chunks of v = 4 vectors per consumer thread
+// (opt->chunk_bytes may ask for v = 2: 16 * v * consumer threads bytes);
+// as many ring slots as shared memory holds, up to 32 (or opt->stages, at
+// least 2); one CTA per SM, at most one per row (or slice).  cluster > 1
+// splits each row over a thread-block cluster of that many CTAs.
+rmsnorm_status_t sm_plan_stream(const SmCall& c, int cluster, SmPlan* P) {
+    int vb;
+    rmsnorm_status_t st = sm_pick_vb(c, &vb);
+    if (st != RMSNORM_OK) return st;
+    if (vb != 16) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t row_bytes = c.cols * c.sz;
+    const int64_t nvec = row_bytes / 16;
+    const int64_t per = (nvec + cluster - 1) / cluster;       // vectors per CTA slice
+    if (static_cast<int64_t>(cluster - 1) * per >= nvec) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t slice_bytes = per * 16;
+    const int max_nc = softmax_stream_max_threads() - 32;
+    const int nc = c.opt.threads > 0 ? c.opt.threads : max_nc;
+    if (nc % 32 != 0 || nc > max_nc) return RMSNORM_ERR_UNSUPPORTED;
+    int v = 4;
+    if (c.opt.chunk_bytes != 0) {
+        if (c.opt.chunk_bytes == 2 * 16 * nc) v = 2;
+        else if (c.opt.chunk_bytes == 4 * 16 * nc) v = 4;
+        else return RMSNORM_ERR_UNSUPPORTED;
+    }
+    const int64_t chunk = static_cast<int64_t>(16) * v * nc;
+    const int64_t nchunks = (slice_bytes + chunk - 1) / chunk;
+    if (nchunks > 0x7FFFFFFFll) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t budget = c.dv.smem_optin - kStreamHeaderHost;
+    int64_t slots = c.opt.stages ? c.opt.stages : budget / chunk;
+    if (!c.opt.stages && slots > kStagedMaxSlotsHost) slots = kStagedMaxSlotsHost;
+    if (slots < 2 || slots > kStagedMaxSlotsHost || slots * chunk > budget)
+        return RMSNORM_ERR_UNSUPPORTED;
+    KernelFn fn = softmax_stream_ptr(c.dtype, v, cluster > 1);
+    if (!fn) return RMSNORM_ERR_UNSUPPORTED;
+    const int block = nc + 32;
+    const int smem = static_cast<int>(kStreamHeaderHost + slots * chunk);
+    int occ = 0;
+    if (cached_occupancy(c.dv.dev, c.dv.smem_optin, fn, block, smem, cluster, &occ) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
+    int64_t grid;
+    if (cluster == 1) {
+        const int64_t resident = static_cast<int64_t>(c.dv.sms) * occ;
+        grid = c.opt.grid > 0 ? c.opt.grid : (c.rows < resident ? c.rows : resident);
+    } else {
+        const int64_t nclusters = c.opt.grid > 0 ? (c.opt.grid + cluster - 1) / cluster
+                                                 : (c.rows < occ ? c.rows : occ);
+        grid = nclusters * cluster;
+    }
+    *P = SmPlan{};             // every field this plan does not set keeps its default
+    P->path = RMSNORM_PATH_STREAM;
+    P->cluster = cluster;
+    P->slice_vecs = static_cast<int>(per);
+    P->group = nc;
+    P->block = block;
+    P->rpc = 1;
+    P->grid = static_cast<int>(grid);
+    P->vb = 16;
+    P->nv = v;
+    P->nvec = static_cast<int>(nvec);
+    P->smem = smem;
+    P->chunk = static_cast<int>(chunk);
+    P->nchunks = static_cast<int>(nchunks);
+    P->nslots = static_cast<int>(slots);
+    P->fn = fn;
+    P->name = cluster == 1 ? "softmax_stream" : "softmax_cluster_stream";
+    return RMSNORM_OK;
+}
+
 // Automatic choice: few rows of wide rows (or large few-row inputs) are split
 // over a cluster (up to 8 CTAs, slices of at least 4 KB), as for RMSNorm;
 // fp32 rows of more than 8192 elements and bf16 rows of more than 16384 are
@@ -380,6 +458,50 @@ rmsnorm_status_t sm_plan_staged(const SmCall& c, int cluster, SmPlan* P) {
 // 16384 64 in registers against 60 staged); narrower rows are held in
 // registers by the register kernel; what neither takes goes to the
 // three-pass kernel.
+// The streamed kernel, automatically: rows of at least 128 KB that the
+// register-resident staged kernel cannot hold (fp32 rows of more than 32768
+// elements, bf16 rows of 65536 and more), from a quarter of the SM count of
+// rows up.  Each row is split over C CTAs, C the smallest power of two that
+// keeps slices within 400 KB (the rows in flight on all SMs, whose second
+// read must find them in L2, then stay within about 60 MB) and, for fewer
+// rows than SMs, gives at least half the SMs a slice.  Measured (1 GB
+// inputs, % of the measured HBM copy peak; streamed / previous automatic
+// choice): fp32 rows of 36000 / 40000 / 65536 elements 95 / 93 / 93 against
+// 85 / 82 / 83, of 100000 and 200000 (C = 2) 86 / 87 against 63 / 53, of
+// 128256 (prefill logits, C = 2) 83 against 74, of 262144 (C = 4) 87 against
+// 66; bf16 rows of 98304 / 128256 91 / 89 against 75 / 69, of 262144 (C = 2)
+// 93 against 59; bf16 rows of 49152 86 for the three-pass kernel against 79
+// streamed.  One CTA per row where slices of two would do loses on L2
+// (fp32 rows of 128256: 78%), clusters of 3, 5 or 6 leave SMs idle.  Few
+// rows: 64 rows of 128256 elements take 14.7 us (bf16) and 20.9 us (fp32)
+// streamed over clusters of two against 16.3 and 30.1 us for the register
+// split, but 8 fp32 rows 10.4 us against 8.7 us, so fewer than a quarter of
+// the SM count of rows stay with the register split.
+bool sm_stream_eligible(const SmCall& c) {
+    const int64_t row_bytes = c.cols * c.sz;
+    if (row_bytes < kSoftmaxStreamMinRowBytes) return false;
+    if (c.dtype == RMSNORM_DTYPE_F32 && c.cols <= 32768) return false;
+    return 4 * c.rows >= c.dv.sms;
+}
+
+rmsnorm_status_t sm_plan_stream_auto(const SmCall& c, SmPlan* P) {
+    const int64_t row_bytes = c.cols * c.sz;
+    int cl = 1;
+    while (cl < kSoftmaxStreamMaxCluster && (row_bytes + cl - 1) / cl > kSoftmaxStreamMaxSlice)
+        cl <<= 1;
+    while (cl < kSoftmaxStreamMaxCluster && 2 * c.rows * cl < c.dv.sms) cl <<= 1;
+    for (; cl >= 1; cl >>= 1) {
+        SmPlan Q;
+        const rmsnorm_status_t st = sm_plan_stream(c, cl, &Q);
+        if (st == RMSNORM_ERR_CUDA) return st;
+        if (st == RMSNORM_OK) {
+            *P = Q;
+            return RMSNORM_OK;
+        }
+    }
+    return RMSNORM_ERR_UNSUPPORTED;
+}
+
 rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
     switch (c.opt.path) {
         case RMSNORM_PATH_ROWREG: return sm_plan_rowreg(c, 1, P);
@@ -387,10 +509,15 @@ rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
         case RMSNORM_PATH_TWOPASS:
             return sm_plan_threepass(c, c.opt.cluster ? c.opt.cluster : 1, P);
         case RMSNORM_PATH_STAGED: return sm_plan_staged(c, c.opt.cluster ? c.opt.cluster : 1, P);
+        case RMSNORM_PATH_STREAM: return sm_plan_stream(c, c.opt.cluster ? c.opt.cluster : 1, P);
         default: break;
     }
     const int64_t row_bytes = c.cols * c.sz;
     rmsnorm_status_t st;
+    if (sm_stream_eligible(c)) {
+        st = sm_plan_stream_auto(c, P);
+        if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+    }
     if (c.rows < c.dv.sms && (row_bytes > kSoftmaxSplitRowBytes ||
                               c.rows * row_bytes >= kSoftmaxSplitMinBytes)) {
         int want = 1;

@@ -125,7 +125,9 @@ def test_softmax_fault_injection_is_test_build_only(lib):
                  dict(path="staged", cluster=2, fault_inject=2),
                  dict(path="cluster", cluster=2, fault_inject=2),
                  dict(fault_inject=1), dict(path="rowreg", fault_inject=2),
-                 dict(path="twopass", fault_inject=1)):
+                 dict(path="twopass", fault_inject=1), dict(path="stream", fault_inject=1),
+                 dict(path="stream", cluster=2, fault_inject=2),
+                 dict(path="stream", fault_inject=2)):
         o = binding.make_options(**opts)
         assert binding.raw.rowsoftmax_fwd_ex(0, A, B, 4, 8, o) == unsupported, opts
     for v in (-1, 3):
@@ -149,10 +151,12 @@ def test_softmax_ex_staged_shape_options_are_checked(lib):
 
 def test_softmax_cluster_sizes_are_checked(lib):
     """A split over a cluster takes 2..16 CTAs: any size for the three-pass
-    kernel (RMSNORM_PATH_TWOPASS), powers of two for the register and staged
-    kernels; anything else is refused before any CUDA call."""
+    and streamed kernels (RMSNORM_PATH_TWOPASS, RMSNORM_PATH_STREAM), powers
+    of two for the register and staged kernels; anything else is refused
+    before any CUDA call."""
     for path, cluster in (("cluster", 3), ("cluster", 12), ("staged", 6), ("twopass", 17),
-                          ("twopass", -1), ("rowreg", 2), ("auto", 2)):
+                          ("twopass", -1), ("stream", 17), ("stream", -2), ("rowreg", 2),
+                          ("auto", 2)):
         o = binding.make_options(path=path)
         o.cluster = cluster
         assert binding.raw.rowsoftmax_fwd_ex(0, A, B, 4, 8, o) == INVALID, (path, cluster)

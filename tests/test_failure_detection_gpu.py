@@ -125,6 +125,11 @@ SOFTMAX_CASES = [
      (16, 128256)),
     ("softmax three-pass cluster withholds a pair",
      dict(path="twopass", cluster=4, fault_inject=2), (8, 65536)),
+    ("softmax stream withholds a copy", dict(path="stream", fault_inject=1), (64, 128256)),
+    ("softmax stream cluster withholds a copy", dict(path="stream", cluster=2, fault_inject=1),
+     (16, 128256)),
+    ("softmax stream cluster withholds a pair", dict(path="stream", cluster=2, fault_inject=2),
+     (16, 128256)),
 ]
 
 

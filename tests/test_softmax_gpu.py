@@ -78,6 +78,7 @@ def test_width_sweep(dtype, cols):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("path,cluster", [("rowreg", 0), ("twopass", 0), ("staged", 0),
+                                          ("stream", 0),
                                           ("cluster", 2), ("cluster", 4), ("cluster", 8),
                                           ("cluster", 16), ("twopass", 2), ("twopass", 16),
                                           ("twopass", 5), ("twopass", 12)])
@@ -140,7 +141,8 @@ def large_magnitude_rows(cols, seed):
 @pytest.mark.parametrize("path,cluster,cols", [
     ("auto", 0, 4096), ("auto", 0, 32000), ("rowreg", 0, 4096), ("staged", 0, 32000),
     ("cluster", 4, 65536), ("twopass", 0, 65536), ("twopass", 4, 65536),
-    ("staged", 2, 128256), ("staged", 4, 128256)])
+    ("staged", 2, 128256), ("staged", 4, 128256), ("stream", 0, 65536),
+    ("stream", 0, 128256), ("stream", 2, 128256), ("stream", 3, 100000)])
 def test_large_magnitude_rows(dtype, path, cluster, cols):
     """Rows with maxima from 2e6 to 3.38e38 (either sign) through every
     softmax kernel: finite results equal to the oracle's, no NaN rows."""
@@ -153,6 +155,77 @@ def test_large_magnitude_rows(dtype, path, cluster, cols):
         raise
     assert not torch.isnan(y.float()).any()
     compare(y, ref_for(x), f"large magnitudes {path} C={cluster} {dtype} cols={cols}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols,cluster,stages,grid", [
+    (300, 128256, 2, 0, 0),           # prefill-logit rows over clusters of two
+    (77, 262144, 4, 0, 0),            # clusters of four
+    (9, 100000, 3, 2, 6),             # odd cluster, two-slot ring, two clusters
+    (5, 4104, 2, 0, 0),               # slices shorter than one chunk
+    (3, 24, 2, 0, 0),                 # three vectors per row split over two CTAs
+])
+def test_stream_cluster_split(dtype, rows, cols, cluster, stages, grid):
+    """The streamed kernel with each row split over a thread-block cluster
+    (one (maximum, sum) exchange per row through distributed shared memory)."""
+    x = case(rows, cols, dtype, rows * 11 + cols + cluster)
+    try:
+        y = run(x.cuda(), path="stream", cluster=cluster, stages=stages, grid=grid)
+    except binding.RmsnormError as e:
+        assert e.status == binding.RMSNORM_ERR_UNSUPPORTED
+        nvec = cols * x.element_size() // 16
+        assert (cols * x.element_size()) % 16 != 0 or (cluster - 1) * (-(-nvec // cluster)) >= nvec
+        return
+    compare(y, ref_for(x), f"stream split C={cluster} {dtype} {rows}x{cols} S={stages} grid={grid}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols,chunk,stages,grid,threads", [
+    (300, 128256, 0, 0, 0, 0),        # prefill-logit rows, automatic ring
+    (7, 8, 0, 0, 0, 0),               # a row shorter than one vector per thread
+    (40, 2056, 0, 0, 0, 0),           # one partial chunk per row
+    (33, 7684, 0, 0, 0, 0),           # fp32: one full 30720-byte chunk and a 16-byte one
+    (160, 100000, 0, 0, 0, 0),        # more rows than SMs, ragged last chunk
+    (19, 262144, 0, 2, 5, 0),         # a two-slot ring, five CTAs, many rows each
+    (25, 77780, 0, 3, 0, 64),         # 64 consumer threads, three slots (bf16: refused)
+    (12, 50000, 16 * 2 * 480, 0, 0, 0),      # two vectors per thread and chunk
+])
+def test_stream_ring_shapes(dtype, rows, cols, chunk, stages, grid, threads):
+    """The two-read streamed kernel over ragged widths, ring depths, grid
+    sizes (several rows per CTA) and consumer counts; widths whose rows are
+    not a multiple of 16 bytes are refused."""
+    x = case(rows, cols, dtype, rows * 7 + cols)
+    try:
+        y = run(x.cuda(), path="stream", chunk_bytes=chunk, stages=stages, grid=grid,
+                threads=threads)
+    except binding.RmsnormError as e:
+        assert e.status == binding.RMSNORM_ERR_UNSUPPORTED
+        assert (cols * x.element_size()) % 16 != 0
+        return
+    compare(y, ref_for(x), f"stream {dtype} {rows}x{cols} chunk={chunk} S={stages} "
+                           f"grid={grid} threads={threads}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_stream_special_values(dtype):
+    """Masked entries, a fully masked row, NaN and +inf rows, and a row whose
+    first 40000 entries are -inf (whole chunks of it, so some threads see only
+    -inf before the finite part) through the streamed kernel; in place too."""
+    cols = 128256
+    x = case(6, cols, "f32", 23)
+    x[0, ::7] = -float("inf")
+    x[1] = -float("inf")
+    x[2, 60000] = float("nan")
+    x[3, 3] = float("inf")
+    x[4, :40000] = -float("inf")
+    x[5, 100000:] = -float("inf")
+    x = x.to(DT[dtype])
+    ref = ref_for(x)
+    for cl in (0, 2, 4):
+        compare(run(x.cuda(), path="stream", cluster=cl), ref, f"stream C={cl} special {dtype}")
+        xd = x.cuda()
+        run(xd, xd, path="stream", cluster=cl)
+        compare(xd, ref, f"stream C={cl} special in place {dtype}")
 
 
 MAX_COLS = (1 << 31) - 1      # the widest row the ABI accepts
@@ -368,15 +441,19 @@ def test_guards_and_determinism(dtype):
     ((4096, 32000), "f32", "softmax_staged"),
     ((8192, 32000), "bf16", "softmax_staged"),
     ((16384, 16384), "bf16", "softmax_rowreg"),          # eight vectors per thread
-    ((1024, 128256), "f32", "softmax_cluster_staged"),   # prefill logits, fp32
-    ((2048, 128256), "bf16", "softmax_cluster_staged"),  # prefill logits, bf16: slices 98% full
-    ((2048, 262144), "bf16", "softmax_cluster_staged"),  # full slices over 8 CTAs
-    ((5368, 100000), "bf16", "softmax_threepass"),       # slices 76% full
-    ((8192, 65536), "bf16", "softmax_threepass"),        # rows of 128 KB: L2 serves the re-reads
-    ((5592, 48000), "f32", "softmax_threepass"),         # rows of 188 KB
-    ((4096, 65536), "f32", "softmax_cluster_staged"),    # rows of 256 KB
-    ((8, 128256), "f32", "softmax_cluster_rowreg"),      # decode logits
+    ((1024, 128256), "f32", "softmax_cluster_stream"),   # prefill logits, fp32: slices of 2
+    ((2048, 128256), "bf16", "softmax_stream"),          # prefill logits, bf16: rows of 256 KB
+    ((2048, 262144), "bf16", "softmax_cluster_stream"),  # rows of 512 KB over 2 CTAs
+    ((5368, 100000), "bf16", "softmax_stream"),          # rows of 195 KB
+    ((8192, 65536), "bf16", "softmax_stream"),           # rows of 128 KB
+    ((8192, 49152), "bf16", "softmax_threepass"),        # rows of 96 KB: L2 serves the re-reads
+    ((5592, 48000), "f32", "softmax_stream"),            # rows of 188 KB
+    ((4096, 65536), "f32", "softmax_stream"),            # rows of 256 KB
+    ((1024, 1 << 20), "f32", "softmax_cluster_stream"),  # rows of 4 MB over 8 CTAs
+    ((64, 128256), "bf16", "softmax_cluster_stream"),    # decode logits, 64 sequences
+    ((8, 128256), "f32", "softmax_cluster_rowreg"),      # decode logits, 8 sequences
     ((2, 1 << 20), "f32", "softmax_cluster_threepass"),  # few rows of 4 MB
+    ((2048, 128255), "f32", "softmax_threepass"),        # rows not a multiple of 16 bytes
 ])
 def test_automatic_choice(shape, dtype, kernel):
     """The automatic kernel choice for representative shapes (no launch)."""
@@ -385,15 +462,18 @@ def test_automatic_choice(shape, dtype, kernel):
     assert p["kernel"] == kernel, p
 
 
-def test_rejected_split_leaves_no_trace_in_the_plan():
-    """bf16 rows whose cluster split is planned and then rejected (slices too
-    empty) launch the three-pass kernel as a plain launch: no cluster and no
-    shared-memory reservation left over from the split."""
+def test_plans_report_each_kernels_own_launch():
+    """Each plan reports the launch of the kernel it chose and nothing of the
+    others: the streamed kernel its ring and no cluster, the three-pass kernel
+    (forced) no ring, the staged split (forced) its cluster and ring."""
     x = torch.empty((3533, 151936), dtype=torch.bfloat16, device="cuda")
     p = binding.rowsoftmax_plan(x, torch.empty_like(x))
-    assert p["kernel"] == "softmax_threepass", p
-    assert p["cluster"] == 1 and p["smem_bytes"] == 0 and p["stages"] == 0, p
-    # the split itself, forced, reports its ring
+    assert p["kernel"] == "softmax_stream", p
+    assert p["cluster"] == 1 and p["smem_bytes"] > 0 and p["stages"] >= 2, p
+    assert p["block_threads"] == 512 and p["grid"] == torch.cuda.get_device_properties(0).multi_processor_count, p
+    t = binding.rowsoftmax_plan(x, torch.empty_like(x), options={"path": "twopass"})
+    assert t["kernel"] == "softmax_threepass", t
+    assert t["cluster"] == 1 and t["smem_bytes"] == 0 and t["stages"] == 0, t
     q = binding.rowsoftmax_plan(x, torch.empty_like(x), options={"path": "staged", "cluster": 8})
     assert q["cluster"] == 8 and q["smem_bytes"] > 0 and q["stages"] >= 1, q
 
