@@ -386,8 +386,8 @@ def run_ours(args, wl):
     if softmax:
         staged = args.path in ("staged", "stream")
         options = binding.make_options(
-            path=args.path if args.path in ("rowreg", "twopass", "cluster", "staged", "stream")
-            else "auto",
+            path=args.path if args.path in ("rowreg", "twopass", "cluster", "staged", "stream",
+                                            "grid") else "auto",
             cluster=args.cluster if args.path in ("cluster", "staged", "twopass", "stream") else 0,
             grid=args.grid, threads=args.threads,
             chunk_bytes=args.chunk if staged else 0, stages=args.stages if staged else 0)
@@ -698,7 +698,7 @@ def main():
                     help="use only this many rows of the workload (small profiling cases)")
     ap.add_argument("--path", default="auto",
                     choices=["auto", "rowreg", "staged", "cluster", "twopass", "page", "ringreg",
-                             "stream"],
+                             "stream", "grid"],
                     help="force a kernel family through rmsnorm_fwd_ex (evidence runs)")
     ap.add_argument("--cluster", type=int, default=0)
     ap.add_argument("--grid", type=int, default=0, help="force the CTA count")

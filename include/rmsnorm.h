@@ -23,8 +23,13 @@
  *  - y == x (exact in-place) is allowed; any other overlap of x and y is
  *    rejected.  w may not overlap y.
  *  - The call is asynchronous on `stream` (NULL = the legacy default stream)
- *    and allocates no memory.  Argument errors are detected on the host
- *    before any launch and leave the device untouched.
+ *    and allocates no memory, with one exception: the few-very-wide-rows
+ *    kernel (RMSNORM_PATH_GRID: forced through rmsnorm_fwd_ex, and chosen
+ *    automatically by the row softmax for fewer rows than SMs of 16 MB and
+ *    more, totalling 96 MB or more) takes a scratch area of at most 17 KB from
+ *    the current device's default memory pool in stream order and returns it
+ *    on the same stream.  Argument errors are detected on the host before any
+ *    launch and leave the device untouched.
  *  - rows == 0 returns RMSNORM_OK without a launch.
  *  - The library's only device state is one status word per device, written
  *    by a kernel whose bounded wait ran out (see rmsnorm_last_device_status).
@@ -84,10 +89,23 @@ typedef enum {
                                   shared memory; opt->threads = consumer threads,
                                   opt->chunk_bytes = 2 or 4 vectors per consumer thread
                                   (x 16 bytes x threads), opt->stages = ring slots */
-    RMSNORM_PATH_STREAM = 7    /* row softmax only (rowsoftmax_fwd_ex): each row streamed
+    RMSNORM_PATH_STREAM = 7,   /* row softmax only (rowsoftmax_fwd_ex): each row streamed
                                   twice through a shared-memory ring by bulk copies, the
                                   first read from DRAM (online maximum and sum), the second
-                                  normally from L2 (outputs); one CTA per SM, no cluster */
+                                  normally from L2 (outputs); one CTA per SM; opt->cluster =
+                                  2..16 splits each row over a thread-block cluster */
+    RMSNORM_PATH_GRID = 8      /* few rows of tens of MB (16-byte aligned x, w, y and
+                                  pitch): every row over the whole grid in turn (one CTA
+                                  per SM, a cooperative launch), streamed twice through
+                                  each CTA's shared-memory ring so that the second read of
+                                  a row finds it in L2; the CTAs' partial results meet in
+                                  a scratch area of at most 17 KB that the call takes from
+                                  the device's default memory pool in stream order
+                                  (cudaMallocAsync / cudaFreeAsync on `stream`); opt->grid
+                                  = CTAs (at most one per SM), opt->threads = consumer
+                                  threads (multiple of 32, <= 480), opt->chunk_bytes =
+                                  2 or 4 vectors per consumer thread, opt->stages = ring
+                                  slots (2..32) */
 } rmsnorm_path_t;
 
 /* Options for rmsnorm_fwd_ex / rmsnorm_plan.  Zero-initialise, then set what you

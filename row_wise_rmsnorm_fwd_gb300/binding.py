@@ -29,7 +29,7 @@ RMSNORM_DTYPE_F32 = 0
 RMSNORM_DTYPE_BF16 = 1
 
 PATHS = {"auto": 0, "rowreg": 1, "staged": 2, "cluster": 3, "twopass": 4, "page": 5,
-         "ringreg": 6, "stream": 7}
+         "ringreg": 6, "stream": 7, "grid": 8}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 

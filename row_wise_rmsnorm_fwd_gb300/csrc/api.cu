@@ -73,6 +73,7 @@ struct Plan {
     int nvec = 0;
     int slice_vecs = 0;
     int resident = 0;       // resident CTAs per SM, or resident clusters (split rows)
+    int scratch = 0;        // grid-split kernels: bytes of cleared scratch (cooperative launch)
     KernelFn fn = nullptr;
     const char* name = "";
 };
@@ -425,6 +426,72 @@ rmsnorm_status_t plan_twopass(const Call& c, int cluster, Plan* P) {
     return RMSNORM_OK;
 }
 
+// Every row over the whole grid (rmsnorm_grid_kernel): 16-byte vectors only;
+// the streamed kernels' CTA (480 consumer threads, or opt->threads, and a
+// producer warp; chunks of 4 vectors per consumer thread, or 2 through
+// opt->chunk_bytes; as many ring slots as shared memory holds, or
+// opt->stages, at least 2); one CTA per SM, all resident (a cooperative
+// launch), opt->grid of them at most; each owns a contiguous slice of every
+// row and of w.
+rmsnorm_status_t plan_grid(const Call& c, Plan* P) {
+    if (c.opt.vec_bytes != 0 && c.opt.vec_bytes != 16) return RMSNORM_ERR_UNSUPPORTED;
+    if (widest_vb(c) != 16) return RMSNORM_ERR_UNSUPPORTED;
+    if (c.opt.cluster > 1 || c.opt.weights != 0) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t row_bytes = c.hidden * c.sz;
+    const int64_t nvec = row_bytes / 16;
+    const int max_nc = softmax_stream_max_threads() - 32;
+    const int nc = c.opt.threads > 0 ? c.opt.threads : max_nc;
+    if (nc % 32 != 0 || nc > max_nc) return RMSNORM_ERR_UNSUPPORTED;
+    int v = 4;
+    if (c.opt.chunk_bytes != 0) {
+        if (c.opt.chunk_bytes == 2 * 16 * nc) v = 2;
+        else if (c.opt.chunk_bytes == 4 * 16 * nc) v = 4;
+        else return RMSNORM_ERR_UNSUPPORTED;
+    }
+    const int64_t chunk = static_cast<int64_t>(16) * v * nc;
+    const int64_t budget = c.info->smem_optin - kStreamHeaderHost;
+    if (c.opt.stages < 0) return RMSNORM_ERR_INVALID_ARG;
+    int64_t slots = c.opt.stages ? c.opt.stages : budget / chunk;
+    if (!c.opt.stages && slots > kStagedMaxSlotsHost) slots = kStagedMaxSlotsHost;
+    if (slots < 2 || slots > kStagedMaxSlotsHost || slots * chunk > budget)
+        return RMSNORM_ERR_UNSUPPORTED;
+    KernelFn fn = rmsnorm_grid_kernel_ptr(c.dtype, v, c.opt.epilogue);
+    if (!fn) return RMSNORM_ERR_UNSUPPORTED;
+    const int block = nc + 32;
+    const int smem = static_cast<int>(kStreamHeaderHost + slots * chunk);
+    int occ = 0;
+    if (cached_occupancy(c.dev, c.info->smem_optin, fn, block, smem, 1, &occ) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
+    int64_t resident = static_cast<int64_t>(c.info->sms) * occ;
+    if (resident > kGridMaxCtasHost) resident = kGridMaxCtasHost;
+    if (c.opt.grid > resident) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t grid = c.opt.grid > 0 ? c.opt.grid : resident;
+    // the arrival counter counts grid * rows arrivals in 32 bits
+    if (c.rows > 0xFFFFFFFFll / grid) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t slice = (nvec + grid - 1) / grid;
+    const int64_t nchunks = (slice * 16 + chunk - 1) / chunk;
+    P->path = RMSNORM_PATH_GRID;
+    P->cluster = 1;
+    P->group = nc;
+    P->block = block;
+    P->rpc = 1;
+    P->grid = static_cast<int>(grid);
+    P->vb = 16;
+    P->nv = v;
+    P->smem = smem;
+    P->chunk = static_cast<int>(chunk);
+    P->nchunks = static_cast<int>(nchunks);
+    P->nslots = static_cast<int>(slots);
+    P->w_staged = 0;
+    P->nvec = static_cast<int>(nvec);
+    P->slice_vecs = static_cast<int>(slice);
+    P->scratch = grid_scratch_bytes(static_cast<int>(grid));
+    P->fn = fn;
+    P->name = "grid_stream";
+    return RMSNORM_OK;
+}
+
 // The write-up's own schedule (comparison only): one CTA of 256 threads per
 // row, the whole row staged in shared memory as fp32.
 rmsnorm_status_t plan_page(const Call& c, Plan* P) {
@@ -502,6 +569,11 @@ rmsnorm_status_t plan_auto(const Call& c, Plan* P) {
     const bool split = c.rows < c.info->sms &&
                        (row_bytes > kRowregMaxRowBytes || c.rows * row_bytes >= kSplitMinBytes);
     if (split) {
+        // (The whole-grid split, RMSNORM_PATH_GRID, is not chosen here: on
+        // eight fp32 rows of 64 MiB it measured 51% of the HBM copy peak
+        // against 56% for the cluster two-pass split -- every row also reads
+        // all of w, as large as a row, and x's row and w together do not stay
+        // in L2 between the two reads.)
         int want = pow2_floor(c.info->sms / (c.rows > 0 ? c.rows : 1));
         if (want > kAutoMaxCluster) want = kAutoMaxCluster;
         while (want > 1 && row_bytes / want < 4096) want >>= 1;
@@ -574,6 +646,9 @@ rmsnorm_status_t make_plan(const Call& c, Plan* P) {
         case RMSNORM_PATH_RINGREG:
             if (cl > 1) return RMSNORM_ERR_INVALID_ARG;
             return plan_ringreg(c, P);
+        case RMSNORM_PATH_GRID:
+            if (cl > 1) return RMSNORM_ERR_INVALID_ARG;
+            return plan_grid(c, P);
         default:
             return RMSNORM_ERR_INVALID_ARG;
     }
@@ -652,6 +727,13 @@ rmsnorm_status_t run(int32_t dtype, const void* x, const void* w, void* y, int64
 
     LaunchShape s{P.grid, P.block, P.cluster, P.smem};
     if (ensure_prepared(c.dev, P.fn, c.info->smem_optin) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (P.scratch > 0) {
+        s.cooperative = true;
+        if (launch_with_pool_scratch(P.fn, s, stream, p, static_cast<size_t>(P.scratch)) !=
+            cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+        return RMSNORM_OK;
+    }
     if (note(launch_ex(P.fn, s, stream, p)) != cudaSuccess) return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }

@@ -71,6 +71,7 @@ struct Params {
     float alpha;           // epilogue scale (kEpiScale)
     unsigned* status;      // per-device status word
     uint64_t timeout_ns;   // limit for every bounded wait
+    void* scratch;         // grid-split kernels: cleared exchange records (else null)
 };
 
 // ------------------------------------------------------------ element types --

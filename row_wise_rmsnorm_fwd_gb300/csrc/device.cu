@@ -107,4 +107,18 @@ cudaError_t cached_occupancy(int dev, int smem_optin, KernelFn fn, int block, in
     return cudaSuccess;
 }
 
+cudaError_t launch_with_pool_scratch(KernelFn fn, const LaunchShape& s, cudaStream_t stream,
+                                     Params p, size_t bytes) {
+    void* scratch = nullptr;
+    cudaError_t e = cudaMallocAsync(&scratch, bytes, stream);
+    if (e != cudaSuccess) return note(e);
+    e = cudaMemsetAsync(scratch, 0, bytes, stream);
+    if (e == cudaSuccess) {
+        p.scratch = scratch;
+        e = launch_ex(fn, s, stream, p);
+    }
+    const cudaError_t f = cudaFreeAsync(scratch, stream);
+    return note(e != cudaSuccess ? e : f);
+}
+
 }  // namespace rmsnorm

@@ -32,5 +32,11 @@ cudaError_t ensure_prepared(int dev, KernelFn fn, int smem_optin);
 // 0 when the shape cannot launch.  Cached per device and shape.
 cudaError_t cached_occupancy(int dev, int smem_optin, KernelFn fn, int block, int smem,
                              int cluster, int* out);
+// Launch a grid-split kernel with a scratch area of `bytes` zeroed bytes in
+// p.scratch: taken from the current device's default memory pool in stream
+// order on `stream` (cudaMallocAsync), cleared there (cudaMemsetAsync), and
+// handed back after the launch (cudaFreeAsync).
+cudaError_t launch_with_pool_scratch(KernelFn fn, const LaunchShape& s, cudaStream_t stream,
+                                     Params p, size_t bytes);
 
 }  // namespace rmsnorm

@@ -1,0 +1,309 @@
+// k_grid.cuh -- RMSNorm and row softmax for few rows, each too wide for any
+// one cluster to keep on chip (rows of tens of MB): every row is split over
+// the whole grid, one CTA per SM, each CTA owning one contiguous slice of
+// every row (and of w), and the CTAs' partial results meet in a small global
+// scratch area (grid_post / grid_wait_fold, k_exchange.cuh).
+//
+// A row of 64 MiB fits L2 where the several rows a cluster-per-row split
+// keeps in flight do not, so the whole grid reads the row's slices once from
+// DRAM (first read, L2 evict_last) and the second read finds them in L2.
+// Rows are pipelined: CTA g streams, through its bulk-copy ring, its slice of
+// row 0 (first read), then for every row r, chunk by chunk, row r's chunk
+// again (second read: the outputs, with row r's result) followed by a chunk
+// of row r + 1 (its first read).  DRAM thus sees the writes of one row and
+// the reads of the next interleaved (as a streaming kernel's), not a read
+// phase, a stall and a write phase; and L2 holds about one row, since row
+// r's lines are read for the last time (evict_first) as fast as row r + 1's
+// arrive.  The grid fold of row r + 1 is split: a CTA posts its partial
+// (grid_post), reads the first kGridReadAhead chunks of row r + 2 while the
+// other CTAs arrive, and only then waits (grid_wait_fold); the second pass
+// of row r + 1 then interleaves with row r + 2's remaining chunks.
+//
+//   RMSNorm:  first read: sum of squares; the grid adds the CTA sums;
+//             second read: (x * rstd) * w (w's chunk follows x's in the ring,
+//             L2 evict_last: every row reads all of w).
+//   softmax:  first read: online (maximum, sum) pair per thread; the grid
+//             folds the CTA pairs; second read: exp(x - M) / S.
+//
+// One producer warp (lane 0: ring_push in the order above) and 15 consumer
+// warps; every wait is bounded (the status word records an expiry and the
+// kernel leaves cleanly).
+#pragma once
+#include "k_stream.cuh"
+
+namespace rmsnorm {
+
+enum : int { kGridOpRmsNorm = 0, kGridOpSoftmax = 1 };
+
+// Chunks of the next row a CTA reads while the grid's other CTAs arrive at
+// an exchange.
+#ifndef RMSNORM_GRID_READ_AHEAD
+#define RMSNORM_GRID_READ_AHEAD 4
+#endif
+constexpr int kGridReadAhead = RMSNORM_GRID_READ_AHEAD;
+
+#ifndef RMSNORM_GRID_FIRST_READ_POLICY
+#define RMSNORM_GRID_FIRST_READ_POLICY 0   // first reads: 0 L2 evict_last, 1 evict_normal
+#endif
+#ifndef RMSNORM_GRID_SECOND_READ_POLICY
+#define RMSNORM_GRID_SECOND_READ_POLICY 0  // second reads: 0 L2 evict_first, 1 evict_normal
+#endif
+
+// Per-thread statistic of a first read: RMSNorm a running sum of squares,
+// softmax a running (maximum, sum) pair; both summed in blocks of chunks each
+// started from zero (no fp32 chain grows with the row).
+template <int OP>
+struct GridStat {
+    float m = -INFINITY, s = 0.f;                 // running total
+    float bm = -INFINITY, b0 = 0.f, b1 = 0.f;     // the current block
+    int chunks = 0;
+    __device__ __forceinline__ void close_block() {
+        if constexpr (OP == kGridOpSoftmax) {
+            pair_fold(m, s, bm, b0);
+            bm = -INFINITY;
+            b0 = 0.f;
+        } else {
+            s += b0 + b1;
+            b0 = b1 = 0.f;
+        }
+    }
+    __device__ __forceinline__ void end_chunk() {
+        if (++chunks == kSumBlockChunks) {
+            close_block();
+            chunks = 0;
+        }
+    }
+};
+
+template <int OP, typename T, int V, int EPI>
+__global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params p) {
+    constexpr int EPV = VecTraits<T, 16>::kElems;
+    constexpr bool kSm = OP == kGridOpSoftmax;
+    extern __shared__ __align__(128) unsigned char smem[];
+    // header: full[32] | empty[32] | red[2][32] pairs | wpart[2][32] pairs
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kStagedMaxSlots;
+    float2* red = reinterpret_cast<float2*>(smem + 16 * kStagedMaxSlots);
+    float2* wpart = reinterpret_cast<float2*>(smem + 16 * kStagedMaxSlots + 512);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int NCW = static_cast<int>(blockDim.x >> 5) - 1;   // consumer warps
+    const int NC = NCW * 32;
+    const int NCH = p.nchunks, S = p.nslots, CB = p.chunk_bytes;
+    const int G = gridDim.x, g = blockIdx.x;
+    const int64_t row_bytes = static_cast<int64_t>(p.hidden) * sizeof(T);
+    const int64_t slice_nom = static_cast<int64_t>(p.slice_vecs) * 16;
+    const int64_t sbeg = static_cast<int64_t>(g) * slice_nom;
+    const int64_t send = sbeg + slice_nom < row_bytes ? sbeg + slice_nom : row_bytes;
+    const int64_t my_bytes = send > sbeg ? send - sbeg : 0;
+    const SlotRing ring{full, empty, smem + kStreamHeader, S, NCH, CB, my_bytes};
+    const int64_t rows = p.rows;
+
+    if (tid == 0) {
+        ring_init(ring, NCW);
+        fence_mbarrier_init_cluster();
+    }
+    __syncthreads();
+
+    // first reads of a row before the interleaved part (all of row 0's; the
+    // read-ahead of the later rows)
+    const int D = NCH < kGridReadAhead ? NCH : kGridReadAhead;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer --
+        if (lane == 0) {
+            const uint64_t keep = RMSNORM_GRID_FIRST_READ_POLICY == 0 ? policy_evict_last()
+                                                                      : policy_evict_normal();
+            const uint64_t wpol = policy_evict_last();
+            const uint64_t done = RMSNORM_GRID_SECOND_READ_POLICY == 0 ? policy_evict_first()
+                                                                       : policy_evict_normal();
+            const char* xb = static_cast<const char*>(p.x) + sbeg;
+            const char* wsrc = static_cast<const char*>(p.w) + sbeg;
+            RingCursorSeq c;
+            auto first = [&](int64_t r, int k) {
+                ring_push(p, ring, c, xb + r * row_bytes + static_cast<int64_t>(k) * CB,
+                          ring.chunk_len(k), keep, kSiteStagedEmpty);
+            };
+            for (int k = 0; k < NCH; ++k) first(0, k);
+            if (rows > 1)
+                for (int k = 0; k < D; ++k) first(1, k);
+            for (int64_t r = 0; r < rows && !c.abort; ++r) {
+                for (int k = 0; k < NCH; ++k) {
+                    const int64_t off = static_cast<int64_t>(k) * CB;
+                    const int len = ring.chunk_len(k);
+                    ring_push(p, ring, c, xb + r * row_bytes + off, len, done, kSiteStagedEmpty);
+                    if (!kSm) ring_push(p, ring, c, wsrc + off, len, wpol, kSiteStagedEmpty);
+                    if (r + 1 < rows && k + D < NCH) first(r + 1, k + D);
+                }
+                if (r + 2 < rows)
+                    for (int k = 0; k < D; ++k) first(r + 2, k);
+            }
+            ring_drain(p, ring, c);
+        }
+        __syncwarp();
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers --
+    const int ct = tid - 32;
+    const int cw = warp - 1;
+    int slot = 0;
+    uint32_t lap = 0;
+    bool ok = true;          // warp-uniform; false once a bounded wait expired
+    auto acquire = [&]() {
+        ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded<false>(smem_addr(&full[slot]), lap,
+                                                                    p.timeout_ns));
+        return ok;
+    };
+    auto release = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&empty[slot]));
+        if (++slot == S) {
+            slot = 0;
+            lap ^= 1u;
+        }
+    };
+    auto slot_base = [&]() {
+        return ring.slots + static_cast<int64_t>(slot) * CB + static_cast<int64_t>(ct) * 16;
+    };
+    const int64_t vstride = static_cast<int64_t>(NC) * 16;
+
+    // First read of chunk k (acquired) into the running statistic.
+    auto first_read = [&](int k, GridStat<OP>& st) {
+        const int nv = ring.chunk_len(k) >> 4;
+        Vec<16> raw[V];
+        stream_load<V, false>(raw, slot_base(), vstride, ct, NC, nv);
+        release();
+        if constexpr (kSm) {
+            const float2 ms = stream_fold<T, V, false>(raw, ct, NC, nv, make_float2(st.bm, st.b0));
+            st.bm = ms.x;
+            st.b0 = ms.y;
+        } else {
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                if (ct + i * NC < nv) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) {
+                        const float f = get<T, 16>(raw[i], e);
+                        if (e & 1) st.b1 = fmaf(f, f, st.b1); else st.b0 = fmaf(f, f, st.b0);
+                    }
+                }
+            }
+        }
+        st.end_chunk();
+    };
+    // Post this CTA's result for exchange `it` from every thread's statistic:
+    // warp butterfly, one slot per warp, fixed-order fold, grid_post.  False
+    // (uniform over the consumers) once a wait has run out.
+    auto post = [&](GridStat<OP>& st, uint32_t it) {
+        st.close_block();
+        float m = st.m, s = st.s;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float so = __shfl_xor_sync(0xffffffffu, s, o);
+            if constexpr (kSm) {
+                const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+                pair_fold(m, s, mo, so);
+            } else {
+                s += so;
+            }
+        }
+        const int b = it & 1;
+        if (lane == 0) red[b * 32 + cw] = make_float2(m, s);
+        if (named_bar_or(1, NC, !ok)) {
+            if (ct == 0) report_timeout(p.status, kSiteStagedFull);
+            return false;
+        }
+        if (ct == 0) {
+            m = -INFINITY;
+            s = 0.f;
+            for (int w = 0; w < NCW; ++w) {
+                if constexpr (kSm) {
+                    pair_fold(m, s, red[b * 32 + w].x, red[b * 32 + w].y);
+                } else {
+                    s += red[b * 32 + w].y;
+                }
+            }
+            grid_post(p.scratch, G, g, it, m, s, p);
+        }
+        return true;
+    };
+    // First reads of chunks [k0, k1) of the row after this one.
+    auto read_ahead = [&](GridStat<OP>& st, int k0, int k1) {
+        for (int k = k0; k < k1 && acquire(); ++k) first_read(k, st);
+    };
+
+    // row 0's first read and result
+    GridStat<OP> st;
+#pragma unroll 1
+    for (int k = 0; k < NCH && acquire(); ++k) first_read(k, st);
+    if (!post(st, 0)) return;
+    GridStat<OP> nst;
+    if (rows > 1) read_ahead(nst, 0, D);
+    float M, Ssum;
+    if (!grid_wait_fold<kSm>(p.scratch, G, 0, wpart, ct, NC, p, M, Ssum)) return;
+
+    char* ybase = static_cast<char*>(p.y) + sbeg + static_cast<int64_t>(ct) * 16;
+    for (int64_t r = 0; r < rows; ++r) {
+        const bool next = r + 1 < rows;
+        // the outputs' scale: RMSNorm rstd; softmax 1 / S with the row's
+        // offset, fused where row_exp_offset_ok allows, else exact
+        const float rstd = kSm ? 0.f : rsqrtf(fmaf(Ssum, p.inv_hidden, p.eps));
+        const bool fast = kSm && row_exp_offset_ok(M);
+        const float c = row_exp_bias<T>() - M * kLog2e;
+        const float Mu = M == -INFINITY ? 0.f : M;
+        const float inv = kSm ? (fast ? slice_offset_correction<T>(M, c) : 1.0f) / Ssum : 0.f;
+        const float ms = fast ? 0.f : Mu, cs = fast ? c : row_exp_bias<T>();
+        char* dst = ybase + r * row_bytes;
+#pragma unroll 1
+        for (int k = 0; k < NCH; ++k) {
+            const int nv = ring.chunk_len(k) >> 4;
+            // second read of row r, chunk k: the outputs
+            if (!acquire()) break;
+            Vec<16> xr[V];
+            stream_load<V, false>(xr, slot_base(), vstride, ct, NC, nv);
+            release();
+            Vec<16> wr[V];
+            if constexpr (!kSm) {
+                if (!acquire()) break;
+                stream_load<V, false>(wr, slot_base(), vstride, ct, NC, nv);
+                release();
+            }
+            char* cdst = dst + static_cast<int64_t>(k) * CB;
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                if (ct + i * NC < nv) {
+                    if constexpr (kSm) {
+                        RowVec<T, 16> e;
+                        e.widen(xr[i]);
+                        st_stream<16>(cdst + i * vstride, e.exp_shift_scaled(ms, cs, inv));
+                    } else {
+                        float o[EPV];
+#pragma unroll
+                        for (int j = 0; j < EPV; ++j)
+                            o[j] = epilogue<EPI>((get<T, 16>(xr[i], j) * rstd) *
+                                                     get<T, 16>(wr[i], j),
+                                                 p.alpha);
+                        st_stream<16>(cdst + i * vstride, pack<T, 16>(o));
+                    }
+                }
+            }
+            // first read of row r + 1, chunk k + D
+            if (next && k + D < NCH) {
+                if (!acquire()) break;
+                first_read(k + D, nst);
+            }
+        }
+        if (!next) break;
+        // (a consumer warp whose wait ran out arrives here with ok false; the
+        // named barrier in post makes the stop uniform)
+        const uint32_t it = static_cast<uint32_t>(r + 1);
+        if (!post(nst, it)) break;
+        nst = GridStat<OP>{};
+        if (r + 2 < rows) read_ahead(nst, 0, D);
+        if (!grid_wait_fold<kSm>(p.scratch, G, it, wpart, ct, NC, p, M, Ssum)) break;
+    }
+}
+
+}  // namespace rmsnorm

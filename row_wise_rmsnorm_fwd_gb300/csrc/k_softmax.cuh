@@ -395,6 +395,18 @@ __device__ __forceinline__ bool cluster_pair_allreduce(PairExchange* ex, float m
     return ok;
 }
 
+// Fold the pair (mo, so) into (m, s): each sum is of exponentials relative
+// to its own maximum; the result is relative to max(m, mo).  A pair whose
+// maximum is the result's keeps its sum unscaled, so two empty pairs (-inf,
+// 0) give (-inf, 0) rather than 0 * 2^NaN.
+__device__ __forceinline__ void pair_fold(float& m, float& s, float mo, float so) {
+    const float M = fmaxf(m, mo);
+    const float a = m == M ? s : s * exp2f((m - M) * kLog2e);
+    const float b = mo == M ? so : so * exp2f((mo - M) * kLog2e);
+    m = M;
+    s = a + b;
+}
+
 template <int NV>
 constexpr int softmax_max_threads() { return NV >= 4 ? 512 : 1024; }
 

@@ -28,7 +28,7 @@
 // only -inf entries keeps (-inf, 0) and adds nothing; a row of -inf, or with
 // a NaN or +inf, ends with a NaN sum and a NaN row, as the definition gives.
 #pragma once
-#include "k_softmax.cuh"
+#include "k_exchange.cuh"
 
 #ifndef RMSNORM_STREAM_FIRST_PASS_POLICY
 #define RMSNORM_STREAM_FIRST_PASS_POLICY 0   // L2 policy of pass A: 0 evict_last, 1 evict_normal
@@ -50,18 +50,6 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
-}
-
-// Fold the pair (mo, so) into (m, s): each sum is of exponentials relative
-// to its own maximum; the result is relative to max(m, mo).  A pair whose
-// maximum is the result's keeps its sum unscaled, so two empty pairs (-inf,
-// 0) give (-inf, 0) rather than 0 * 2^NaN.
-__device__ __forceinline__ void pair_fold(float& m, float& s, float mo, float so) {
-    const float M = fmaxf(m, mo);
-    const float a = m == M ? s : s * exp2f((m - M) * kLog2e);
-    const float b = mo == M ? so : so * exp2f((mo - M) * kLog2e);
-    m = M;
-    s = a + b;
 }
 
 // This thread's vectors of one chunk, raw (bf16: half the registers of the
@@ -108,19 +96,28 @@ __device__ __forceinline__ float2 stream_fold(const Vec<16> (&raw)[V], int q0, i
     return make_float2(mt, st + sums.total());
 }
 
-// Shared-memory header of the streamed kernel: full[32] | empty[32] |
-// red[2][32] pairs | the cluster pair exchange (split rows).
+// Shared-memory header of the streamed kernels: full[32] | empty[32] |
+// red[2][32] pairs | the cluster pair exchange (split rows), or the grid
+// kernels' warp slots (k_grid.cuh).
 constexpr int kStreamHeader = 2048;
 
+// Splits of a row over several CTAs (the whole-grid split is softmax_grid's,
+// k_grid.cuh).
+enum : int {
+    kSplitNone = 0,      // one CTA per row
+    kSplitCluster = 1,   // a thread-block cluster per row, pairs through DSMEM
+};
+
 // V: 16-byte vectors per consumer thread per chunk (chunk_bytes = 16 * V *
-// consumer threads).  CL: each row is split over a thread-block cluster of
-// p.cluster CTAs, CTA rank r streaming slice r (p.slice_vecs vectors) of its
-// cluster's rows; the CTAs' (maximum, sum) pairs cross the cluster once per
-// row through distributed shared memory (cluster_pair_allreduce, bounded
-// wait).  Splitting halves (for two CTAs) the bytes of rows in flight, which
-// the second read needs to find in L2.
-template <typename T, int V, bool CL>
+// consumer threads).  SPLIT = kSplitCluster: each row over a thread-block
+// cluster of p.cluster CTAs, CTA rank r streaming slice r (p.slice_vecs
+// vectors) of its cluster's rows; the CTAs' (maximum, sum) pairs cross the
+// cluster once per row through distributed shared memory
+// (cluster_pair_allreduce, bounded wait).  Splitting halves (for two CTAs)
+// the bytes of rows in flight, which the second read needs to find in L2.
+template <typename T, int V, int SPLIT>
 __global__ void __launch_bounds__(kStreamMaxThreads, 1) softmax_stream_kernel(const Params p) {
+    constexpr bool CL = SPLIT == kSplitCluster;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kStagedMaxSlots;
@@ -141,7 +138,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) softmax_stream_kernel(co
         unit = cluster_id_x();
         nunits = cluster_count_x();
     }
-    const int64_t slice_nom = CL ? static_cast<int64_t>(p.slice_vecs) * 16 : row_bytes;
+    const int64_t slice_nom = SPLIT != kSplitNone ? static_cast<int64_t>(p.slice_vecs) * 16
+                                                  : row_bytes;
     const int64_t sbeg = static_cast<int64_t>(rank) * slice_nom;
     const int64_t send = sbeg + slice_nom < row_bytes ? sbeg + slice_nom : row_bytes;
     const int64_t my_bytes = send > sbeg ? send - sbeg : 0;
@@ -200,7 +198,10 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) softmax_stream_kernel(co
 
         uint32_t it = 0;
         for (int64_t row = unit; row < p.rows; row += nunits, ++it) {
-            // pass A: the online (maximum, sum) pair of this thread's elements
+            // pass A: the online (maximum, sum) pair of this thread's elements,
+            // in blocks of chunks each folded from an empty pair (no fp32 chain
+            // grows with the row)
+            float mt = -INFINITY, st = 0.f;
             float2 ms = make_float2(-INFINITY, 0.f);
 #pragma unroll 1
             for (int k = 0; k < NCH && acquire(); ++k) {
@@ -215,8 +216,12 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) softmax_stream_kernel(co
                     release();
                     ms = stream_fold<T, V, false>(raw, ct, NC, nv, ms);
                 }
+                if ((k + 1) % kSumBlockChunks == 0) {
+                    pair_fold(mt, st, ms.x, ms.y);
+                    ms = make_float2(-INFINITY, 0.f);
+                }
             }
-            float mt = ms.x, st = ms.y;
+            pair_fold(mt, st, ms.x, ms.y);
             // the CTA's pair: warp butterfly, one slot per warp, fixed-order fold
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {

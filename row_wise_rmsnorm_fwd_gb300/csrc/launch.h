@@ -13,6 +13,7 @@ struct LaunchShape {
     int block;      // threads per CTA
     int cluster;    // CTAs per cluster (1 = plain launch)
     int smem;       // dynamic shared memory bytes
+    bool cooperative = false;   // all CTAs resident at once (grid-split kernels)
 };
 
 // Kernel instances; nullptr when the combination is not compiled.
@@ -56,6 +57,16 @@ int softmax_staged_max_threads();
 constexpr int kStreamHeaderHost = 2048;
 KernelFn softmax_stream_ptr(int dtype, int v, bool cluster);
 int softmax_stream_max_threads();
+// RMSNorm and row softmax with every row over the whole grid (few rows of
+// tens of MB): the streamed kernel's launch shape (producer warp + consumers
+// of v 16-byte vectors per chunk), cooperative, at most kGridMaxCtasHost
+// CTAs; Params.scratch = grid_scratch_bytes(grid) cleared bytes.
+KernelFn rmsnorm_grid_kernel_ptr(int dtype, int v, int epi);
+KernelFn softmax_grid_ptr(int dtype, int v);
+constexpr int kGridMaxCtasHost = 1024;
+constexpr int kGridCounterBytesHost = 128;
+constexpr int kGridScratchBytesHost = kGridCounterBytesHost + 2 * kGridMaxCtasHost * 8;
+inline int grid_scratch_bytes(int grid) { return kGridCounterBytesHost + 2 * grid * 8; }
 
 // Comparison kernel with the compiler write-up's schedule (one CTA per row).
 KernelFn page_kernel_ptr(int dtype);
@@ -84,15 +95,22 @@ inline cudaError_t launch_ex(KernelFn kernel, const LaunchShape& s, cudaStream_t
     cfg.blockDim = dim3(static_cast<unsigned>(s.block), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(s.smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
     if (s.cluster > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(s.cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(s.cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
     }
+    if (s.cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 

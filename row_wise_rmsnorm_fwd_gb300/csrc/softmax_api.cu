@@ -24,6 +24,8 @@ constexpr int64_t kSoftmaxUnsplitMaxVecs = 0x7FFFFFFFll - 1024;  // three-pass, 
 constexpr int64_t kSoftmaxStreamMinRowBytes = 128 << 10;   // streamed: rows of at least this
 constexpr int64_t kSoftmaxStreamMaxSlice = 400 << 10;      // streamed: split rows above this
 constexpr int kSoftmaxStreamMaxCluster = 8;
+constexpr int64_t kSoftmaxGridMinRowBytes = 16ll << 20;  // auto: rows over the whole grid
+constexpr int64_t kSoftmaxGridMinBytes = 96ll << 20;     // ... for few-row inputs this large
 
 struct SmCall {
     int dtype;
@@ -50,6 +52,7 @@ struct SmPlan {
     int nchunks = 0;       // staged path: copies per row
     int nslots = 0;        // staged path: ring slots
     int resident = 0;      // three-pass split: resident clusters
+    int scratch = 0;       // grid split: bytes of cleared scratch (cooperative launch)
     KernelFn fn = nullptr;
     const char* name = "";
 };
@@ -85,19 +88,20 @@ rmsnorm_status_t sm_validate(int32_t dtype, const void* x, const void* y, int64_
         if (o.fault_inject != 0 &&
             (!RMSNORM_FAULT_INJECT ||
              (o.fault_inject == 1 && o.path != RMSNORM_PATH_STAGED &&
-              o.path != RMSNORM_PATH_STREAM) ||
-             (o.fault_inject == 2 && o.path != RMSNORM_PATH_CLUSTER &&
+              o.path != RMSNORM_PATH_STREAM && o.path != RMSNORM_PATH_GRID) ||
+             (o.fault_inject == 2 && o.path != RMSNORM_PATH_CLUSTER && o.path != RMSNORM_PATH_GRID &&
               !((o.path == RMSNORM_PATH_STAGED || o.path == RMSNORM_PATH_TWOPASS ||
                  o.path == RMSNORM_PATH_STREAM) &&
                 o.cluster > 1))))
             return RMSNORM_ERR_UNSUPPORTED;
         if (o.path != RMSNORM_PATH_AUTO && o.path != RMSNORM_PATH_ROWREG &&
             o.path != RMSNORM_PATH_TWOPASS && o.path != RMSNORM_PATH_CLUSTER &&
-            o.path != RMSNORM_PATH_STAGED && o.path != RMSNORM_PATH_STREAM)
+            o.path != RMSNORM_PATH_STAGED && o.path != RMSNORM_PATH_STREAM &&
+            o.path != RMSNORM_PATH_GRID)
             return RMSNORM_ERR_INVALID_ARG;
         // chunk and ring sizes shape the ring kernels only
         if ((o.chunk_bytes || o.stages) && o.path != RMSNORM_PATH_STAGED &&
-            o.path != RMSNORM_PATH_STREAM)
+            o.path != RMSNORM_PATH_STREAM && o.path != RMSNORM_PATH_GRID)
             return RMSNORM_ERR_INVALID_ARG;
         if (o.chunk_bytes < 0 || o.chunk_bytes % 16 != 0 || o.stages < 0)
             return RMSNORM_ERR_INVALID_ARG;
@@ -458,6 +462,68 @@ rmsnorm_status_t sm_plan_stream(const SmCall& c, int cluster, SmPlan* P) {
 // 16384 64 in registers against 60 staged); narrower rows are held in
 // registers by the register kernel; what neither takes goes to the
 // three-pass kernel.
+// The streamed kernel with every row over the whole grid (few rows of tens
+// of MB): the CTA shape of sm_plan_stream, one CTA per SM, all resident (a
+// cooperative launch; opt->grid of them at most), each owning a contiguous
+// slice of every row; the CTAs' (maximum, sum) pairs meet in global scratch.
+rmsnorm_status_t sm_plan_stream_grid(const SmCall& c, SmPlan* P) {
+    int vb;
+    rmsnorm_status_t st = sm_pick_vb(c, &vb);
+    if (st != RMSNORM_OK) return st;
+    if (vb != 16 || c.opt.cluster > 1) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t row_bytes = c.cols * c.sz;
+    const int64_t nvec = row_bytes / 16;
+    const int max_nc = softmax_stream_max_threads() - 32;
+    const int nc = c.opt.threads > 0 ? c.opt.threads : max_nc;
+    if (nc % 32 != 0 || nc > max_nc) return RMSNORM_ERR_UNSUPPORTED;
+    int v = 4;
+    if (c.opt.chunk_bytes != 0) {
+        if (c.opt.chunk_bytes == 2 * 16 * nc) v = 2;
+        else if (c.opt.chunk_bytes == 4 * 16 * nc) v = 4;
+        else return RMSNORM_ERR_UNSUPPORTED;
+    }
+    const int64_t chunk = static_cast<int64_t>(16) * v * nc;
+    const int64_t budget = c.dv.smem_optin - kStreamHeaderHost;
+    int64_t slots = c.opt.stages ? c.opt.stages : budget / chunk;
+    if (!c.opt.stages && slots > kStagedMaxSlotsHost) slots = kStagedMaxSlotsHost;
+    if (slots < 2 || slots > kStagedMaxSlotsHost || slots * chunk > budget)
+        return RMSNORM_ERR_UNSUPPORTED;
+    KernelFn fn = softmax_grid_ptr(c.dtype, v);
+    if (!fn) return RMSNORM_ERR_UNSUPPORTED;
+    const int block = nc + 32;
+    const int smem = static_cast<int>(kStreamHeaderHost + slots * chunk);
+    int occ = 0;
+    if (cached_occupancy(c.dv.dev, c.dv.smem_optin, fn, block, smem, 1, &occ) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (occ <= 0) return RMSNORM_ERR_UNSUPPORTED;
+    int64_t resident = static_cast<int64_t>(c.dv.sms) * occ;
+    if (resident > kGridMaxCtasHost) resident = kGridMaxCtasHost;
+    if (c.opt.grid > resident) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t grid = c.opt.grid > 0 ? c.opt.grid : resident;
+    // the arrival counter counts grid * rows arrivals in 32 bits
+    if (c.rows > 0xFFFFFFFFll / grid) return RMSNORM_ERR_UNSUPPORTED;
+    const int64_t per = (nvec + grid - 1) / grid;
+    *P = SmPlan{};             // every field this plan does not set keeps its default
+    P->path = RMSNORM_PATH_GRID;
+    P->cluster = 1;
+    P->slice_vecs = static_cast<int>(per);
+    P->group = nc;
+    P->block = block;
+    P->rpc = 1;
+    P->grid = static_cast<int>(grid);
+    P->vb = 16;
+    P->nv = v;
+    P->nvec = static_cast<int>(nvec);
+    P->smem = smem;
+    P->chunk = static_cast<int>(chunk);
+    P->nchunks = static_cast<int>((per * 16 + chunk - 1) / chunk);
+    P->nslots = static_cast<int>(slots);
+    P->scratch = grid_scratch_bytes(static_cast<int>(grid));
+    P->fn = fn;
+    P->name = "softmax_grid_stream";
+    return RMSNORM_OK;
+}
+
 // The streamed kernel, automatically: rows of at least 128 KB that the
 // register-resident staged kernel cannot hold (fp32 rows of more than 32768
 // elements, bf16 rows of 65536 and more), from a quarter of the SM count of
@@ -510,10 +576,22 @@ rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
             return sm_plan_threepass(c, c.opt.cluster ? c.opt.cluster : 1, P);
         case RMSNORM_PATH_STAGED: return sm_plan_staged(c, c.opt.cluster ? c.opt.cluster : 1, P);
         case RMSNORM_PATH_STREAM: return sm_plan_stream(c, c.opt.cluster ? c.opt.cluster : 1, P);
+        case RMSNORM_PATH_GRID: return sm_plan_stream_grid(c, P);
         default: break;
     }
     const int64_t row_bytes = c.cols * c.sz;
     rmsnorm_status_t st;
+    // Few rows of tens of MB totalling more than L2 can hold at once: each
+    // row over the whole grid in turn, so that its second read finds it in
+    // L2.  Measured (% of the HBM copy peak, against the three-pass kernel
+    // split over clusters, which reads x three times): eight fp32 rows of
+    // 64 MiB 62 against 40 (clusters of 12), sixteen rows of 32 MiB 65
+    // against 31 (8), thirty-two rows of 16 MiB 52 against 45 (4).
+    if (c.rows < c.dv.sms && row_bytes >= kSoftmaxGridMinRowBytes &&
+        c.rows * row_bytes >= kSoftmaxGridMinBytes) {
+        st = sm_plan_stream_grid(c, P);
+        if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+    }
     if (sm_stream_eligible(c)) {
         st = sm_plan_stream_auto(c, P);
         if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
@@ -600,6 +678,13 @@ rmsnorm_status_t sm_run(int32_t dtype, const void* x, void* y, int64_t rows, int
     p.timeout_ns = c.opt.wait_timeout_ns ? c.opt.wait_timeout_ns : kDefaultTimeoutNs;
     LaunchShape s{P.grid, P.block, P.cluster, P.smem};
     if (ensure_prepared(c.dv.dev, P.fn, c.dv.smem_optin) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (P.scratch > 0) {
+        s.cooperative = true;
+        if (launch_with_pool_scratch(P.fn, s, stream, p, static_cast<size_t>(P.scratch)) !=
+            cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+        return RMSNORM_OK;
+    }
     if (note(launch_ex(P.fn, s, stream, p)) != cudaSuccess) return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }

@@ -69,6 +69,8 @@ CASES = [
     ("ring-to-register withholds a copy", dict(path="ringreg", fault_inject=1), (64, 16384)),
     ("two-pass cluster withholds a partial", dict(path="twopass", cluster=4, fault_inject=2),
      (8, 65536)),
+    ("grid withholds a copy", dict(path="grid", fault_inject=1), (3, 1 << 18)),
+    ("grid withholds a partial", dict(path="grid", fault_inject=2), (3, 1 << 18)),
 ]
 
 
@@ -130,6 +132,8 @@ SOFTMAX_CASES = [
      (16, 128256)),
     ("softmax stream cluster withholds a pair", dict(path="stream", cluster=2, fault_inject=2),
      (16, 128256)),
+    ("softmax grid withholds a copy", dict(path="grid", fault_inject=1), (3, 1 << 18)),
+    ("softmax grid withholds a pair", dict(path="grid", fault_inject=2), (3, 1 << 18)),
 ]
 
 

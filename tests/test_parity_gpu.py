@@ -171,7 +171,8 @@ FORCED = [
     ("ringreg", {"threads": 256}), ("ringreg", {"grid": 2}),
     ("twopass", {"cluster": 2}), ("twopass", {"cluster": 16}),
     ("twopass", {"cluster": 4, "threads": 96}), ("twopass", {"cluster": 3}),
-    ("twopass", {"cluster": 12}),
+    ("twopass", {"cluster": 12}), ("grid", {}), ("grid", {"grid": 5}), ("grid", {"stages": 2}),
+    ("grid", {"threads": 64, "grid": 100}),
 ]
 
 
@@ -287,7 +288,7 @@ def test_in_place(dtype, rows, hidden):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("path", ["auto", "rowreg", "staged", "cluster", "twopass", "page",
-                                  "ringreg"])
+                                  "ringreg", "grid"])
 def test_guard_regions_untouched(dtype, path):
     """Sentinels before and after y stay intact (no out-of-bounds stores)."""
     rows, hidden = 21, 4104
@@ -339,7 +340,7 @@ def test_eps_zero_zero_row_is_nan():
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("path", ["auto", "rowreg", "staged", "cluster", "twopass", "page",
-                                  "ringreg"])
+                                  "ringreg", "grid"])
 def test_deterministic(dtype, path):
     x, w = rand_case(64, 8192, dtype, seed=123)
     xc, wc = x.cuda(), w.cuda()
@@ -386,6 +387,7 @@ def test_plan_reports_families():
     ((1024, 24576), "f32", "twopass", 1024, 0),      # fp32 rows of 96 KB
     ((8, 262144), "bf16", "cluster_rowreg", 512, 8), # c5b: few wide rows
     ((2, 1 << 20), "f32", "twopass_cluster", 1024, 0),   # few rows of 4 MB
+    ((8, 1 << 24), "f32", "twopass_cluster", 1024, 0),   # w16m: rows of 64 MiB over clusters
 ])
 def test_automatic_choice(shape, dtype, kernel, lanes, nv):
     """The automatic kernel choice for representative shapes (a guard on the
@@ -408,6 +410,24 @@ def test_few_very_wide_rows_split_over_clusters():
     x = torch.empty(300, 1 << 20, device="cuda")   # many rows: one CTA per row
     p = binding.rmsnorm_plan(x, w)
     assert p["kernel"] == "twopass" and p["cluster"] == 1, p
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,hidden,extra", [
+    (3, 1 << 22, {}),                     # rows of 16 / 8 MB over the whole grid
+    (2, 4 * 300007 + 4, {"grid": 37}),    # ragged last slice, few CTAs
+    (5, 1 << 20, {"stages": 2, "chunk_bytes": 2 * 16 * 480}),
+    (1, 1024, {}),                        # a row shorter than the grid: most slices empty
+])
+def test_rows_over_the_whole_grid(dtype, rows, hidden, extra):
+    """Every row split over the whole (cooperatively launched) grid, the CTAs'
+    sums of squares meeting in global scratch; in place too."""
+    x, w = rand_case(rows, hidden, dtype, seed=rows + hidden % 1000)
+    ref = oracle_for(x, w, 1e-6)
+    xc, wc = x.cuda(), w.cuda()
+    compare(run(xc, wc, 1e-6, path="grid", **extra), ref, f"grid {extra} {dtype} {rows}x{hidden}")
+    run(xc, wc, 1e-6, y=xc, path="grid", **extra)
+    compare(xc, ref, f"grid in place {extra} {dtype} {rows}x{hidden}")
 
 
 def test_row_kernel_grid_has_about_three_row_blocks_per_cta():
@@ -433,7 +453,8 @@ def test_unsupported_forced_option_launches_nothing():
 
 EPI_PATHS = [("auto", {}), ("rowreg", {}), ("staged", {}), ("ringreg", {}),
              ("cluster", {"cluster": 2}),
-             ("cluster", {"cluster": 8}), ("twopass", {}), ("rowreg", {"vec_bytes": 4})]
+             ("cluster", {"cluster": 8}), ("twopass", {}), ("rowreg", {"vec_bytes": 4}),
+             ("grid", {})]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])

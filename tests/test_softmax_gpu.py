@@ -78,7 +78,7 @@ def test_width_sweep(dtype, cols):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("path,cluster", [("rowreg", 0), ("twopass", 0), ("staged", 0),
-                                          ("stream", 0),
+                                          ("stream", 0), ("grid", 0),
                                           ("cluster", 2), ("cluster", 4), ("cluster", 8),
                                           ("cluster", 16), ("twopass", 2), ("twopass", 16),
                                           ("twopass", 5), ("twopass", 12)])
@@ -142,7 +142,8 @@ def large_magnitude_rows(cols, seed):
     ("auto", 0, 4096), ("auto", 0, 32000), ("rowreg", 0, 4096), ("staged", 0, 32000),
     ("cluster", 4, 65536), ("twopass", 0, 65536), ("twopass", 4, 65536),
     ("staged", 2, 128256), ("staged", 4, 128256), ("stream", 0, 65536),
-    ("stream", 0, 128256), ("stream", 2, 128256), ("stream", 3, 100000)])
+    ("stream", 0, 128256), ("stream", 2, 128256), ("stream", 3, 100000), ("grid", 0, 128256),
+    ("grid", 0, 1 << 20)])
 def test_large_magnitude_rows(dtype, path, cluster, cols):
     """Rows with maxima from 2e6 to 3.38e38 (either sign) through every
     softmax kernel: finite results equal to the oracle's, no NaN rows."""
@@ -221,11 +222,11 @@ def test_stream_special_values(dtype):
     x[5, 100000:] = -float("inf")
     x = x.to(DT[dtype])
     ref = ref_for(x)
-    for cl in (0, 2, 4):
-        compare(run(x.cuda(), path="stream", cluster=cl), ref, f"stream C={cl} special {dtype}")
+    for path, cl in (("stream", 0), ("stream", 2), ("stream", 4), ("grid", 0)):
+        compare(run(x.cuda(), path=path, cluster=cl), ref, f"{path} C={cl} special {dtype}")
         xd = x.cuda()
-        run(xd, xd, path="stream", cluster=cl)
-        compare(xd, ref, f"stream C={cl} special in place {dtype}")
+        run(xd, xd, path=path, cluster=cl)
+        compare(xd, ref, f"{path} C={cl} special in place {dtype}")
 
 
 MAX_COLS = (1 << 31) - 1      # the widest row the ABI accepts
@@ -453,6 +454,7 @@ def test_guards_and_determinism(dtype):
     ((64, 128256), "bf16", "softmax_cluster_stream"),    # decode logits, 64 sequences
     ((8, 128256), "f32", "softmax_cluster_rowreg"),      # decode logits, 8 sequences
     ((2, 1 << 20), "f32", "softmax_cluster_threepass"),  # few rows of 4 MB
+    ((8, 1 << 24), "f32", "softmax_grid_stream"),        # rows of 64 MiB over the whole grid
     ((2048, 128255), "f32", "softmax_threepass"),        # rows not a multiple of 16 bytes
 ])
 def test_automatic_choice(shape, dtype, kernel):
