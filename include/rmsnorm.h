@@ -198,6 +198,38 @@ rmsnorm_status_t rmsnorm_fwd_ex(int32_t dtype, const void* x, const void* w, voi
                                 const rmsnorm_options_t* opt, rmsnorm_stream_t stream);
 
 /*
+ * rmsnorm_fwd_grid_noalloc -- the page has no counterpart: this is an
+ * interface variant, not part of the method.  The same result as
+ * rmsnorm_fwd_ex with opt->path = RMSNORM_PATH_GRID (every row split over the
+ * whole grid; meant for few rows of tens of MB), but the call allocates
+ * nothing: the kernel's exchange area (an arrival counter and the CTAs'
+ * partial sums, 16512 bytes at most: grids of up to 1024 CTAs) lives in a
+ * fixed device array inside the library instead of coming from the memory
+ * pool on every call.  For callers that may not allocate device memory while
+ * they run -- an engine or plugin host that owns every byte of device memory
+ * and accounts for it, code on a path that must not risk an allocation
+ * failing or blocking mid-step, or a process whose device has no usable
+ * stream-ordered memory pool.
+ *  - x, w, y, rows, hidden, eps and stream as for rmsnorm_fwd_f32 /
+ *    rmsnorm_fwd_bf16; dtype is RMSNORM_DTYPE_F32 or RMSNORM_DTYPE_BF16.
+ *    x, w, y and the row pitch must be 16-byte aligned, else
+ *    RMSNORM_ERR_UNSUPPORTED (nothing launched).
+ *  - RMSNORM_ERR_UNSUPPORTED too if the grid this device would launch needs
+ *    more exchange space than the array holds (more than 1024 CTAs).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before capturing any stream into a CUDA graph.
+ *  - Each call clears the part of the array it uses (cudaMemsetAsync on
+ *    `stream`) and then launches.  Every call on a device shares the one
+ *    array, so calls whose kernels can overlap on the GPU (other streams, or
+ *    other host threads) race with each other and give undefined results:
+ *    serialise them, or use rmsnorm_fwd_ex, whose scratch is per call.
+ */
+rmsnorm_status_t rmsnorm_fwd_grid_noalloc(int32_t dtype, const void* x, const void* w, void* y,
+                                          int64_t rows, int64_t hidden, float eps,
+                                          rmsnorm_stream_t stream);
+
+/*
  * rmsnorm_plan -- no passage of the page: a query of this library's launch
  * heuristics.  Fill *plan with what rmsnorm_fwd_ex(dtype, x, w, y, rows,
  * hidden, ., opt, .) would launch on the current device, without launching.

@@ -86,6 +86,8 @@ def open_library(path: str):
     lib.rmsnorm_fwd_ex.argtypes = [i32, vp, vp, vp, i64, i64, f32,
                                    ctypes.POINTER(rmsnorm_options_t), vp]
     lib.rmsnorm_fwd_ex.restype = ctypes.c_int
+    lib.rmsnorm_fwd_grid_noalloc.argtypes = [i32, vp, vp, vp, i64, i64, f32, vp]
+    lib.rmsnorm_fwd_grid_noalloc.restype = ctypes.c_int
     lib.rmsnorm_plan.argtypes = [i32, vp, vp, vp, i64, i64,
                                  ctypes.POINTER(rmsnorm_options_t),
                                  ctypes.POINTER(rmsnorm_plan_t)]
@@ -276,6 +278,22 @@ def rmsnorm_fwd_ex(x, w, y=None, eps: float = 1e-6, options=None, stream=None):
     if isinstance(options, dict):
         options = make_options(**options)
     return _fwd(dtype, x, w, y, eps, options, stream)
+
+
+def rmsnorm_fwd_grid_noalloc(x, w, y=None, eps: float = 1e-6, stream=None):
+    """The whole-grid kernel with the library's fixed exchange array: the C
+    call allocates no device memory (for callers that must not allocate).
+    Calls that can overlap on the GPU share that array and race."""
+    torch = _torch()
+    dtype = RMSNORM_DTYPE_F32 if x.dtype == torch.float32 else RMSNORM_DTYPE_BF16
+    if y is None:
+        y = torch.empty_like(x)
+    rows, hidden = _check_tensors(x, w, y, dtype)
+    st = load().rmsnorm_fwd_grid_noalloc(dtype, x.data_ptr(), w.data_ptr(), y.data_ptr(), rows,
+                                         hidden, float(eps), _stream_handle(stream) or None)
+    if st != RMSNORM_OK:
+        raise RmsnormError(st, "rmsnorm_fwd_grid_noalloc")
+    return y
 
 
 def rmsnorm_plan(x, w, y=None, options=None) -> dict:

@@ -738,6 +738,88 @@ rmsnorm_status_t run(int32_t dtype, const void* x, const void* w, void* y, int64
     return RMSNORM_OK;
 }
 
+// ------------------------------------------- the allocation-free grid call --
+//
+// rmsnorm_fwd_grid_noalloc runs the whole-grid kernel (RMSNORM_PATH_GRID) with
+// its exchange area in this file-scope device array instead of memory taken
+// from the pool per call, for callers that must not allocate.  Every GPU that
+// loads the library holds one copy of the array until the process exits.
+constexpr size_t kNoAllocScratchBytes = kGridScratchBytesHost;   // 16512 bytes: 1024 CTAs
+static __device__ __align__(256) unsigned char g_grid_scratch_noalloc[kNoAllocScratchBytes];
+
+// The array's device address, looked up once per device (with that device
+// current) on the first call there.
+struct NoAllocDevice {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    void* scratch = nullptr;
+};
+NoAllocDevice g_noalloc_dev[64];
+
+cudaError_t noalloc_scratch(int dev, void** out) {
+    if (dev < 0 || dev >= 64) return note(cudaErrorInvalidDevice);
+    NoAllocDevice& d = g_noalloc_dev[dev];
+    std::call_once(d.once, [&] {
+        d.err = cudaGetSymbolAddress(&d.scratch, g_grid_scratch_noalloc);
+    });
+    *out = d.scratch;
+    return note(d.err);
+}
+
+rmsnorm_status_t run_grid_noalloc(int32_t dtype, const void* x, const void* w, void* y,
+                                  int64_t rows, int64_t hidden, float eps, cudaStream_t stream) {
+    rmsnorm_options_t opt;
+    std::memset(&opt, 0, sizeof(opt));
+    opt.path = RMSNORM_PATH_GRID;
+    Call c;
+    rmsnorm_status_t st = validate(dtype, x, w, y, rows, hidden, &opt, &c);
+    if (st != RMSNORM_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.f) return RMSNORM_ERR_INVALID_ARG;
+    if (rows == 0) return RMSNORM_OK;
+    if (current_device(&c.view) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    c.info = &c.view;
+    c.dev = c.view.dev;
+    Plan P;
+    st = make_plan(c, &P);
+    if (st != RMSNORM_OK) return st;
+    // the grid this device launches must fit the fixed array
+    if (P.scratch <= 0 || static_cast<size_t>(P.scratch) > kNoAllocScratchBytes)
+        return RMSNORM_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    if (noalloc_scratch(c.dev, &scratch) != cudaSuccess) return RMSNORM_ERR_CUDA;
+
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = x;
+    p.w = w;
+    p.y = y;
+    p.rows = rows;
+    p.hidden = static_cast<int32_t>(hidden);
+    p.nvec = P.nvec;
+    p.inv_hidden = 1.0f / static_cast<float>(hidden);
+    p.eps = eps;
+    p.group = P.group;
+    p.rows_per_cta = P.rpc;
+    p.cluster = P.cluster;
+    p.slice_vecs = P.slice_vecs;
+    p.chunk_bytes = P.chunk;
+    p.nchunks = P.nchunks;
+    p.nslots = P.nslots;
+    p.alpha = 1.0f;
+    p.status = c.info->status;
+    p.timeout_ns = kDefaultTimeoutNs;
+    p.scratch = scratch;
+
+    LaunchShape s{P.grid, P.block, P.cluster, P.smem};
+    s.cooperative = true;
+    if (ensure_prepared(c.dev, P.fn, c.info->smem_optin) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    // the previous call's counter and partials are still there: clear them
+    if (note(cudaMemsetAsync(scratch, 0, static_cast<size_t>(P.scratch), stream)) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (note(launch_ex(P.fn, s, stream, p)) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    return RMSNORM_OK;
+}
+
 }  // namespace
 }  // namespace rmsnorm
 
@@ -830,6 +912,13 @@ int32_t rmsnorm_last_cuda_error(char* msg, size_t len) {
     if (msg && len > 0)
         std::snprintf(msg, len, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
     return static_cast<int32_t>(e);
+}
+
+rmsnorm_status_t rmsnorm_fwd_grid_noalloc(int32_t dtype, const void* x, const void* w, void* y,
+                                          int64_t rows, int64_t hidden, float eps,
+                                          rmsnorm_stream_t stream) {
+    return run_grid_noalloc(dtype, x, w, y, rows, hidden, eps,
+                            reinterpret_cast<cudaStream_t>(stream));
 }
 
 int32_t rmsnorm_abi_version(void) { return 10200; }
