@@ -10,9 +10,13 @@
  * The compiler write-up "A hackable Python ML compiler, part 2" lists such
  * small reductions (softmax inside SDPA) among the ops its generated kernels
  * win on, without printing a formula; this is the plain definition in the
- * stable form.  fp32 arithmetic (CUDA expf); bf16 inputs are widened exactly
- * and each output is rounded once.  IEEE semantics for special values: -inf
- * entries give 0; a row of -inf, or any NaN or +inf in a row, gives a NaN row.
+ * stable form.  fp32 arithmetic: exp(x - m) as a base-2 exponential of
+ * (x - m) * log2(e) (CUDA's exp2f for fp32 rows, one SFU instruction for bf16
+ * rows), the offset m * log2(e) fused into one FMA for rows whose maximum has
+ * |m| < 2^21 and subtracted exactly for larger or non-finite maxima; bf16
+ * inputs are widened exactly and each output is rounded once.  Every finite
+ * input is in the domain.  IEEE semantics for special values: -inf entries
+ * give 0; a row of -inf, or any NaN or +inf in a row, gives a NaN row.
  *
  *  - x, y: DEVICE pointers owned by the caller, rows*cols elements, contiguous
  *    row-major; y == x (in place) is allowed, any other overlap is rejected.
@@ -56,6 +60,16 @@ rmsnorm_status_t rowsoftmax_fwd_bf16(const uint16_t* x, uint16_t* y, int64_t row
  * zero for the defaults; opt->threads = threads per CTA, a multiple of 32 up
  * to 512; opt->cluster = 2..16 splits each row over a thread-block cluster,
  * maximum and sum combined through distributed shared memory) or
+ * RMSNORM_PATH_STREAM (rows streamed twice through a shared-memory ring by
+ * bulk copies: first read online maximum and sum, second read the outputs,
+ * normally from L2; 16-byte aligned rows, else RMSNORM_ERR_UNSUPPORTED;
+ * opt->cluster = 2..16 (any size) splits each row over a thread-block
+ * cluster; opt->threads = consumer threads (multiple of 32, <= 480),
+ * opt->chunk_bytes = 2 or 4 vectors of 16 bytes per consumer thread,
+ * opt->stages = ring slots), RMSNORM_PATH_GRID (every row over the whole
+ * grid, see rmsnorm.h: takes a scratch area of at most 17 KB from the
+ * device's memory pool in stream order; chosen automatically for fewer rows
+ * than SMs of 16 MB and more totalling 96 MB or more),
  * RMSNORM_PATH_TWOPASS (the wide-row kernel:
  * reads each row three times, the repeats normally from L2; opt->cluster =
  * 2..16 (any size; the other paths take powers of two) splits each row over
@@ -65,9 +79,10 @@ rmsnorm_status_t rowsoftmax_fwd_bf16(const uint16_t* x, uint16_t* y, int64_t row
  * RMSNORM_ERR_UNSUPPORTED); opt->threads,
  * opt->grid, opt->vec_bytes and opt->wait_timeout_ns as for rmsnorm_fwd_ex.
  * opt->fault_inject (failure-detection tests, test build of the library
- * only): 1 = STAGED withholds each CTA's first bulk copy, 2 = a split row
- * (CLUSTER, or STAGED or TWOPASS with cluster > 1) has CTA rank 0 withhold its first
- * (maximum, sum) pair; the bounded waits then expire (see
+ * only): 1 = STAGED, STREAM or GRID withholds each CTA's first bulk copy,
+ * 2 = a split row (CLUSTER or GRID, or STAGED, STREAM or TWOPASS with
+ * cluster > 1) has CTA rank 0 withhold its first (maximum, sum) pair; the
+ * bounded waits then expire (see
  * rmsnorm_last_device_status).  The product library, and any path without
  * that site, return RMSNORM_ERR_UNSUPPORTED; values outside 0..2 are
  * RMSNORM_ERR_INVALID_ARG.  chunk_bytes and stages with any other path, and

@@ -30,9 +30,6 @@
 #pragma once
 #include "k_exchange.cuh"
 
-#ifndef RMSNORM_STREAM_FIRST_PASS_POLICY
-#define RMSNORM_STREAM_FIRST_PASS_POLICY 0   // L2 policy of pass A: 0 evict_last, 1 evict_normal
-#endif
 
 namespace rmsnorm {
 
@@ -159,10 +156,10 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) softmax_stream_kernel(co
     if (warp == 0) {
         // ---------------------------------------------------------- producer --
         if (lane == 0) {
-            const uint64_t keep = RMSNORM_STREAM_FIRST_PASS_POLICY == 0 ? policy_evict_last()
-                                                                        : policy_evict_normal();
-            ring_produce(p, ring, unit, nunits, row_bytes, sbeg, keep, kSiteStagedEmpty, 2,
-                         policy_evict_first());
+            // first read evict_last (measured against evict_normal: prefill
+            // logits bf16 88.6 / 84.7%, fp32 C=2 83.1 / 81.6% of the HBM copy peak)
+            ring_produce(p, ring, unit, nunits, row_bytes, sbeg, policy_evict_last(),
+                         kSiteStagedEmpty, 2, policy_evict_first());
         }
         __syncwarp();
     } else {
