@@ -25,10 +25,10 @@
  *  - The call is asynchronous on `stream` (NULL = the legacy default stream)
  *    and allocates no memory, with one exception: the few-very-wide-rows
  *    kernel (RMSNORM_PATH_GRID: forced through rmsnorm_fwd_ex, and chosen
- *    automatically by the row softmax for fewer rows than SMs of 16 MB and
- *    more, totalling 96 MB or more) takes a scratch area of at most 17 KB from
- *    the current device's default memory pool in stream order and returns it
- *    on the same stream.  Argument errors are detected on the host before any
+ *    automatically for fewer rows than SMs of 10 to 32 MiB by RMSNorm and of
+ *    16 MiB and more, totalling 96 MiB or more, by the row softmax) takes a
+ *    scratch area of at most 17 KB from the current device's default memory
+ *    pool in stream order and returns it on the same stream.  Argument errors are detected on the host before any
  *    launch and leave the device untouched.
  *  - rows == 0 returns RMSNORM_OK without a launch.
  *  - The library's only device state is one status word per device, written
@@ -103,7 +103,7 @@ typedef enum {
                                   the device's default memory pool in stream order
                                   (cudaMallocAsync / cudaFreeAsync on `stream`); opt->grid
                                   = CTAs (at most one per SM), opt->threads = consumer
-                                  threads (multiple of 32, <= 480), opt->chunk_bytes =
+                                  threads (multiple of 32, <= 448), opt->chunk_bytes =
                                   2 or 4 vectors per consumer thread, opt->stages = ring
                                   slots (2..32) */
 } rmsnorm_path_t;

@@ -67,7 +67,8 @@ rmsnorm_status_t rowsoftmax_fwd_bf16(const uint16_t* x, uint16_t* y, int64_t row
  * cluster; opt->threads = consumer threads (multiple of 32, <= 480),
  * opt->chunk_bytes = 2 or 4 vectors of 16 bytes per consumer thread,
  * opt->stages = ring slots), RMSNORM_PATH_GRID (every row over the whole
- * grid, see rmsnorm.h: takes a scratch area of at most 17 KB from the
+ * grid, see rmsnorm.h; opt->threads = consumer threads, a multiple of 32 up
+ * to 448: takes a scratch area of at most 17 KB from the
  * device's memory pool in stream order; chosen automatically for fewer rows
  * than SMs of 16 MB and more totalling 96 MB or more),
  * RMSNORM_PATH_TWOPASS (the wide-row kernel:

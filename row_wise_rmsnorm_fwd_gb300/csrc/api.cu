@@ -40,6 +40,8 @@ constexpr int64_t kStagedMaxRowBytes = 65536;   // auto: fp32 staged up to here
 constexpr int kAutoMaxCluster = 8;              // auto: portable cluster sizes only
 constexpr int64_t kSplitMinBytes = 16 << 20;    // auto: split narrow few-row inputs from here
 constexpr int kRingregSlots = 3;                 // ring-to-register kernel: ring slots
+constexpr int64_t kGridMinRowBytes = 10ll << 20;     // auto: rows over the whole grid from here
+constexpr int64_t kGridMaxRowBytes = 32ll << 20;     //   to here
 constexpr int64_t kRingregLowMaxRowBytes = 57344;    // auto: ringreg for rows above 32 KB to here
 constexpr int64_t kRingregHighMinRowBytes = 114688;  // auto: and above this (to 128 KB)
 constexpr int64_t kUnsplitMaxVecs = 0x7FFFFFFFll - 1024;  // two-pass, one CTA per row: up to here
@@ -439,7 +441,8 @@ rmsnorm_status_t plan_grid(const Call& c, Plan* P) {
     if (c.opt.cluster > 1 || c.opt.weights != 0) return RMSNORM_ERR_UNSUPPORTED;
     const int64_t row_bytes = c.hidden * c.sz;
     const int64_t nvec = row_bytes / 16;
-    const int max_nc = softmax_stream_max_threads() - 32;
+    // one producer warp and one exchange warp beside the consumers
+    const int max_nc = softmax_stream_max_threads() - 64;
     const int nc = c.opt.threads > 0 ? c.opt.threads : max_nc;
     if (nc % 32 != 0 || nc > max_nc) return RMSNORM_ERR_UNSUPPORTED;
     int v = 4;
@@ -457,7 +460,7 @@ rmsnorm_status_t plan_grid(const Call& c, Plan* P) {
         return RMSNORM_ERR_UNSUPPORTED;
     KernelFn fn = rmsnorm_grid_kernel_ptr(c.dtype, v, c.opt.epilogue);
     if (!fn) return RMSNORM_ERR_UNSUPPORTED;
-    const int block = nc + 32;
+    const int block = nc + 64;
     const int smem = static_cast<int>(kStreamHeaderHost + slots * chunk);
     int occ = 0;
     if (cached_occupancy(c.dev, c.info->smem_optin, fn, block, smem, 1, &occ) != cudaSuccess)
@@ -569,11 +572,19 @@ rmsnorm_status_t plan_auto(const Call& c, Plan* P) {
     const bool split = c.rows < c.info->sms &&
                        (row_bytes > kRowregMaxRowBytes || c.rows * row_bytes >= kSplitMinBytes);
     if (split) {
-        // (The whole-grid split, RMSNORM_PATH_GRID, is not chosen here: on
-        // eight fp32 rows of 64 MiB it measured 51% of the HBM copy peak
-        // against 56% for the cluster two-pass split -- every row also reads
-        // all of w, as large as a row, and x's row and w together do not stay
-        // in L2 between the two reads.)
+        // Rows of 10 to 32 MiB: each over the whole grid in turn, its second
+        // read (and w) from L2.  Measured (% of the HBM copy peak, whole grid
+        // against the cluster two-pass split, which reads x twice): fp32 rows
+        // of 10 MiB 63 / 60, 12 MiB 70 / 60, 16 MiB 55-75 / 43-64 (4 to 150
+        // rows), 24 MiB 69 / 56, 32 MiB 56 / 55; bf16 rows of 12 MiB 68 / 60,
+        // 16 MiB 63-70 / 52-53, 32 MiB 55 / 54.  Outside that range the
+        // cluster split wins: rows of 8 MiB 58 / 60 (bf16 55 / 59), whose
+        // exchanges come too often, and of 40 and 64 MiB 51 / 61 and 51 / 57,
+        // which L2 does not keep beside w between the two reads.
+        if (row_bytes >= kGridMinRowBytes && row_bytes <= kGridMaxRowBytes) {
+            st = plan_grid(c, P);
+            if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;
+        }
         int want = pow2_floor(c.info->sms / (c.rows > 0 ? c.rows : 1));
         if (want > kAutoMaxCluster) want = kAutoMaxCluster;
         while (want > 1 && row_bytes / want < 4096) want >>= 1;

@@ -5,7 +5,8 @@
 
 namespace rmsnorm {
 
-static_assert(16 * kStagedMaxSlots + 4 * 32 * sizeof(float2) <= kStreamHeader,
+static_assert(16 * kStagedMaxSlots + 2 * 32 * sizeof(float2) + 4 * 8 + 2 * sizeof(float2) <=
+                  kStreamHeader,
               "grid kernel header overflows");
 static_assert(kGridMaxCtas == kGridMaxCtasHost && kGridScratchBytes == kGridScratchBytesHost &&
                   kGridCounterBytes == kGridCounterBytesHost,

@@ -5,19 +5,23 @@
 //
 // The exchange.  The scratch area holds an arrival counter (its own 128-byte
 // line) and two sets of G partials (G = CTAs in the grid), used by alternate
-// exchanges.  For exchange `it`, CTA g writes its partial into slot g of set
-// it & 1 with a relaxed store and then adds 1 to the counter with a release
-// reduction (gpu scope), which orders the partial before the arrival.  One
-// thread of every CTA then reads the counter with acquire loads until it
-// reaches G * (it + 1) (bounded by %globaltimer), fences, and passes a block
-// barrier; the CTA's threads read the G partials (relaxed, gpu scope: not
-// from L1) and fold them in slot order -- a butterfly in each warp, then the
-// warps in order -- so every CTA computes the bitwise same result.  A CTA
-// writes exchange it + 2's partial into a set only after the counter showed
-// that every CTA arrived at exchange it + 1, which each did only after
-// reading all of exchange it's partials: two sets suffice.  The host clears
-// the scratch before each launch, and the launch is cooperative, so all G
-// CTAs are resident at once and every wait can end.
+// exchanges.  For exchange `it`, CTA g's exchange warp adds the CTA's partial
+// into slot g of set it & 1 (which reads zero) and 1 to the counter, both
+// relaxed reductions (gpu scope): a release, or a plain store, would wait
+// behind every output store the SM still has in flight, microseconds on the
+// critical path.  It then reads the
+// counter with acquire loads until it reaches G * (it + 1) (bounded by
+// %globaltimer), and its 32 lanes read the G partials (relaxed, gpu scope:
+// not from L1), each slot again until it is non-zero -- a partial's bits
+// never are, and the arrival may be seen first -- and fold them in a fixed
+// order, so every CTA computes the bitwise same result.  A slot must read
+// zero, or the new partial, until it is rewritten: the host clears the
+// scratch before each launch, and after exchange it (which showed that every
+// CTA has read exchange it - 1's partials) each CTA clears its slot of the
+// set exchange it + 1 reuses, then issues a release fence; its next arrival
+// comes after that fence, so a CTA that sees it also sees the slot cleared.
+// The launch is cooperative, so all G CTAs are resident at once and every
+// wait can end.
 #pragma once
 #include "k_softmax.cuh"
 
@@ -39,8 +43,14 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void red_relaxed_add_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void red_relaxed_add(unsigned* p, unsigned v) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
     unsigned v;
@@ -48,9 +58,7 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
     return v;
 }
 
-// The exchange in two halves, so that a CTA can keep streaming while the
-// others arrive.  grid_post (one thread): this CTA's partial (a, b) for
-// exchange `it`.
+// grid_post (one thread): this CTA's partial (a, b) for exchange `it`.
 __device__ __forceinline__ void grid_post(void* scratch, int G, int g, uint32_t it, float a,
                                           float b, const Params& p) {
     unsigned* counter = static_cast<unsigned*>(scratch);
@@ -63,51 +71,95 @@ __device__ __forceinline__ void grid_post(void* scratch, int G, int g, uint32_t 
 #else
     (void)p;
 #endif
-    st_relaxed_u64(&set[g], (static_cast<unsigned long long>(__float_as_uint(b)) << 32) |
-                                __float_as_uint(a));
-    red_release_add(counter, 1u);
+    // the slot reads zero here: adding the partial writes it, by a reduction
+    // rather than a store, which would queue behind the SM's output stores
+    red_relaxed_add_u64(&set[g], (static_cast<unsigned long long>(__float_as_uint(b)) << 32) |
+                                     __float_as_uint(a));
+    red_relaxed_add(counter, 1u);
 }
 
-// grid_wait_fold (all NC consumer threads, warps 1.. of the CTA, named
-// barrier 1): wait until every CTA posted exchange `it`, then fold the G
-// partials.  kPair: (maximum, sum) pairs folded with pair_fold (the
-// online-softmax combine); else the sums b are added.  `wpart` is shared
-// memory for 2 x 32 warp slots.  Returns false (uniform over the consumers)
-// if the wait ran out (the status word then records it).
+// After exchange `it` (one thread of the exchange warp): clear this CTA's
+// slot in the set that exchange it + 1 reuses (it holds exchange it - 1's
+// partial, which every CTA has read: all of them posted exchange it), then a
+// release fence, so that a CTA that sees exchange it + 1's arrivals also sees
+// the slot cleared or rewritten, never the old partial.
+__device__ __forceinline__ void grid_clear_next(void* scratch, int G, int g, uint32_t it) {
+    unsigned long long* set = reinterpret_cast<unsigned long long*>(
+                                  static_cast<char*>(scratch) + kGridCounterBytes) +
+                              ((it + 1u) & 1u) * G;
+    if (it > 0) st_relaxed_u64(&set[g], 0ull);
+    fence_acq_rel_gpu();
+}
+
+// grid_exchange (the CTA's exchange warp, all 32 lanes; it issues no global
+// stores but these, so the release in grid_post waits for nothing else):
+// post this CTA's partial (a, b) for exchange `it`, wait until every CTA has
+// posted, then fold the G partials -- each lane the slots j = lane (mod 32)
+// in order, then a butterfly, lane 0's result taken -- so every CTA computes
+// the bitwise same (M, S).  kPair: (maximum, sum) pairs folded with pair_fold
+// (the online-softmax combine); else the sums b are added.  Returns false
+// (uniform over the warp) if the wait ran out (the status word records it).
 template <bool kPair>
-__device__ __forceinline__ bool grid_wait_fold(void* scratch, int G, uint32_t it, float2* wpart,
-                                               int ct, int NC, const Params& p, float& M,
-                                               float& S) {
+__device__ __forceinline__ bool grid_exchange(void* scratch, int G, int g, uint32_t it, float a,
+                                              float b, const Params& p, float& M, float& S) {
+    const int lane = threadIdx.x & 31;
     const unsigned* counter = static_cast<const unsigned*>(scratch);
     const unsigned long long* set = reinterpret_cast<const unsigned long long*>(
                                         static_cast<const char*>(scratch) + kGridCounterBytes) +
                                     (it & 1u) * G;
-    bool ok = true;
-    if (ct == 0) {
+    int ok = 1;
+    if (lane == 0) {
+        grid_post(scratch, G, g, it, a, b, p);
         const unsigned target = static_cast<unsigned>(G) * (it + 1u);
         if (static_cast<int>(ld_acquire_u32(counter) - target) < 0) {
             const uint64_t t0 = global_timer_ns();
             while (static_cast<int>(ld_acquire_u32(counter) - target) < 0) {
                 if (global_timer_ns() - t0 > p.timeout_ns) {
-                    ok = false;
+                    ok = 0;
                     report_timeout(p.status, kSiteClusterExchange);
                     break;
                 }
-                __nanosleep(64);
             }
         }
-        __threadfence();
     }
-    if (named_bar_or(1, NC, !ok)) return false;
+    // lane 0's acquire, then the warp barrier, orders every lane's reads of
+    // the partials after the other CTAs' posts
+    __syncwarp();
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
     float m = -INFINITY, s = 0.f;
-    for (int j = ct; j < G; j += NC) {
-        const unsigned long long d = ld_relaxed_u64(&set[j]);
-        const float ra = __uint_as_float(static_cast<uint32_t>(d));
-        const float rb = __uint_as_float(static_cast<uint32_t>(d >> 32));
-        if constexpr (kPair) {
-            pair_fold(m, s, ra, rb);
-        } else {
-            s += rb;
+    // the lane's slots j = lane (mod 32), eight loads in flight at a time,
+    // folded in slot order
+    constexpr int kBatch = 8;
+    for (int j0 = lane; j0 < G && ok; j0 += 32 * kBatch) {
+        unsigned long long d[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = j0 + 32 * u;
+            d[u] = j < G ? ld_relaxed_u64(&set[j]) : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = j0 + 32 * u;
+            if (j >= G || !ok) continue;
+            // the arrival can be seen before the partial: wait (bounded) for
+            // the slot to be written (a partial is never all-zero bits)
+            if (d[u] == 0ull) {
+                const uint64_t t0 = global_timer_ns();
+                while ((d[u] = ld_relaxed_u64(&set[j])) == 0ull) {
+                    if (global_timer_ns() - t0 > p.timeout_ns) {
+                        ok = 0;
+                        report_timeout(p.status, kSiteClusterExchange);
+                        break;
+                    }
+                }
+            }
+            const float ra = __uint_as_float(static_cast<uint32_t>(d[u]));
+            const float rb = __uint_as_float(static_cast<uint32_t>(d[u] >> 32));
+            if constexpr (kPair) {
+                pair_fold(m, s, ra, rb);
+            } else {
+                s += rb;
+            }
         }
     }
 #pragma unroll
@@ -120,22 +172,9 @@ __device__ __forceinline__ bool grid_wait_fold(void* scratch, int G, uint32_t it
             s += so;
         }
     }
-    const int NCW = NC >> 5;
-    float2* slots = wpart + (it & 1u) * 32;
-    if ((ct & 31) == 0) slots[ct >> 5] = make_float2(m, s);
-    named_bar_sync(1, NC);
-    m = -INFINITY;
-    s = 0.f;
-    for (int w = 0; w < NCW; ++w) {
-        if constexpr (kPair) {
-            pair_fold(m, s, slots[w].x, slots[w].y);
-        } else {
-            s += slots[w].y;
-        }
-    }
-    M = m;
-    S = s;
-    return true;
+    M = __shfl_sync(0xffffffffu, m, 0);
+    S = __shfl_sync(0xffffffffu, s, 0);
+    return __all_sync(0xffffffffu, ok);
 }
 
 // A producer lane's position in its CTA's chunk stream.

@@ -2,11 +2,12 @@
 // one cluster to keep on chip (rows of tens of MB): every row is split over
 // the whole grid, one CTA per SM, each CTA owning one contiguous slice of
 // every row (and of w), and the CTAs' partial results meet in a small global
-// scratch area (grid_post / grid_wait_fold, k_exchange.cuh).
+// scratch area (grid_exchange, k_exchange.cuh).
 //
-// A row of 64 MiB fits L2 where the several rows a cluster-per-row split
-// keeps in flight do not, so the whole grid reads the row's slices once from
-// DRAM (first read, L2 evict_last) and the second read finds them in L2.
+// One row in flight needs less L2 than the several rows a cluster-per-row
+// split keeps in flight, so the whole grid reads the row's slices from DRAM
+// (first read, L2 evict_last) and the second read finds them in L2 as far as
+// L2 keeps them.
 // Rows are pipelined: CTA g streams, through its bulk-copy ring, its slice of
 // row 0 (first read), then for every row r, chunk by chunk, row r's chunk
 // again (second read: the outputs, with row r's result) followed by a chunk
@@ -14,10 +15,13 @@
 // the reads of the next interleaved (as a streaming kernel's), not a read
 // phase, a stall and a write phase; and L2 holds about one row, since row
 // r's lines are read for the last time (evict_first) as fast as row r + 1's
-// arrive.  The grid fold of row r + 1 is split: a CTA posts its partial
-// (grid_post), reads the first kGridReadAhead chunks of row r + 2 while the
-// other CTAs arrive, and only then waits (grid_wait_fold); the second pass
-// of row r + 1 then interleaves with row r + 2's remaining chunks.
+// arrive.  The grid fold of row r + 1 runs beside the streaming: the
+// consumer warps hand their partials to the CTA's exchange warp (shared
+// memory, an mbarrier) and read the first kGridReadAhead chunks of row r + 2
+// while that warp posts the CTA's partial, waits for the other CTAs and folds
+// theirs; the consumers then take the row's result from it (shared memory,
+// a second mbarrier), and the second pass of row r + 1 interleaves with row
+// r + 2's remaining chunks.
 //
 //   RMSNorm:  first read: sum of squares; the grid adds the CTA sums;
 //             second read: (x * rstd) * w (w's chunk follows x's in the ring,
@@ -25,9 +29,16 @@
 //   softmax:  first read: online (maximum, sum) pair per thread; the grid
 //             folds the CTA pairs; second read: exp(x - M) / S.
 //
-// One producer warp (lane 0: ring_push in the order above) and 15 consumer
-// warps; every wait is bounded (the status word records an expiry and the
+// One producer warp (lane 0: ring_push in the order above), 14 consumer
+// warps and the exchange warp, whose polls, partial loads and release fence
+// (which waits for the SM's output stores in flight) run off the consumers'
+// path.  Every wait is bounded (the status word records an expiry and the
 // kernel leaves cleanly).
+//
+// Measured (fp32 softmax, 1 GB in and out): the second read finds the row in
+// L2 for rows of 16 MiB (DRAM reads 1.00 x the input), half of it for rows
+// of 32 MiB (1.36 x) and a sixth of it for rows of 64 MiB (1.87 x): L2 keeps
+// far less than its capacity of a row streamed beside its outputs.
 #pragma once
 #include "k_stream.cuh"
 
@@ -73,15 +84,18 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
     constexpr int EPV = VecTraits<T, 16>::kElems;
     constexpr bool kSm = OP == kGridOpSoftmax;
     extern __shared__ __align__(128) unsigned char smem[];
-    // header: full[32] | empty[32] | red[2][32] pairs | wpart[2][32] pairs
+    // header: full[32] | empty[32] | red[2][32] pairs | xbar[4] | xres[2] pairs
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kStagedMaxSlots;
     float2* red = reinterpret_cast<float2*>(smem + 16 * kStagedMaxSlots);
-    float2* wpart = reinterpret_cast<float2*>(smem + 16 * kStagedMaxSlots + 512);
+    // xbar[b]: the consumer warps' partials of exchanges b, b + 2, ... are in
+    // red[b]; xbar[2 + b]: the exchange's result is in xres[b]
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + 16 * kStagedMaxSlots + 512);
+    float2* xres = reinterpret_cast<float2*>(smem + 16 * kStagedMaxSlots + 512 + 32);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int NCW = static_cast<int>(blockDim.x >> 5) - 1;   // consumer warps
+    const int NCW = static_cast<int>(blockDim.x >> 5) - 2;   // consumer warps 1 .. NCW
     const int NC = NCW * 32;
     const int NCH = p.nchunks, S = p.nslots, CB = p.chunk_bytes;
     const int G = gridDim.x, g = blockIdx.x;
@@ -95,6 +109,10 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
 
     if (tid == 0) {
         ring_init(ring, NCW);
+        mbar_init(smem_addr(&xbar[0]), NCW);
+        mbar_init(smem_addr(&xbar[1]), NCW);
+        mbar_init(smem_addr(&xbar[2]), 1);
+        mbar_init(smem_addr(&xbar[3]), 1);
         fence_mbarrier_init_cluster();
     }
     __syncthreads();
@@ -132,6 +150,33 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
             ring_drain(p, ring, c);
         }
         __syncwarp();
+        return;
+    }
+
+    if (warp == NCW + 1) {
+        // ---------------------------------------------------------- exchange --
+        for (int64_t r = 0; r < rows; ++r) {
+            const uint32_t it = static_cast<uint32_t>(r), b = it & 1u;
+            if (!mbar_wait_bounded<false>(smem_addr(&xbar[b]), (it >> 1) & 1u, p.timeout_ns)) {
+                if (lane == 0) report_timeout(p.status, kSiteClusterExchange);
+                return;
+            }
+            float m = -INFINITY, s = 0.f;
+            for (int w = 0; w < NCW; ++w) {
+                if constexpr (kSm) {
+                    pair_fold(m, s, red[b * 32 + w].x, red[b * 32 + w].y);
+                } else {
+                    s += red[b * 32 + w].y;
+                }
+            }
+            float M, Ssum;
+            if (!grid_exchange<kSm>(p.scratch, G, g, it, m, s, p, M, Ssum)) return;
+            if (lane == 0) {
+                xres[b] = make_float2(M, Ssum);
+                mbar_arrive(smem_addr(&xbar[2 + b]));
+                if (r + 1 < rows) grid_clear_next(p.scratch, G, g, it);
+            }
+        }
         return;
     }
 
@@ -183,9 +228,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
         }
         st.end_chunk();
     };
-    // Post this CTA's result for exchange `it` from every thread's statistic:
-    // warp butterfly, one slot per warp, fixed-order fold, grid_post.  False
-    // (uniform over the consumers) once a wait has run out.
+    // Hand this warp's part of exchange `it` to the exchange warp: warp
+    // butterfly, one slot per warp, an arrival on xbar[it & 1].
     auto post = [&](GridStat<OP>& st, uint32_t it) {
         st.close_block();
         float m = st.m, s = st.s;
@@ -199,24 +243,23 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
                 s += so;
             }
         }
-        const int b = it & 1;
-        if (lane == 0) red[b * 32 + cw] = make_float2(m, s);
-        if (named_bar_or(1, NC, !ok)) {
-            if (ct == 0) report_timeout(p.status, kSiteStagedFull);
+        if (lane == 0) {
+            red[(it & 1u) * 32 + cw] = make_float2(m, s);
+            mbar_arrive(smem_addr(&xbar[it & 1u]));
+        }
+    };
+    // The result of exchange `it` (bounded wait); false once a wait ran out.
+    auto result = [&](uint32_t it, float& M, float& Ssum) {
+        ok = __all_sync(0xffffffffu,
+                        ok && mbar_wait_bounded<false>(smem_addr(&xbar[2 + (it & 1u)]),
+                                                       (it >> 1) & 1u, p.timeout_ns));
+        if (!ok) {
+            if (lane == 0) report_timeout(p.status, kSiteClusterExchange);
             return false;
         }
-        if (ct == 0) {
-            m = -INFINITY;
-            s = 0.f;
-            for (int w = 0; w < NCW; ++w) {
-                if constexpr (kSm) {
-                    pair_fold(m, s, red[b * 32 + w].x, red[b * 32 + w].y);
-                } else {
-                    s += red[b * 32 + w].y;
-                }
-            }
-            grid_post(p.scratch, G, g, it, m, s, p);
-        }
+        const float2 v = xres[it & 1u];
+        M = v.x;
+        Ssum = v.y;
         return true;
     };
     // First reads of chunks [k0, k1) of the row after this one.
@@ -228,11 +271,12 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
     GridStat<OP> st;
 #pragma unroll 1
     for (int k = 0; k < NCH && acquire(); ++k) first_read(k, st);
-    if (!post(st, 0)) return;
+    if (!ok) return;
+    post(st, 0);
     GridStat<OP> nst;
     if (rows > 1) read_ahead(nst, 0, D);
     float M, Ssum;
-    if (!grid_wait_fold<kSm>(p.scratch, G, 0, wpart, ct, NC, p, M, Ssum)) return;
+    if (!result(0, M, Ssum)) return;
 
     char* ybase = static_cast<char*>(p.y) + sbeg + static_cast<int64_t>(ct) * 16;
     for (int64_t r = 0; r < rows; ++r) {
@@ -285,14 +329,12 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
                 first_read(k + D, nst);
             }
         }
-        if (!next) break;
-        // (a consumer warp whose wait ran out arrives here with ok false; the
-        // named barrier in post makes the stop uniform)
+        if (!next || !ok) break;
         const uint32_t it = static_cast<uint32_t>(r + 1);
-        if (!post(nst, it)) break;
+        post(nst, it);
         nst = GridStat<OP>{};
         if (r + 2 < rows) read_ahead(nst, 0, D);
-        if (!grid_wait_fold<kSm>(p.scratch, G, it, wpart, ct, NC, p, M, Ssum)) break;
+        if (!result(it, M, Ssum)) break;
     }
 }
 

@@ -473,7 +473,8 @@ rmsnorm_status_t sm_plan_stream_grid(const SmCall& c, SmPlan* P) {
     if (vb != 16 || c.opt.cluster > 1) return RMSNORM_ERR_UNSUPPORTED;
     const int64_t row_bytes = c.cols * c.sz;
     const int64_t nvec = row_bytes / 16;
-    const int max_nc = softmax_stream_max_threads() - 32;
+    // one producer warp and one exchange warp beside the consumers
+    const int max_nc = softmax_stream_max_threads() - 64;
     const int nc = c.opt.threads > 0 ? c.opt.threads : max_nc;
     if (nc % 32 != 0 || nc > max_nc) return RMSNORM_ERR_UNSUPPORTED;
     int v = 4;
@@ -490,7 +491,7 @@ rmsnorm_status_t sm_plan_stream_grid(const SmCall& c, SmPlan* P) {
         return RMSNORM_ERR_UNSUPPORTED;
     KernelFn fn = softmax_grid_ptr(c.dtype, v);
     if (!fn) return RMSNORM_ERR_UNSUPPORTED;
-    const int block = nc + 32;
+    const int block = nc + 64;
     const int smem = static_cast<int>(kStreamHeaderHost + slots * chunk);
     int occ = 0;
     if (cached_occupancy(c.dv.dev, c.dv.smem_optin, fn, block, smem, 1, &occ) != cudaSuccess)
@@ -585,8 +586,10 @@ rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
     // row over the whole grid in turn, so that its second read finds it in
     // L2.  Measured (% of the HBM copy peak, against the three-pass kernel
     // split over clusters, which reads x three times): eight fp32 rows of
-    // 64 MiB 62 against 40 (clusters of 12), sixteen rows of 32 MiB 65
-    // against 31 (8), thirty-two rows of 16 MiB 52 against 45 (4).
+    // 64 MiB 62 against 40 (clusters of 12), sixteen rows of 32 MiB 74
+    // against 31 (8), thirty-two rows of 16 MiB 69 against 45 (4).  Rows of
+    // 8 MiB exchange too often: 50 against 67 for the streamed kernel split
+    // over clusters of 8 (fp32 and bf16 alike).
     if (c.rows < c.dv.sms && row_bytes >= kSoftmaxGridMinRowBytes &&
         c.rows * row_bytes >= kSoftmaxGridMinBytes) {
         st = sm_plan_stream_grid(c, P);

@@ -388,6 +388,11 @@ def test_plan_reports_families():
     ((8, 262144), "bf16", "cluster_rowreg", 512, 8), # c5b: few wide rows
     ((2, 1 << 20), "f32", "twopass_cluster", 1024, 0),   # few rows of 4 MB
     ((8, 1 << 24), "f32", "twopass_cluster", 1024, 0),   # w16m: rows of 64 MiB over clusters
+    ((12, 10 << 20), "f32", "twopass_cluster", 1024, 0), # rows of 40 MiB over clusters
+    ((32, 1 << 22), "f32", "grid_stream", 448, 4),       # rows of 16 MiB over the whole grid
+    ((16, 1 << 23), "bf16", "grid_stream", 448, 4),      # the same in bf16
+    ((40, 5 << 19), "f32", "grid_stream", 448, 4),       # rows of 10 MiB
+    ((64, 1 << 21), "f32", "twopass_cluster", 1024, 0),  # rows of 8 MiB: clusters again
 ])
 def test_automatic_choice(shape, dtype, kernel, lanes, nv):
     """The automatic kernel choice for representative shapes (a guard on the
@@ -397,6 +402,20 @@ def test_automatic_choice(shape, dtype, kernel, lanes, nv):
     p = binding.rmsnorm_plan(x, w)
     assert p["kernel"] == kernel, p
     assert p["threads_per_row"] == lanes and p["vecs_per_thread"] == nv, p
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_automatic_whole_grid_rows(dtype):
+    """Rows of 16 MiB that the automatic choice spreads over the whole grid
+    (cooperative launch, pool scratch), against the oracle; in place too."""
+    hidden = (1 << 22) if dtype == "f32" else (1 << 23)
+    x, w = rand_case(3, hidden, dtype, seed=41)
+    ref = oracle_for(x, w, 1e-6)
+    xc, wc = x.cuda(), w.cuda()
+    assert binding.rmsnorm_plan(xc, wc)["kernel"] == "grid_stream"
+    compare(run(xc, wc, 1e-6), ref, f"auto whole grid {dtype}")
+    run(xc, wc, 1e-6, y=xc)
+    compare(xc, ref, f"auto whole grid in place {dtype}")
 
 
 def test_few_very_wide_rows_split_over_clusters():
@@ -416,7 +435,7 @@ def test_few_very_wide_rows_split_over_clusters():
 @pytest.mark.parametrize("rows,hidden,extra", [
     (3, 1 << 22, {}),                     # rows of 16 / 8 MB over the whole grid
     (2, 4 * 300007 + 4, {"grid": 37}),    # ragged last slice, few CTAs
-    (5, 1 << 20, {"stages": 2, "chunk_bytes": 2 * 16 * 480}),
+    (5, 1 << 20, {"stages": 2, "chunk_bytes": 2 * 16 * 448}),
     (1, 1024, {}),                        # a row shorter than the grid: most slices empty
 ])
 def test_rows_over_the_whole_grid(dtype, rows, hidden, extra):
