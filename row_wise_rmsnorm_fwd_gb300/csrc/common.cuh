@@ -267,6 +267,22 @@ __device__ __forceinline__ void report_timeout(unsigned* status, unsigned site) 
     if (status) atomicCAS(status, 0u, kStatusTimeout | (site << 8));
 }
 
+// ------------------------------------------ programmatic dependent launch --
+// Every kernel is launched so that it may start while the kernel before it in
+// the stream is still running (launch.h).  pdl_trigger lets the next kernel's
+// CTAs be scheduled once every CTA of this one has issued it; pdl_wait blocks
+// until the kernels before this one have completed and their memory is
+// visible.  Each kernel issues pdl_wait before its first global memory access
+// (reads of x and w, which the previous kernel may write, and writes of y,
+// which it may read), so only launch latency and set-up overlap.  Both are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -81,6 +81,8 @@ struct GridStat {
 
 template <int OP, typename T, int V, int EPI>
 __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params p) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int EPV = VecTraits<T, 16>::kElems;
     constexpr bool kSm = OP == kGridOpSoftmax;
     extern __shared__ __align__(128) unsigned char smem[];

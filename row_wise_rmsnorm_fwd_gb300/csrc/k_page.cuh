@@ -88,6 +88,8 @@ __device__ __forceinline__ void write_normalised_row(T* out, const float* staged
 
 template <typename T>
 __global__ void __launch_bounds__(kPageThreads) page_kernel(const Params p) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ float staged[];            // the whole row, fp32
     __shared__ float slots[kPageWarps];
     const int n = p.hidden;

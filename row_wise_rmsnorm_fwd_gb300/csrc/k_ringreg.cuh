@@ -35,6 +35,8 @@ constexpr int kRingregMaxConsumers = 512;   // 16 consumer warps + the producer 
 // files of the SM sub-partitions; NV = 16 packed vectors take 64 of them.
 template <typename T, int NV, int M, int EPI>
 __global__ void __launch_bounds__(32 + kRingregMaxConsumers) ringreg_kernel(const Params p) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int EPV = 16 / static_cast<int>(sizeof(T));
     constexpr int NCHMAX = NV / M;                        // chunks a thread's vectors span
     static_assert(NV % M == 0, "M must divide NV");

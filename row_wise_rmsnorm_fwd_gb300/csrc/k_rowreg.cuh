@@ -44,6 +44,7 @@ rowreg_kernel(const Params p) {
     __shared__ float red[2][32];
     __shared__ ClusterExchange ex;
 
+    pdl_trigger();
     const int G = p.group;
     const int tid = threadIdx.x;
     const int g = tid / G;             // row group inside the CTA
@@ -62,6 +63,7 @@ rowreg_kernel(const Params p) {
         nunits = cluster_count_x();
         cluster_exchange_init(&ex);
     }
+    pdl_wait();
 
     // Vector indices this thread owns inside the row (or the CTA's slice).
     const int vbase = (ncta > 1) ? static_cast<int>(rank) * p.slice_vecs : 0;

@@ -422,6 +422,8 @@ constexpr int softmax_max_threads() { return NV >= 4 ? 512 : 1024; }
 template <typename T, int VB, int NV, bool PF, bool CL>
 __global__ void __launch_bounds__(softmax_max_threads<NV>())
 softmax_rowreg_kernel(const Params p) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[2][2][32];      // [max | sum][double buffer][warp]
     __shared__ PairExchange ex;        // cluster split only
 
@@ -577,6 +579,8 @@ constexpr int kSoftmaxStagedMaxThreads = 512;
 
 template <typename T, int NV, bool CL>
 __global__ void __launch_bounds__(kSoftmaxStagedMaxThreads) softmax_staged_kernel(const Params p) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     // header: full[32] | red[max|sum][buffer][16 warps] | the cluster pair exchange
@@ -737,6 +741,8 @@ constexpr int kSoftmaxWideThreads = 1024;
 
 template <typename T, int VB>
 __global__ void __launch_bounds__(kSoftmaxWideThreads) softmax_threepass_kernel(const Params p) {
+    pdl_trigger();
+    pdl_wait();
     // bf16 vectors of two or more elements: the packed-pair passes; fp32 (and
     // one-element) vectors: scalar code with one maximum chain and two sums,
     // which keeps the kernel at 32 registers and two 1024-thread CTAs per SM

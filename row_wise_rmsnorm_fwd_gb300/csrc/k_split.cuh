@@ -47,6 +47,8 @@ __device__ __forceinline__ void split_slice(const Params& p, uint32_t rank, uint
 
 template <typename T, int VB, int EPI>
 __global__ void __launch_bounds__(kSplitThreads, 1) twopass_cluster_kernel(const Params p) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int EPV = VecTraits<T, VB>::kElems;
     constexpr uint32_t U = kSplitReadBatch, U2 = kSplitWriteBatch;
     __shared__ float red[2][32];
@@ -145,6 +147,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1) twopass_cluster_kernel(const
 
 template <typename T, int VB>
 __global__ void __launch_bounds__(kSplitThreads, 1) softmax_threepass_cluster_kernel(const Params p) {
+    pdl_trigger();
+    pdl_wait();
     // bf16 vectors of two or more elements: the packed-pair passes; fp32 (and
     // one-element) vectors: scalar code.
     constexpr bool kPairs = sizeof(T) == 2 && VecTraits<T, VB>::kElems >= 2;

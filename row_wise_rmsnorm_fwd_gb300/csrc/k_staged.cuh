@@ -29,6 +29,8 @@ constexpr int kStagedUnroll = 4;                             // vectors per batc
 // that two 9-warp CTAs fit the register file of every SM sub-partition.
 template <typename T, int NCW, int EPI>
 __global__ void __maxnreg__(96) staged_kernel(const Params p) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int EPV = 16 / static_cast<int>(sizeof(T));
     constexpr int NC = 32 * NCW;
     extern __shared__ __align__(128) unsigned char smem[];

@@ -114,6 +114,8 @@ enum : int {
 // the bytes of rows in flight, which the second read needs to find in L2.
 template <typename T, int V, int SPLIT>
 __global__ void __launch_bounds__(kStreamMaxThreads, 1) softmax_stream_kernel(const Params p) {
+    pdl_trigger();
+    pdl_wait();
     constexpr bool CL = SPLIT == kSplitCluster;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);

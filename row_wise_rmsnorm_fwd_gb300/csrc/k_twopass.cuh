@@ -15,6 +15,8 @@ constexpr int kTwoPassThreads = 1024;
 
 template <typename T, int VB, int EPI>
 __global__ void __launch_bounds__(kTwoPassThreads) twopass_kernel(const Params p) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int EPV = VecTraits<T, VB>::kElems;
     __shared__ float red[2][32];
     const int tid = threadIdx.x;

@@ -95,7 +95,7 @@ inline cudaError_t launch_ex(KernelFn kernel, const LaunchShape& s, cudaStream_t
     cfg.blockDim = dim3(static_cast<unsigned>(s.block), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(s.smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     unsigned n = 0;
     if (s.cluster > 1) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
@@ -107,6 +107,12 @@ inline cudaError_t launch_ex(KernelFn kernel, const LaunchShape& s, cudaStream_t
     if (s.cooperative) {
         attr[n].id = cudaLaunchAttributeCooperative;
         attr[n].val.cooperative = 1;
+        ++n;
+    } else {
+        // may start before the previous kernel in the stream ends: its CTAs
+        // are placed and set up, then wait (pdl_wait) for that kernel's memory
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
         ++n;
     }
     cfg.attrs = n ? attr : nullptr;
