@@ -365,23 +365,36 @@ struct PairExchange {
     float2 slot[2][16];
 };
 
-__device__ __forceinline__ bool cluster_pair_allreduce(PairExchange* ex, float m, float s,
-                                                       int ncta, uint32_t rank, uint32_t it,
-                                                       const Params& p, float* M, float* S,
-                                                       int lt) {
+// The exchange in two halves, so that a CTA can keep working between them.
+// cluster_pair_send: this CTA's pair (m, s) of row iteration `it` to every
+// CTA of the cluster (threads lt < ncta send; lt == 0 arms the barrier).
+__device__ __forceinline__ void cluster_pair_send(PairExchange* ex, float m, float s, int ncta,
+                                                  uint32_t rank, uint32_t it, const Params& p,
+                                                  int lt) {
     const uint32_t b = it & 1u;
     const uint32_t bar = smem_addr(&ex->bar[b]);
     if (lt == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ncta) * 8u);
     bool send = lt < ncta;
 #if RMSNORM_FAULT_INJECT
     if (p.fault == kFaultClusterWithholdPartial && rank == 0 && it == 0) send = false;
+#else
+    (void)p;
 #endif
     if (send) {
         const uint32_t peer = static_cast<uint32_t>(lt);
         st_async_v2_f32(map_to_rank(smem_addr(&ex->slot[b][rank]), peer), m, s,
                         map_to_rank(bar, peer));
     }
-    const bool ok = mbar_wait_bounded<true>(bar, (it >> 1) & 1u, p.timeout_ns);
+}
+
+// cluster_pair_wait: wait (bounded) for every CTA's pair of iteration `it`
+// and fold them in rank order (every CTA gets the bitwise same result).
+// Returns false if the wait expired (the status word is then set).
+__device__ __forceinline__ bool cluster_pair_wait(PairExchange* ex, int ncta, uint32_t it,
+                                                  const Params& p, float* M, float* S, int lt) {
+    const uint32_t b = it & 1u;
+    const bool ok = mbar_wait_bounded<true>(smem_addr(&ex->bar[b]), (it >> 1) & 1u,
+                                            p.timeout_ns);
     float mx = -INFINITY, sum = 0.f;
     if (ok) {
         for (int c = 0; c < ncta; ++c) mx = fmaxf(mx, ex->slot[b][c].x);
@@ -393,6 +406,14 @@ __device__ __forceinline__ bool cluster_pair_allreduce(PairExchange* ex, float m
     *M = mx;
     *S = sum;
     return ok;
+}
+
+__device__ __forceinline__ bool cluster_pair_allreduce(PairExchange* ex, float m, float s,
+                                                       int ncta, uint32_t rank, uint32_t it,
+                                                       const Params& p, float* M, float* S,
+                                                       int lt) {
+    cluster_pair_send(ex, m, s, ncta, rank, it, p, lt);
+    return cluster_pair_wait(ex, ncta, it, p, M, S, lt);
 }
 
 // Fold the pair (mo, so) into (m, s): each sum is of exponentials relative

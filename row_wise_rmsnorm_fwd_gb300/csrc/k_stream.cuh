@@ -2,9 +2,11 @@
 // (prefill logits of a large vocabulary: rows of 128256 elements), every row
 // streamed twice through the bulk-copy slot ring of k_ring.cuh.
 //
-// One CTA per SM, one row at a time, no cluster: warp 0's lane 0 produces
-// (ring_produce with two passes per row: the row's chunks, then the same
-// chunks again), the other warps consume.
+// One CTA per SM (or a cluster of CTAs per row, each a slice), one row at a
+// time: warp 0's lane 0 produces (ring_push: the row's chunks, then the same
+// chunks again, with the next row's first kStreamReadAhead chunks between the
+// two so that DRAM stays busy while the CTA combines the row's pairs), the
+// other warps consume.
 //   pass A: each consumer thread keeps an online pair (m_t, s_t): the
 //     maximum of the elements it has seen and the sum of their exponentials
 //     relative to it; a chunk that raises m_t first rescales s_t.  At the
@@ -36,6 +38,12 @@ namespace rmsnorm {
 // 15 consumer warps + the producer: four warps per SM sub-partition, up to 128
 // registers a thread (a 17th warp would cap them at 96 and spill).
 constexpr int kStreamMaxThreads = 512;
+// Chunks of the next row a CTA of a split row reads while its cluster
+// combines a row's pairs.  Measured on fp32 prefill logits (1024 x 128256,
+// clusters of 2; % of the HBM copy peak): 0 / 1 / 2 / 3 / 4 / 6 chunks 83.6 /
+// 85.0 / 84.9 / 84.6 / 81.2 / 76.6.  Unsplit rows combine within the CTA and
+// read nothing ahead (2 chunks measured 1-2 points lower there).
+constexpr int kStreamReadAhead = 2;
 
 __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;
@@ -154,14 +162,38 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) softmax_stream_kernel(co
     }
     __syncthreads();
     if (CL) cluster_sync_all();        // no peer sends before the barriers exist
+    // chunks of the next row read while the cluster combines this row
+    const int D = !CL ? 0 : NCH < kStreamReadAhead ? NCH : kStreamReadAhead;
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer --
         if (lane == 0) {
             // first read evict_last (measured against evict_normal: prefill
-            // logits bf16 88.6 / 84.7%, fp32 C=2 83.1 / 81.6% of the HBM copy peak)
-            ring_produce(p, ring, unit, nunits, row_bytes, sbeg, policy_evict_last(),
-                         kSiteStagedEmpty, 2, policy_evict_first());
+            // logits bf16 88.6 / 84.7%, fp32 C=2 83.1 / 81.6% of the HBM copy
+            // peak), second read evict_first.  Order: row r's first read
+            // (less the chunks read ahead), the next row's first D chunks
+            // (read while the consumers combine row r), row r's second read.
+            const uint64_t keep = policy_evict_last(), done = policy_evict_first();
+            if (!CL) {
+                ring_produce(p, ring, unit, nunits, row_bytes, sbeg, keep, kSiteStagedEmpty, 2,
+                             done);
+            } else {
+                const char* xb = static_cast<const char*>(p.x) + sbeg;
+                RingCursorSeq c;
+                auto push = [&](int64_t row, int k0, int k1, uint64_t pol) {
+                    for (int k = k0; k < k1; ++k)
+                        ring_push(p, ring, c,
+                                  xb + row * row_bytes + static_cast<int64_t>(k) * CB,
+                                  ring.chunk_len(k), pol, kSiteStagedEmpty);
+                };
+                if (unit < p.rows) push(unit, 0, D, keep);
+                for (int64_t row = unit; row < p.rows && !c.abort; row += nunits) {
+                    push(row, D, NCH, keep);
+                    if (row + nunits < p.rows) push(row + nunits, 0, D, keep);
+                    push(row, 0, NCH, done);
+                }
+                ring_drain(p, ring, c);
+            }
         }
         __syncwarp();
     } else {
@@ -195,59 +227,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) softmax_stream_kernel(co
         const int64_t vstride = static_cast<int64_t>(NC) * 16;
         const int full_nv = V * NC;            // vectors of a full chunk
 
-        uint32_t it = 0;
-        for (int64_t row = unit; row < p.rows; row += nunits, ++it) {
-            // pass A: the online (maximum, sum) pair of this thread's elements,
-            // in blocks of chunks each folded from an empty pair (no fp32 chain
-            // grows with the row)
-            float mt = -INFINITY, st = 0.f;
-            float2 ms = make_float2(-INFINITY, 0.f);
-#pragma unroll 1
-            for (int k = 0; k < NCH && acquire(); ++k) {
-                const int nv = ring.chunk_len(k) >> 4;
-                Vec<16> raw[V];
-                if (nv == full_nv) {
-                    stream_load<V, true>(raw, slot_base(), vstride, ct, NC, nv);
-                    release();
-                    ms = stream_fold<T, V, true>(raw, ct, NC, nv, ms);
-                } else {
-                    stream_load<V, false>(raw, slot_base(), vstride, ct, NC, nv);
-                    release();
-                    ms = stream_fold<T, V, false>(raw, ct, NC, nv, ms);
-                }
-                if ((k + 1) % kSumBlockChunks == 0) {
-                    pair_fold(mt, st, ms.x, ms.y);
-                    ms = make_float2(-INFINITY, 0.f);
-                }
-            }
-            pair_fold(mt, st, ms.x, ms.y);
-            // the CTA's pair: warp butterfly, one slot per warp, fixed-order fold
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float mo = __shfl_xor_sync(0xffffffffu, mt, o);
-                const float so = __shfl_xor_sync(0xffffffffu, st, o);
-                pair_fold(mt, st, mo, so);
-            }
-            const int b = it & 1;
-            if (lane == 0) red[b * 32 + cw] = make_float2(mt, st);
-            if (named_bar_or(1, NC, !ok)) {
-                if (ct == 0) report_timeout(p.status, kSiteStagedFull);
-                break;
-            }
-            float M = -INFINITY, Ssum = 0.f;
-            for (int w = 0; w < NCW; ++w)
-                pair_fold(M, Ssum, red[b * 32 + w].x, red[b * 32 + w].y);
-            if (CL) {
-                // the row's pair from the cluster's CTA pairs (one exchange)
-                float Mr, Sr;
-                const bool cok =
-                    cluster_pair_allreduce(ex, M, Ssum, ncta, rank, it, p, &Mr, &Sr, ct);
-                if (named_bar_or(1, NC, !cok)) break;   // uniform: stop, leave cleanly
-                M = Mr;
-                Ssum = Sr;
-            }
-
-            // pass B: exp(x - M) / S from the same chunks again
+        // pass B: exp(x - M) / S from the same chunks again
+        auto pass_b = [&](int64_t row, float M, float Ssum) {
             const bool fast = row_exp_offset_ok(M);
             const float c = row_exp_bias<T>() - M * kLog2e;
             const float Mu = M == -INFINITY ? 0.f : M;
@@ -280,6 +261,108 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) softmax_stream_kernel(co
 #pragma unroll 1
                 for (int k = 0; k < NCH && acquire(); ++k)
                     pass_b_chunk(std::false_type{}, std::false_type{}, k, ring.chunk_len(k) >> 4);
+            }
+        };
+        // pass A on chunk k (acquired): fold it into the online (maximum, sum)
+        // pair (m, s) of this thread's elements; the pairs are summed in blocks
+        // of kSumBlockChunks chunks, each folded from an empty pair, into
+        // (mt, st) (no fp32 chain grows with the row)
+        auto first_read = [&](int k, float2& ms) {
+            const int nv = ring.chunk_len(k) >> 4;
+            Vec<16> raw[V];
+            if (nv == full_nv) {
+                stream_load<V, true>(raw, slot_base(), vstride, ct, NC, nv);
+                release();
+                ms = stream_fold<T, V, true>(raw, ct, NC, nv, ms);
+            } else {
+                stream_load<V, false>(raw, slot_base(), vstride, ct, NC, nv);
+                release();
+                ms = stream_fold<T, V, false>(raw, ct, NC, nv, ms);
+            }
+        };
+        // The CTA's pair of a row: warp butterfly, one slot per warp, a
+        // fixed-order fold in every thread.  False (uniform) once a wait ran
+        // out.
+        auto cta_pair = [&](float mt, float st, uint32_t it, float& M, float& Ssum) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float mo = __shfl_xor_sync(0xffffffffu, mt, o);
+                const float so = __shfl_xor_sync(0xffffffffu, st, o);
+                pair_fold(mt, st, mo, so);
+            }
+            const int b = it & 1;
+            if (lane == 0) red[b * 32 + cw] = make_float2(mt, st);
+            if (named_bar_or(1, NC, !ok)) {
+                if (ct == 0) report_timeout(p.status, kSiteStagedFull);
+                return false;
+            }
+            M = -INFINITY;
+            Ssum = 0.f;
+            for (int w = 0; w < NCW; ++w)
+                pair_fold(M, Ssum, red[b * 32 + w].x, red[b * 32 + w].y);
+            return true;
+        };
+
+        if constexpr (!CL) {
+            uint32_t it = 0;
+            for (int64_t row = unit; row < p.rows; row += nunits, ++it) {
+                float mt = -INFINITY, st = 0.f;
+                float2 ms = make_float2(-INFINITY, 0.f);
+#pragma unroll 1
+                for (int k = 0; k < NCH && acquire(); ++k) {
+                    first_read(k, ms);
+                    if ((k + 1) % kSumBlockChunks == 0) {
+                        pair_fold(mt, st, ms.x, ms.y);
+                        ms = make_float2(-INFINITY, 0.f);
+                    }
+                }
+                pair_fold(mt, st, ms.x, ms.y);
+                float M, Ssum;
+                if (!cta_pair(mt, st, it, M, Ssum)) break;
+                pass_b(row, M, Ssum);
+            }
+        } else {
+            // The next row's first D chunks are read while the cluster
+            // combines this row's pairs; a row's pass A then starts at D.
+            float2 ms = make_float2(-INFINITY, 0.f);
+            int n = 0;             // chunks folded into ms / the current block
+            float mt = -INFINITY, st = 0.f;
+            auto block = [&]() {
+                if (++n % kSumBlockChunks == 0) {
+                    pair_fold(mt, st, ms.x, ms.y);
+                    ms = make_float2(-INFINITY, 0.f);
+                }
+            };
+            if (unit < p.rows)
+                for (int k = 0; k < D && acquire(); ++k) {
+                    first_read(k, ms);
+                    block();
+                }
+            uint32_t it = 0;
+            for (int64_t row = unit; row < p.rows; row += nunits, ++it) {
+#pragma unroll 1
+                for (int k = D; k < NCH && acquire(); ++k) {
+                    first_read(k, ms);
+                    block();
+                }
+                pair_fold(mt, st, ms.x, ms.y);
+                float M, Ssum;
+                if (!cta_pair(mt, st, it, M, Ssum)) break;
+                // the row's pair from the cluster's CTA pairs (one exchange)
+                cluster_pair_send(ex, M, Ssum, ncta, rank, it, p, ct);
+                mt = -INFINITY;
+                st = 0.f;
+                ms = make_float2(-INFINITY, 0.f);
+                n = 0;
+                if (row + nunits < p.rows)
+                    for (int k = 0; k < D && acquire(); ++k) {
+                        first_read(k, ms);
+                        block();
+                    }
+                float Mr, Sr;
+                const bool cok = cluster_pair_wait(ex, ncta, it, p, &Mr, &Sr, ct) && ok;
+                if (named_bar_or(1, NC, !cok)) break;   // uniform: stop, leave cleanly
+                pass_b(row, Mr, Sr);
             }
         }
     }
