@@ -34,7 +34,8 @@ L2_BYTES = 129e6
 # Timed after the main region of the default run, same method and clocks: the
 # other graded RMSNorm config, the few-row split-row config, the few very wide
 # rows, and the prefill-logit row softmax.
-SECONDARY_DEFAULT = ("c4", "c5b", "w16m", "sm_prefill_f32", "sm_prefill_bf16", "sm_wide_f32")
+SECONDARY_DEFAULT = ("c4", "c5b", "w16m", "w4m", "sm_prefill_f32", "sm_prefill_bf16",
+                     "sm_wide_f32")
 METRIC = "RMSNorm GB/s and rows/s on 1 GB300; % of HBM roofline"
 METRIC_SOFTMAX = "row softmax GB/s and rows/s on 1 GB300; % of HBM roofline"
 

@@ -72,6 +72,7 @@ struct Params {
     unsigned* status;      // per-device status word
     uint64_t timeout_ns;   // limit for every bounded wait
     void* scratch;         // grid-split kernels: cleared exchange records (else null)
+    int32_t read_ahead;    // streamed split rows: next-row chunks read during an exchange
 };
 
 // ------------------------------------------------------------ element types --

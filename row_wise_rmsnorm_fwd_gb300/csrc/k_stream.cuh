@@ -3,10 +3,10 @@
 // streamed twice through the bulk-copy slot ring of k_ring.cuh.
 //
 // One CTA per SM (or a cluster of CTAs per row, each a slice), one row at a
-// time: warp 0's lane 0 produces (ring_push: the row's chunks, then the same
-// chunks again, with the next row's first kStreamReadAhead chunks between the
-// two so that DRAM stays busy while the CTA combines the row's pairs), the
-// other warps consume.
+// time: warp 0's lane 0 produces (the row's chunks, then the same chunks
+// again; for a split row, with the next row's first p.read_ahead chunks
+// between the two, so that DRAM keeps reading while the cluster combines the
+// row's pairs), the other warps consume.
 //   pass A: each consumer thread keeps an online pair (m_t, s_t): the
 //     maximum of the elements it has seen and the sum of their exponentials
 //     relative to it; a chunk that raises m_t first rescales s_t.  At the
@@ -38,12 +38,7 @@ namespace rmsnorm {
 // 15 consumer warps + the producer: four warps per SM sub-partition, up to 128
 // registers a thread (a 17th warp would cap them at 96 and spill).
 constexpr int kStreamMaxThreads = 512;
-// Chunks of the next row a CTA of a split row reads while its cluster
-// combines a row's pairs.  Measured on fp32 prefill logits (1024 x 128256,
-// clusters of 2; % of the HBM copy peak): 0 / 1 / 2 / 3 / 4 / 6 chunks 83.6 /
-// 85.0 / 84.9 / 84.6 / 81.2 / 76.6.  Unsplit rows combine within the CTA and
-// read nothing ahead (2 chunks measured 1-2 points lower there).
-constexpr int kStreamReadAhead = 2;
+
 
 __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;
@@ -162,8 +157,12 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) softmax_stream_kernel(co
     }
     __syncthreads();
     if (CL) cluster_sync_all();        // no peer sends before the barriers exist
-    // chunks of the next row read while the cluster combines this row
-    const int D = !CL ? 0 : NCH < kStreamReadAhead ? NCH : kStreamReadAhead;
+    // chunks of the next row read while the cluster combines this row (the
+    // planner's choice: measured on fp32 prefill logits, clusters of 2, %
+    // of the HBM copy peak, 0 / 1 / 2 / 3 / 4 / 6 chunks 83.6 / 85.0 / 84.9 /
+    // 84.6 / 81.2 / 76.6; unsplit rows combine within the CTA and read
+    // nothing ahead -- 2 chunks measured 1-2 points lower there)
+    const int D = !CL ? 0 : NCH < p.read_ahead ? NCH : p.read_ahead;
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer --
@@ -174,7 +173,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) softmax_stream_kernel(co
             // (less the chunks read ahead), the next row's first D chunks
             // (read while the consumers combine row r), row r's second read.
             const uint64_t keep = policy_evict_last(), done = policy_evict_first();
-            if (!CL) {
+            if (D == 0) {
                 ring_produce(p, ring, unit, nunits, row_bytes, sbeg, keep, kSiteStagedEmpty, 2,
                              done);
             } else {
@@ -303,7 +302,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) softmax_stream_kernel(co
             return true;
         };
 
-        if constexpr (!CL) {
+        if (D == 0) {
             uint32_t it = 0;
             for (int64_t row = unit; row < p.rows; row += nunits, ++it) {
                 float mt = -INFINITY, st = 0.f;
@@ -319,6 +318,15 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) softmax_stream_kernel(co
                 pair_fold(mt, st, ms.x, ms.y);
                 float M, Ssum;
                 if (!cta_pair(mt, st, it, M, Ssum)) break;
+                if (CL) {
+                    // the row's pair from the cluster's CTA pairs (one exchange)
+                    float Mr, Sr;
+                    const bool cok =
+                        cluster_pair_allreduce(ex, M, Ssum, ncta, rank, it, p, &Mr, &Sr, ct);
+                    if (named_bar_or(1, NC, !cok)) break;   // uniform: stop, leave cleanly
+                    M = Mr;
+                    Ssum = Sr;
+                }
                 pass_b(row, M, Ssum);
             }
         } else {

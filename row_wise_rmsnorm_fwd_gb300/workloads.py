@@ -131,6 +131,9 @@ WORKLOADS = {
         Workload("w16m", 9, (8, 1 << 24), "f32", ("normal", 0.0, 1.0),
                  ("normal", 1.0, 0.1), 1e-6,
                  description="few very wide fp32 rows (8,16777216), 64 MiB per row"),
+        Workload("w4m", 30, (32, 1 << 22), "f32", ("normal", 0.0, 1.0),
+                 ("normal", 1.0, 0.1), 1e-6,
+                 description="few wide fp32 rows (32,4194304), 16 MiB per row"),
     ]
 }
 

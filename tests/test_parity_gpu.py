@@ -74,7 +74,7 @@ def test_workload_page_schedule(name):
     check_case(x.reshape(-1, wl.hidden), w, wl.eps, f"page schedule {name}", path="page")
 
 
-@pytest.mark.parametrize("name", ["c4", "c5a", "w16m"])
+@pytest.mark.parametrize("name", ["c4", "c5a", "w16m", "w4m"])
 def test_workload_full_size_every_row(name):
     """Full-size workload in the bench's launch configuration (automatic
     path, current stream, inputs drawn on the device); every row is checked

@@ -162,6 +162,7 @@ def test_large_magnitude_rows(dtype, path, cluster, cols):
 @pytest.mark.parametrize("rows,cols,cluster,stages,grid", [
     (300, 128256, 2, 0, 0),           # prefill-logit rows over clusters of two
     (77, 262144, 4, 0, 0),            # clusters of four
+    (100, 262144, 2, 0, 0),           # rows in flight beyond the read-ahead bound
     (9, 100000, 3, 2, 6),             # odd cluster, two-slot ring, two clusters
     (5, 4104, 2, 0, 0),               # slices shorter than one chunk
     (3, 24, 2, 0, 0),                 # three vectors per row split over two CTAs
