@@ -30,6 +30,11 @@
  *    scratch area of at most 17 KB from the current device's default memory
  *    pool in stream order and returns it on the same stream.  Argument errors are detected on the host before any
  *    launch and leave the device untouched.
+ *  - Each kernel (all but the whole-grid one, a cooperative launch) is launched
+ *    so that its CTAs may be placed and set up before the kernel ahead of it on
+ *    `stream` has finished; it reads and writes no global memory until that
+ *    kernel has completed and its writes are visible (programmatic dependent
+ *    launch), so stream order holds as for any launch.
  *  - rows == 0 returns RMSNORM_OK without a launch.
  *  - The library's only device state is one status word per device, written
  *    by a kernel whose bounded wait ran out (see rmsnorm_last_device_status).

@@ -21,9 +21,12 @@
  *  - x, y: DEVICE pointers owned by the caller, rows*cols elements, contiguous
  *    row-major; y == x (in place) is allowed, any other overlap is rejected.
  *  - rows >= 0 (0: OK, no launch); 1 <= cols <= 2^31-1.
- *  - Asynchronous on `stream`; allocates nothing; argument errors are found on
- *    the host before any launch (RMSNORM_ERR_INVALID_ARG); a failed CUDA call
- *    returns RMSNORM_ERR_CUDA (see rmsnorm_last_cuda_error).
+ *  - Asynchronous on `stream`; allocates nothing but the whole-grid path's
+ *    scratch area (RMSNORM_PATH_GRID, as in rmsnorm.h); kernels are launched
+ *    as rmsnorm.h's common contract states (set-up may overlap the kernel
+ *    ahead, memory is touched only after it completes); argument errors are
+ *    found on the host before any launch (RMSNORM_ERR_INVALID_ARG); a failed
+ *    CUDA call returns RMSNORM_ERR_CUDA (see rmsnorm_last_cuda_error).
  */
 #ifndef ROWSOFTMAX_H_
 #define ROWSOFTMAX_H_
