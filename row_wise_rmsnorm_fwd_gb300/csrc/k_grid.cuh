@@ -17,7 +17,7 @@
 // r's lines are read for the last time (evict_first) as fast as row r + 1's
 // arrive.  The grid fold of row r + 1 runs beside the streaming: the
 // consumer warps hand their partials to the CTA's exchange warp (shared
-// memory, an mbarrier) and read the first kGridReadAhead chunks of row r + 2
+// memory, an mbarrier) and read the first p.read_ahead chunks of row r + 2
 // while that warp posts the CTA's partial, waits for the other CTAs and folds
 // theirs; the consumers then take the row's result from it (shared memory,
 // a second mbarrier), and the second pass of row r + 1 interleaves with row
@@ -46,12 +46,6 @@ namespace rmsnorm {
 
 enum : int { kGridOpRmsNorm = 0, kGridOpSoftmax = 1 };
 
-// Chunks of the next row a CTA reads while the grid's other CTAs arrive at
-// an exchange.  Measured on fp32 rows of 16 / 32 / 64 MiB (% of the HBM copy
-// peak): 1 / 4 / 8 / 12 chunks within 3 points of each other.  The L2 hints
-// (first reads evict_last, second reads evict_first) measured within 1 point
-// of evict_normal for both.
-constexpr int kGridReadAhead = 4;
 
 // Per-thread statistic of a first read: RMSNorm a running sum of squares,
 // softmax a running (maximum, sum) pair; both summed in blocks of chunks each
@@ -120,8 +114,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
     __syncthreads();
 
     // first reads of a row before the interleaved part (all of row 0's; the
-    // read-ahead of the later rows)
-    const int D = NCH < kGridReadAhead ? NCH : kGridReadAhead;
+    // read-ahead of the later rows, p.read_ahead chunks: the planner's choice)
+    const int D = NCH < p.read_ahead ? NCH : p.read_ahead;
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer --

@@ -531,6 +531,12 @@ rmsnorm_status_t sm_plan_stream_grid(const SmCall& c, SmPlan* P) {
     P->smem = smem;
     P->chunk = static_cast<int>(chunk);
     P->nchunks = static_cast<int>((per * 16 + chunk - 1) / chunk);
+    // Chunks of the next row read while the CTAs' pairs meet.  Measured on
+    // fp32 rows (% of the HBM copy peak; 1 / 2 / 3 / 4 / 8 chunks): rows of
+    // 16 MiB, four chunks per slice, 63.4 / 65.4 / 66.4 / 68.5 / 68.4 (the
+    // whole next slice); 32 MiB, eight chunks, 77.9 / 78.0 / 76.0 / 73.8 /
+    // 68.9; 64 MiB, sixteen chunks, 59.8 / 60.4 / 61.4 / 61.7 / 62.7.
+    P->read_ahead = P->nchunks <= 4 ? P->nchunks : P->nchunks <= 12 ? 2 : 4;
     P->nslots = static_cast<int>(slots);
     P->scratch = grid_scratch_bytes(static_cast<int>(grid));
     P->fn = fn;
