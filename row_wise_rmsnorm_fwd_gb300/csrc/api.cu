@@ -42,6 +42,7 @@ constexpr int64_t kSplitMinBytes = 16 << 20;    // auto: split narrow few-row in
 constexpr int kRingregSlots = 3;                 // ring-to-register kernel: ring slots
 constexpr int64_t kGridMinRowBytes = 10ll << 20;     // auto: rows over the whole grid from here
 constexpr int kGridReadAheadRmsNorm = 2;             // see plan_grid
+constexpr int64_t kGridInterleavedMaxRowBytes = 24ll << 20;   // see plan_grid
 constexpr int64_t kGridMaxRowBytes = 32ll << 20;     //   to here
 constexpr int64_t kRingregLowMaxRowBytes = 57344;    // auto: ringreg for rows above 32 KB to here
 constexpr int64_t kRingregHighMinRowBytes = 114688;  // auto: and above this (to 128 KB)
@@ -78,6 +79,7 @@ struct Plan {
     int resident = 0;       // resident CTAs per SM, or resident clusters (split rows)
     int scratch = 0;        // grid-split kernels: bytes of cleared scratch (cooperative launch)
     int read_ahead = 0;     // grid-split kernels: next-row chunks read during an exchange
+    int schedule = 0;       // grid-split kernels: row schedule
     KernelFn fn = nullptr;
     const char* name = "";
 };
@@ -497,6 +499,17 @@ rmsnorm_status_t plan_grid(const Call& c, Plan* P) {
     // peak): 1 / 2 / 3 / 4 / 8 chunks 71.8 / 74.3 / 73.5 / 72.0 / 72.4;
     // rows of 10 and 32 MiB within a point of each other at every depth.
     P->read_ahead = kGridReadAheadRmsNorm;
+    // Row schedule.  Measured (% of the HBM copy peak; interleaved / phased
+    // / phased with the second read reversed): fp32 rows of 16 MiB 74 / 65
+    // / 65, 24 MiB 65 / 62 / 63, 32 MiB 55 / 61 / 61, 40 MiB 50 / 56 / 57,
+    // 64 MiB 51 / 54 / 56; bf16 rows of 32 MiB 54 / 62 / 60, 64 MiB 50 /
+    // 52 / 55.  Interleaving keeps DRAM reading and writing at once, but
+    // lengthens the distance between a chunk's two reads to about two rows
+    // of traffic (the next row's reads and this row's writes), which L2
+    // holds only for rows of up to about 24 MiB.
+    P->schedule = row_bytes <= kGridInterleavedMaxRowBytes ? 0
+                  : row_bytes <= kGridMaxRowBytes          ? 1
+                                                           : 2;
     P->fn = fn;
     P->name = "grid_stream";
     return RMSNORM_OK;
@@ -738,6 +751,7 @@ rmsnorm_status_t run(int32_t dtype, const void* x, const void* w, void* y, int64
     p.nchunks = P.nchunks;
     p.nslots = P.nslots;
     p.read_ahead = P.read_ahead;
+    p.schedule = P.schedule;
     p.w_staged = P.w_staged;
     p.fault = c.opt.fault_inject;
     p.alpha = c.opt.epilogue == 1 ? c.opt.epilogue_alpha : 1.0f;
@@ -825,6 +839,7 @@ rmsnorm_status_t run_grid_noalloc(int32_t dtype, const void* x, const void* w, v
     p.nchunks = P.nchunks;
     p.nslots = P.nslots;
     p.read_ahead = P.read_ahead;
+    p.schedule = P.schedule;
     p.alpha = 1.0f;
     p.status = c.info->status;
     p.timeout_ns = kDefaultTimeoutNs;

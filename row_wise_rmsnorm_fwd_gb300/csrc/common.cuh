@@ -73,6 +73,7 @@ struct Params {
     uint64_t timeout_ns;   // limit for every bounded wait
     void* scratch;         // grid-split kernels: cleared exchange records (else null)
     int32_t read_ahead;    // streamed split rows: next-row chunks read during an exchange
+    int32_t schedule;      // grid-split kernels: row schedule (k_grid.cuh)
 };
 
 // ------------------------------------------------------------ element types --

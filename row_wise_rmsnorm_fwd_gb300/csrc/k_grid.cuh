@@ -23,6 +23,12 @@
 // a second mbarrier), and the second pass of row r + 1 interleaves with row
 // r + 2's remaining chunks.
 //
+// That interleaving puts about two rows of traffic (the next row's reads,
+// this row's writes) between a chunk's two reads, more than L2 keeps for the
+// widest rows; for those the planner takes a phased schedule (p.schedule):
+// row r's whole second read, then row r + 1's first read (after the chunks
+// read ahead), with the second read in chunk order or reversed.
+//
 //   RMSNorm:  first read: sum of squares; the grid adds the CTA sums;
 //             second read: (x * rstd) * w (w's chunk follows x's in the ring,
 //             L2 evict_last: every row reads all of w).
@@ -45,6 +51,11 @@
 namespace rmsnorm {
 
 enum : int { kGridOpRmsNorm = 0, kGridOpSoftmax = 1 };
+// Row schedules (p.schedule): the second read of row r interleaved chunk by
+// chunk with the first read of row r + 1; or phased -- row r's second read,
+// then row r + 1's first read -- with the second read in chunk order or
+// reversed.
+enum : int { kGridInterleaved = 0, kGridPhased = 1, kGridPhasedReversed = 2 };
 
 
 // Per-thread statistic of a first read: RMSNorm a running sum of squares,
@@ -116,6 +127,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
     // first reads of a row before the interleaved part (all of row 0's; the
     // read-ahead of the later rows, p.read_ahead chunks: the planner's choice)
     const int D = NCH < p.read_ahead ? NCH : p.read_ahead;
+    const int sched = p.schedule;
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer --
@@ -133,13 +145,16 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
             if (rows > 1)
                 for (int k = 0; k < D; ++k) first(1, k);
             for (int64_t r = 0; r < rows && !c.abort; ++r) {
-                for (int k = 0; k < NCH; ++k) {
+                for (int kk = 0; kk < NCH; ++kk) {
+                    const int k = sched == kGridPhasedReversed ? NCH - 1 - kk : kk;
                     const int64_t off = static_cast<int64_t>(k) * CB;
                     const int len = ring.chunk_len(k);
                     ring_push(p, ring, c, xb + r * row_bytes + off, len, done, kSiteStagedEmpty);
                     if (!kSm) ring_push(p, ring, c, wsrc + off, len, wpol, kSiteStagedEmpty);
-                    if (r + 1 < rows && k + D < NCH) first(r + 1, k + D);
+                    if (sched == kGridInterleaved && r + 1 < rows && kk + D < NCH) first(r + 1, kk + D);
                 }
+                if (sched != kGridInterleaved && r + 1 < rows)
+                    for (int k = D; k < NCH; ++k) first(r + 1, k);
                 if (r + 2 < rows)
                     for (int k = 0; k < D; ++k) first(r + 2, k);
             }
@@ -287,7 +302,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
         const float ms = fast ? 0.f : Mu, cs = fast ? c : row_exp_bias<T>();
         char* dst = ybase + r * row_bytes;
 #pragma unroll 1
-        for (int k = 0; k < NCH; ++k) {
+        for (int kk = 0; kk < NCH; ++kk) {
+            const int k = sched == kGridPhasedReversed ? NCH - 1 - kk : kk;
             const int nv = ring.chunk_len(k) >> 4;
             // second read of row r, chunk k: the outputs
             if (!acquire()) break;
@@ -320,12 +336,15 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
                 }
             }
             // first read of row r + 1, chunk k + D
-            if (next && k + D < NCH) {
+            if (sched == kGridInterleaved && next && kk + D < NCH) {
                 if (!acquire()) break;
-                first_read(k + D, nst);
+                first_read(kk + D, nst);
             }
         }
         if (!next || !ok) break;
+        if (sched != kGridInterleaved)
+            for (int k = D; k < NCH && acquire(); ++k) first_read(k, nst);
+        if (!ok) break;
         const uint32_t it = static_cast<uint32_t>(r + 1);
         post(nst, it);
         nst = GridStat<OP>{};

@@ -56,6 +56,7 @@ struct SmPlan {
     int resident = 0;      // three-pass split: resident clusters
     int scratch = 0;       // grid split: bytes of cleared scratch (cooperative launch)
     int read_ahead = 0;    // streamed split: next-row chunks read during each exchange
+    int schedule = 0;      // grid split: row schedule
     KernelFn fn = nullptr;
     const char* name = "";
 };
@@ -537,6 +538,14 @@ rmsnorm_status_t sm_plan_stream_grid(const SmCall& c, SmPlan* P) {
     // whole next slice); 32 MiB, eight chunks, 77.9 / 78.0 / 76.0 / 73.8 /
     // 68.9; 64 MiB, sixteen chunks, 59.8 / 60.4 / 61.4 / 61.7 / 62.7.
     P->read_ahead = P->nchunks <= 4 ? P->nchunks : P->nchunks <= 12 ? 2 : 4;
+    // Row schedule: a row's second read interleaved with the next row's first
+    // read, or phased (second read, then the next first read).  Measured
+    // (interleaved / phased / phased reversed): fp32 rows of 24 MiB 72 / 67 /
+    // 67, 32 MiB 76 / 62 / 63, 40 MiB 69 / 62 / 61, 64 MiB 62 / 65 / 62; bf16
+    // rows of 64 MiB 61 / 65 / 61.  Interleaving puts about two rows of
+    // traffic between a chunk's two reads, more than L2 keeps for the widest
+    // rows.
+    P->schedule = P->nchunks > 12 ? 1 : 0;
     P->nslots = static_cast<int>(slots);
     P->scratch = grid_scratch_bytes(static_cast<int>(grid));
     P->fn = fn;
@@ -696,6 +705,7 @@ rmsnorm_status_t sm_run(int32_t dtype, const void* x, void* y, int64_t rows, int
     p.nchunks = P.nchunks;
     p.nslots = P.nslots;
     p.read_ahead = P.read_ahead;
+    p.schedule = P.schedule;
     p.status = c.dv.status;
     p.fault = c.opt.fault_inject;
     p.timeout_ns = c.opt.wait_timeout_ns ? c.opt.wait_timeout_ns : kDefaultTimeoutNs;

@@ -449,6 +449,23 @@ def test_rows_over_the_whole_grid(dtype, rows, hidden, extra):
     compare(xc, ref, f"grid in place {extra} {dtype} {rows}x{hidden}")
 
 
+@pytest.mark.parametrize("dtype,rows,hidden", [
+    ("f32", 2, 7 << 20),      # rows of 28 MiB: phased (second read, then the next first read)
+    ("f32", 2, 10 << 20),     # rows of 40 MiB: phased, second read reversed
+    ("bf16", 2, 14 << 20),    # rows of 28 MiB
+    ("bf16", 3, 20 << 20),    # rows of 40 MiB, three rows
+])
+def test_whole_grid_row_schedules(dtype, rows, hidden):
+    """The whole-grid kernel's phased row schedules (chosen for rows wider than
+    24 MiB), against the oracle; in place too."""
+    x, w = rand_case(rows, hidden, dtype, seed=hidden % 997 + rows)
+    ref = oracle_for(x, w, 1e-6)
+    xc, wc = x.cuda(), w.cuda()
+    compare(run(xc, wc, 1e-6, path="grid"), ref, f"grid schedule {dtype} {rows}x{hidden}")
+    run(xc, wc, 1e-6, y=xc, path="grid")
+    compare(xc, ref, f"grid schedule in place {dtype} {rows}x{hidden}")
+
+
 def test_row_kernel_grid_has_about_three_row_blocks_per_cta():
     x = torch.empty(262144, 8192, dtype=torch.bfloat16, device="cuda")
     w = torch.empty(8192, dtype=torch.bfloat16, device="cuda")

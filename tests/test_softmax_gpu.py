@@ -230,6 +230,17 @@ def test_stream_special_values(dtype):
         compare(xd, ref, f"{path} C={cl} special in place {dtype}")
 
 
+@pytest.mark.parametrize("dtype,rows,cols", [
+    ("f32", 3, 1 << 23),      # rows of 32 MiB: the second read interleaved with the next first read
+    ("f32", 2, 1 << 24),      # rows of 64 MiB: phased
+    ("bf16", 2, 1 << 25),     # rows of 64 MiB
+])
+def test_whole_grid_row_schedules(dtype, rows, cols):
+    """Both row schedules of the whole-grid kernel against the oracle."""
+    x = case(rows, cols, dtype, rows + cols % 991)
+    compare(run(x.cuda(), path="grid"), ref_for(x), f"grid schedule {dtype} {rows}x{cols}")
+
+
 MAX_COLS = (1 << 31) - 1      # the widest row the ABI accepts
 
 
