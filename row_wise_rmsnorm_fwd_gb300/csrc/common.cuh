@@ -74,6 +74,7 @@ struct Params {
     void* scratch;         // grid-split kernels: cleared exchange records (else null)
     int32_t read_ahead;    // streamed split rows: next-row chunks read during an exchange
     int32_t schedule;      // grid-split kernels: row schedule (k_grid.cuh)
+    int32_t resident;      // grid-split kernels: slice chunks kept in shared memory
 };
 
 // ------------------------------------------------------------ element types --

@@ -6,8 +6,10 @@
 namespace rmsnorm {
 
 static_assert(16 * kStagedMaxSlots + 2 * 32 * sizeof(float2) + 4 * 8 + 2 * sizeof(float2) <=
-                  kStreamHeader,
+                      kGridResBarOffset &&
+                  kGridResBarOffset + 2 * 8 * kGridMaxResident <= kStreamHeader,
               "grid kernel header overflows");
+static_assert(kGridMaxResident == kGridMaxResidentHost, "host and device resident limits differ");
 static_assert(kGridMaxCtas == kGridMaxCtasHost && kGridScratchBytes == kGridScratchBytesHost &&
                   kGridCounterBytes == kGridCounterBytesHost,
               "host and device grid scratch sizes differ");

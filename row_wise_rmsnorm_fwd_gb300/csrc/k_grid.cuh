@@ -27,7 +27,12 @@
 // this row's writes) between a chunk's two reads, more than L2 keeps for the
 // widest rows; for those the planner takes a phased schedule (p.schedule):
 // row r's whole second read, then row r + 1's first read (after the chunks
-// read ahead), with the second read in chunk order or reversed.
+// read ahead), with the second read in chunk order or reversed.  Phased, a
+// CTA may also keep chunks D .. D + R - 1 of its slice (p.resident, after the
+// D chunks read ahead) in shared memory beside the ring from the first read
+// to the second, so that L2 holds less of the row; the second read takes
+// them first, which frees their slots before the next row's first read
+// refills them.
 //
 //   RMSNorm:  first read: sum of squares; the grid adds the CTA sums;
 //             second read: (x * rstd) * w (w's chunk follows x's in the ring,
@@ -56,6 +61,11 @@ enum : int { kGridOpRmsNorm = 0, kGridOpSoftmax = 1 };
 // then row r + 1's first read -- with the second read in chunk order or
 // reversed.
 enum : int { kGridInterleaved = 0, kGridPhased = 1, kGridPhasedReversed = 2 };
+// Resident slots (phased schedule): at most kGridMaxResident chunks of a
+// slice kept in shared memory between a row's two reads; their barriers sit
+// in the header from kGridResBarOffset.
+constexpr int kGridMaxResident = 16;
+constexpr int kGridResBarOffset = 1088;
 
 
 // Per-thread statistic of a first read: RMSNorm a running sum of squares,
@@ -91,7 +101,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
     constexpr int EPV = VecTraits<T, 16>::kElems;
     constexpr bool kSm = OP == kGridOpSoftmax;
     extern __shared__ __align__(128) unsigned char smem[];
-    // header: full[32] | empty[32] | red[2][32] pairs | xbar[4] | xres[2] pairs
+    // header: full[32] | empty[32] | red[2][32] pairs | xbar[4] | xres[2] pairs |
+    // (at kGridResBarOffset) rfull[16] | rempty[16]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kStagedMaxSlots;
     float2* red = reinterpret_cast<float2*>(smem + 16 * kStagedMaxSlots);
@@ -99,6 +110,10 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
     // red[b]; xbar[2 + b]: the exchange's result is in xres[b]
     uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + 16 * kStagedMaxSlots + 512);
     float2* xres = reinterpret_cast<float2*>(smem + 16 * kStagedMaxSlots + 512 + 32);
+    // resident slot i holds chunk D + i of the current row from its first
+    // read to its second (rfull: landed; rempty: read by every consumer warp)
+    uint64_t* rfull = reinterpret_cast<uint64_t*>(smem + kGridResBarOffset);
+    uint64_t* rempty = rfull + kGridMaxResident;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -112,7 +127,25 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
     const int64_t send = sbeg + slice_nom < row_bytes ? sbeg + slice_nom : row_bytes;
     const int64_t my_bytes = send > sbeg ? send - sbeg : 0;
     const SlotRing ring{full, empty, smem + kStreamHeader, S, NCH, CB, my_bytes};
+    unsigned char* const rslots = smem + kStreamHeader + static_cast<int64_t>(S) * CB;
     const int64_t rows = p.rows;
+
+    // first reads of a row before the rest (all of row 0's; the read-ahead of
+    // the later rows, p.read_ahead chunks: the planner's choice)
+    const int D = NCH < p.read_ahead ? NCH : p.read_ahead;
+    const int sched = p.schedule;
+    // chunks D .. D + R - 1 of every row stay in shared memory between the
+    // two reads (phased schedule only; the planner keeps D + R <= NCH)
+    const int R = sched == kGridPhased ? p.resident : 0;
+    auto is_res = [&](int k) { return k >= D && k < D + R; };
+    // the chunk of second-read step kk: resident chunks first, then the others
+    // in order (reversed for kGridPhasedReversed)
+    auto b_chunk = [&](int kk) {
+        if (sched == kGridPhasedReversed) return NCH - 1 - kk;
+        if (kk < R) return D + kk;
+        const int j = kk - R;
+        return j < D ? j : j + R;
+    };
 
     if (tid == 0) {
         ring_init(ring, NCW);
@@ -120,14 +153,13 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
         mbar_init(smem_addr(&xbar[1]), NCW);
         mbar_init(smem_addr(&xbar[2]), 1);
         mbar_init(smem_addr(&xbar[3]), 1);
+        for (int i = 0; i < R; ++i) {
+            mbar_init(smem_addr(&rfull[i]), 1);
+            mbar_init(smem_addr(&rempty[i]), NCW);
+        }
         fence_mbarrier_init_cluster();
     }
     __syncthreads();
-
-    // first reads of a row before the interleaved part (all of row 0's; the
-    // read-ahead of the later rows, p.read_ahead chunks: the planner's choice)
-    const int D = NCH < p.read_ahead ? NCH : p.read_ahead;
-    const int sched = p.schedule;
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer --
@@ -137,19 +169,48 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
             const char* xb = static_cast<const char*>(p.x) + sbeg;
             const char* wsrc = static_cast<const char*>(p.w) + sbeg;
             RingCursorSeq c;
+            int64_t res_last[kGridMaxResident];   // last row each resident slot was loaded for
+            for (int i = 0; i < kGridMaxResident; ++i) res_last[i] = -1;
             auto first = [&](int64_t r, int k) {
-                ring_push(p, ring, c, xb + r * row_bytes + static_cast<int64_t>(k) * CB,
-                          ring.chunk_len(k), keep, kSiteStagedEmpty);
+                const char* src = xb + r * row_bytes + static_cast<int64_t>(k) * CB;
+                const int len = ring.chunk_len(k);
+                if (!is_res(k)) {
+                    ring_push(p, ring, c, src, len, keep, kSiteStagedEmpty);
+                    return;
+                }
+                // resident slot i takes one chunk per row: row r's phase of
+                // rfull[i] has parity r & 1, and it waits for row r - 1's
+                // release of the slot
+                const int i = k - D;
+                if (c.abort) return;
+                if (r > 0 && !mbar_wait_bounded<false>(smem_addr(&rempty[i]),
+                                                       static_cast<uint32_t>(r - 1) & 1u,
+                                                       p.timeout_ns)) {
+                    report_timeout(p.status, kSiteStagedEmpty);
+                    c.abort = true;
+                    return;
+                }
+                const uint32_t fb = smem_addr(&rfull[i]);
+                if (len > 0) {
+                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(len));
+                    bulk_g2s(smem_addr(rslots + static_cast<int64_t>(i) * CB), src,
+                             static_cast<uint32_t>(len), fb, keep);
+                } else {
+                    mbar_arrive(fb);
+                }
+                res_last[i] = r;
             };
             for (int k = 0; k < NCH; ++k) first(0, k);
             if (rows > 1)
                 for (int k = 0; k < D; ++k) first(1, k);
             for (int64_t r = 0; r < rows && !c.abort; ++r) {
                 for (int kk = 0; kk < NCH; ++kk) {
-                    const int k = sched == kGridPhasedReversed ? NCH - 1 - kk : kk;
+                    const int k = b_chunk(kk);
                     const int64_t off = static_cast<int64_t>(k) * CB;
                     const int len = ring.chunk_len(k);
-                    ring_push(p, ring, c, xb + r * row_bytes + off, len, done, kSiteStagedEmpty);
+                    if (!is_res(k))
+                        ring_push(p, ring, c, xb + r * row_bytes + off, len, done,
+                                  kSiteStagedEmpty);
                     if (!kSm) ring_push(p, ring, c, wsrc + off, len, wpol, kSiteStagedEmpty);
                     if (sched == kGridInterleaved && r + 1 < rows && kk + D < NCH) first(r + 1, kk + D);
                 }
@@ -159,6 +220,11 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
                     for (int k = 0; k < D; ++k) first(r + 2, k);
             }
             ring_drain(p, ring, c);
+            // no resident copy may still be in flight when the CTA leaves
+            for (int i = 0; i < R; ++i)
+                if (res_last[i] >= 0)
+                    mbar_wait_bounded<false>(smem_addr(&rfull[i]),
+                                             static_cast<uint32_t>(res_last[i]) & 1u, p.timeout_ns);
         }
         __syncwarp();
         return;
@@ -213,14 +279,13 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
     auto slot_base = [&]() {
         return ring.slots + static_cast<int64_t>(slot) * CB + static_cast<int64_t>(ct) * 16;
     };
+    auto res_base = [&](int i) {
+        return rslots + static_cast<int64_t>(i) * CB + static_cast<int64_t>(ct) * 16;
+    };
     const int64_t vstride = static_cast<int64_t>(NC) * 16;
 
-    // First read of chunk k (acquired) into the running statistic.
-    auto first_read = [&](int k, GridStat<OP>& st) {
-        const int nv = ring.chunk_len(k) >> 4;
-        Vec<16> raw[V];
-        stream_load<V, false>(raw, slot_base(), vstride, ct, NC, nv);
-        release();
+    // Fold this thread's vectors of one chunk into the running statistic.
+    auto fold_chunk = [&](const Vec<16> (&raw)[V], int nv, GridStat<OP>& st) {
         if constexpr (kSm) {
             const float2 ms = stream_fold<T, V, false>(raw, ct, NC, nv, make_float2(st.bm, st.b0));
             st.bm = ms.x;
@@ -238,6 +303,27 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
             }
         }
         st.end_chunk();
+    };
+    // First read of chunk k of row r into the running statistic: a ring
+    // chunk (acquired, released), or a resident one (waited for, kept).
+    // False (uniform over the warp) once a wait ran out.
+    auto first_read = [&](int64_t r, int k, GridStat<OP>& st) {
+        const int nv = ring.chunk_len(k) >> 4;
+        Vec<16> raw[V];
+        if (is_res(k)) {
+            ok = __all_sync(0xffffffffu,
+                            ok && mbar_wait_bounded<false>(smem_addr(&rfull[k - D]),
+                                                           static_cast<uint32_t>(r) & 1u,
+                                                           p.timeout_ns));
+            if (!ok) return false;
+            stream_load<V, false>(raw, res_base(k - D), vstride, ct, NC, nv);
+        } else {
+            if (!acquire()) return false;
+            stream_load<V, false>(raw, slot_base(), vstride, ct, NC, nv);
+            release();
+        }
+        fold_chunk(raw, nv, st);
+        return true;
     };
     // Hand this warp's part of exchange `it` to the exchange warp: warp
     // butterfly, one slot per warp, an arrival on xbar[it & 1].
@@ -273,19 +359,18 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
         Ssum = v.y;
         return true;
     };
-    // First reads of chunks [k0, k1) of the row after this one.
-    auto read_ahead = [&](GridStat<OP>& st, int k0, int k1) {
-        for (int k = k0; k < k1 && acquire(); ++k) first_read(k, st);
-    };
 
     // row 0's first read and result
     GridStat<OP> st;
 #pragma unroll 1
-    for (int k = 0; k < NCH && acquire(); ++k) first_read(k, st);
+    for (int k = 0; k < NCH && first_read(0, k, st); ++k) {
+    }
     if (!ok) return;
     post(st, 0);
     GridStat<OP> nst;
-    if (rows > 1) read_ahead(nst, 0, D);
+    if (rows > 1)
+        for (int k = 0; k < D && first_read(1, k, nst); ++k) {
+        }
     float M, Ssum;
     if (!result(0, M, Ssum)) return;
 
@@ -303,13 +388,19 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
         char* dst = ybase + r * row_bytes;
 #pragma unroll 1
         for (int kk = 0; kk < NCH; ++kk) {
-            const int k = sched == kGridPhasedReversed ? NCH - 1 - kk : kk;
+            const int k = b_chunk(kk);
             const int nv = ring.chunk_len(k) >> 4;
             // second read of row r, chunk k: the outputs
-            if (!acquire()) break;
             Vec<16> xr[V];
-            stream_load<V, false>(xr, slot_base(), vstride, ct, NC, nv);
-            release();
+            if (is_res(k)) {
+                stream_load<V, false>(xr, res_base(k - D), vstride, ct, NC, nv);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&rempty[k - D]));
+            } else {
+                if (!acquire()) break;
+                stream_load<V, false>(xr, slot_base(), vstride, ct, NC, nv);
+                release();
+            }
             Vec<16> wr[V];
             if constexpr (!kSm) {
                 if (!acquire()) break;
@@ -336,19 +427,20 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) grid_kernel(const Params
                 }
             }
             // first read of row r + 1, chunk k + D
-            if (sched == kGridInterleaved && next && kk + D < NCH) {
-                if (!acquire()) break;
-                first_read(kk + D, nst);
-            }
+            if (sched == kGridInterleaved && next && kk + D < NCH && !first_read(r + 1, kk + D, nst))
+                break;
         }
         if (!next || !ok) break;
         if (sched != kGridInterleaved)
-            for (int k = D; k < NCH && acquire(); ++k) first_read(k, nst);
+            for (int k = D; k < NCH && first_read(r + 1, k, nst); ++k) {
+            }
         if (!ok) break;
         const uint32_t it = static_cast<uint32_t>(r + 1);
         post(nst, it);
         nst = GridStat<OP>{};
-        if (r + 2 < rows) read_ahead(nst, 0, D);
+        if (r + 2 < rows)
+            for (int k = 0; k < D && first_read(r + 2, k, nst); ++k) {
+            }
         if (!result(it, M, Ssum)) break;
     }
 }

@@ -66,6 +66,20 @@ KernelFn softmax_grid_ptr(int dtype, int v);
 constexpr int kGridMaxCtasHost = 1024;
 constexpr int kGridCounterBytesHost = 128;
 constexpr int kGridScratchBytesHost = kGridCounterBytesHost + 2 * kGridMaxCtasHost * 8;
+constexpr int kGridMaxResidentHost = 16;   // grid kernels: resident chunks per slice, at most
+constexpr int kGridMinRingSlots = 4;       // grid kernels: ring slots kept beside resident ones
+
+// Chunks of each slice the whole-grid kernel keeps in shared memory between a
+// row's two reads (phased schedule only): what the ring's `slots` can spare
+// beyond kGridMinRingSlots, within the slice less its read-ahead.
+inline int grid_resident_chunks(int schedule, int slots, int64_t nchunks, int read_ahead,
+                                bool stages_forced) {
+    if (schedule != 1 || stages_forced) return 0;
+    int64_t r = slots - kGridMinRingSlots;
+    if (r > nchunks - read_ahead) r = nchunks - read_ahead;
+    if (r > kGridMaxResidentHost) r = kGridMaxResidentHost;
+    return r > 0 ? static_cast<int>(r) : 0;
+}
 inline int grid_scratch_bytes(int grid) { return kGridCounterBytesHost + 2 * grid * 8; }
 
 // Comparison kernel with the compiler write-up's schedule (one CTA per row).
