@@ -25,7 +25,7 @@
  *  - The call is asynchronous on `stream` (NULL = the legacy default stream)
  *    and allocates no memory, with one exception: the few-very-wide-rows
  *    kernel (RMSNORM_PATH_GRID: forced through rmsnorm_fwd_ex, and chosen
- *    automatically for fewer rows than SMs of 10 to 32 MiB by RMSNorm and of
+ *    automatically for fewer rows than SMs of 10 to 40 MiB by RMSNorm and of
  *    16 MiB and more, totalling 96 MiB or more, by the row softmax) takes a
  *    scratch area of at most 17 KB from the current device's default memory
  *    pool in stream order and returns it on the same stream.  Argument errors are detected on the host before any

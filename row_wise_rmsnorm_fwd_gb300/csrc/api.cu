@@ -43,7 +43,7 @@ constexpr int kRingregSlots = 3;                 // ring-to-register kernel: rin
 constexpr int64_t kGridMinRowBytes = 10ll << 20;     // auto: rows over the whole grid from here
 constexpr int kGridReadAheadRmsNorm = 2;             // see plan_grid
 constexpr int64_t kGridInterleavedMaxRowBytes = 24ll << 20;   // see plan_grid
-constexpr int64_t kGridMaxRowBytes = 32ll << 20;     //   to here
+constexpr int64_t kGridMaxRowBytes = 40ll << 20;     //   to here
 constexpr int64_t kRingregLowMaxRowBytes = 57344;    // auto: ringreg for rows above 32 KB to here
 constexpr int64_t kRingregHighMinRowBytes = 114688;  // auto: and above this (to 128 KB)
 constexpr int64_t kUnsplitMaxVecs = 0x7FFFFFFFll - 1024;  // two-pass, one CTA per row: up to here
@@ -450,7 +450,10 @@ rmsnorm_status_t plan_grid(const Call& c, Plan* P) {
     const int max_nc = softmax_stream_max_threads() - 64;
     const int nc = c.opt.threads > 0 ? c.opt.threads : max_nc;
     if (nc % 32 != 0 || nc > max_nc) return RMSNORM_ERR_UNSUPPORTED;
-    int v = 4;
+    // Two vectors a consumer thread per chunk (14 KB chunks, twice the ring
+    // slots) for the phased rows above kGridInterleavedMaxRowBytes: fp32 rows
+    // of 32 MiB measured 63.8 against 61.3% of the HBM copy peak with four.
+    int v = row_bytes > kGridInterleavedMaxRowBytes ? 2 : 4;
     if (c.opt.chunk_bytes != 0) {
         if (c.opt.chunk_bytes == 2 * 16 * nc) v = 2;
         else if (c.opt.chunk_bytes == 4 * 16 * nc) v = 4;
@@ -501,13 +504,16 @@ rmsnorm_status_t plan_grid(const Call& c, Plan* P) {
     // rows of 10 and 32 MiB within a point of each other at every depth.
     P->read_ahead = kGridReadAheadRmsNorm;
     // Row schedule.  Measured (% of the HBM copy peak; interleaved / phased
-    // / phased with the second read reversed): fp32 rows of 16 MiB 74 / 65
-    // / 65, 24 MiB 65 / 62 / 63, 32 MiB 55 / 61 / 61, 40 MiB 50 / 56 / 57,
-    // 64 MiB 51 / 54 / 56; bf16 rows of 32 MiB 54 / 62 / 60, 64 MiB 50 /
-    // 52 / 55.  Interleaving keeps DRAM reading and writing at once, but
-    // lengthens the distance between a chunk's two reads to about two rows
-    // of traffic (the next row's reads and this row's writes), which L2
-    // holds only for rows of up to about 24 MiB.
+    // / phased with the second read reversed, four vectors a thread per
+    // chunk): fp32 rows of 16 MiB 74 / 65 / 65, 24 MiB 65 / 62 / 63, 32 MiB
+    // 55 / 61 / 61, 40 MiB 50 / 56 / 57, 64 MiB 51 / 54 / 56; bf16 rows of
+    // 32 MiB 54 / 62 / 60, 64 MiB 50 / 52 / 55.  With two vectors (the
+    // phased rows' chunks) phased in order measured 64 at 32 MiB and 63 at
+    // 40 MiB against 58 reversed, reversed 56 against 53 at 64 MiB.
+    // Interleaving keeps DRAM reading and writing at once, but puts about
+    // two rows of traffic (the next row's reads and this row's writes)
+    // between a chunk's two reads, which L2 holds only for rows of up to
+    // about 24 MiB.
     P->schedule = row_bytes <= kGridInterleavedMaxRowBytes ? 0
                   : row_bytes <= kGridMaxRowBytes          ? 1
                                                            : 2;
@@ -516,6 +522,7 @@ rmsnorm_status_t plan_grid(const Call& c, Plan* P) {
     // wants its slots (fp32 rows of 32 MiB, R = 0 / 2 / 4: 60.6 / 61.8 /
     // 59.4% of the HBM copy peak).
     P->nslots = static_cast<int>(slots);
+
     P->fn = fn;
     P->name = "grid_stream";
     return RMSNORM_OK;
@@ -598,15 +605,16 @@ rmsnorm_status_t plan_auto(const Call& c, Plan* P) {
     const bool split = c.rows < c.info->sms &&
                        (row_bytes > kRowregMaxRowBytes || c.rows * row_bytes >= kSplitMinBytes);
     if (split) {
-        // Rows of 10 to 32 MiB: each over the whole grid in turn, its second
+        // Rows of 10 to 40 MiB: each over the whole grid in turn, its second
         // read (and w) from L2.  Measured (% of the HBM copy peak, whole grid
         // against the cluster two-pass split, which reads x twice): fp32 rows
-        // of 10 MiB 63 / 60, 12 MiB 70 / 60, 16 MiB 55-75 / 43-64 (4 to 150
-        // rows), 24 MiB 69 / 56, 32 MiB 56 / 55; bf16 rows of 12 MiB 68 / 60,
-        // 16 MiB 63-70 / 52-53, 32 MiB 55 / 54.  Outside that range the
-        // cluster split wins: rows of 8 MiB 58 / 60 (bf16 55 / 59), whose
-        // exchanges come too often, and of 40 and 64 MiB 51 / 61 and 51 / 57,
-        // which L2 does not keep beside w between the two reads.
+        // of 10 MiB 63 / 60, 12 MiB 70 / 60, 16 MiB 55-76 / 43-64 (4 to 150
+        // rows), 24 MiB 67 / 56, 32 MiB 64 / 55, 36 MiB 64 / 61, 40 MiB 63 /
+        // 60; bf16 rows of 12 / 16 / 32 / 40 MiB 68 / 63-70 / 61 / 61 against
+        // 60 / 52-53 / 54 / 59.  Outside that range the cluster split wins:
+        // rows of 8 MiB 58 / 60 (bf16 55 / 59), whose exchanges come too
+        // often, and of 44 and 64 MiB 57 / 58 and 55 / 57, which L2 does not
+        // keep beside w between the two reads.
         if (row_bytes >= kGridMinRowBytes && row_bytes <= kGridMaxRowBytes) {
             st = plan_grid(c, P);
             if (st == RMSNORM_OK || st == RMSNORM_ERR_CUDA) return st;

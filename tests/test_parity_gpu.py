@@ -388,7 +388,8 @@ def test_plan_reports_families():
     ((8, 262144), "bf16", "cluster_rowreg", 512, 8), # c5b: few wide rows
     ((2, 1 << 20), "f32", "twopass_cluster", 1024, 0),   # few rows of 4 MB
     ((8, 1 << 24), "f32", "twopass_cluster", 1024, 0),   # w16m: rows of 64 MiB over clusters
-    ((12, 10 << 20), "f32", "twopass_cluster", 1024, 0), # rows of 40 MiB over clusters
+    ((12, 10 << 20), "f32", "grid_stream", 448, 2),      # rows of 40 MiB: phased, 14 KB chunks
+    ((11, 11 << 20), "f32", "twopass_cluster", 1024, 0), # rows of 44 MiB over clusters
     ((32, 1 << 22), "f32", "grid_stream", 448, 4),       # rows of 16 MiB over the whole grid
     ((16, 1 << 23), "bf16", "grid_stream", 448, 4),      # the same in bf16
     ((40, 5 << 19), "f32", "grid_stream", 448, 4),       # rows of 10 MiB
