@@ -623,7 +623,7 @@ rmsnorm_status_t sm_make_plan(const SmCall& c, SmPlan* P) {
     // row over the whole grid in turn, so that its second read finds it in
     // L2.  Measured (% of the HBM copy peak, against the three-pass kernel
     // split over clusters, which reads x three times): eight fp32 rows of
-    // 64 MiB 62 against 40 (clusters of 12), sixteen rows of 32 MiB 74
+    // 64 MiB 72 against 40 (clusters of 12), sixteen rows of 32 MiB 74-79
     // against 31 (8), thirty-two rows of 16 MiB 69 against 45 (4).  Rows of
     // 8 MiB exchange too often: 50 against 67 for the streamed kernel split
     // over clusters of 8 (fp32 and bf16 alike).
