@@ -67,7 +67,7 @@ rmsnorm_status_t rowsoftmax_fwd_bf16(const uint16_t* x, uint16_t* y, int64_t row
  * bulk copies: first read online maximum and sum, second read the outputs,
  * normally from L2; 16-byte aligned rows, else RMSNORM_ERR_UNSUPPORTED;
  * opt->cluster = 2..16 (any size) splits each row over a thread-block
- * cluster; opt->threads = consumer threads (multiple of 32, <= 480),
+ * cluster; opt->threads = consumer threads (multiple of 32, <= 480, default 448),
  * opt->chunk_bytes = 2 or 4 vectors of 16 bytes per consumer thread,
  * opt->stages = ring slots), RMSNORM_PATH_GRID (every row over the whole
  * grid, see rmsnorm.h; opt->threads = consumer threads, a multiple of 32 up

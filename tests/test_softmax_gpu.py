@@ -190,7 +190,7 @@ def test_stream_cluster_split(dtype, rows, cols, cluster, stages, grid):
     (160, 100000, 0, 0, 0, 0),        # more rows than SMs, ragged last chunk
     (19, 262144, 0, 2, 5, 0),         # a two-slot ring, five CTAs, many rows each
     (25, 77780, 0, 3, 0, 64),         # 64 consumer threads, three slots (bf16: refused)
-    (12, 50000, 16 * 2 * 480, 0, 0, 0),      # two vectors per thread and chunk
+    (12, 50000, 16 * 2 * 480, 0, 0, 480),    # two vectors per thread and chunk, 15 warps
 ])
 def test_stream_ring_shapes(dtype, rows, cols, chunk, stages, grid, threads):
     """The two-read streamed kernel over ragged widths, ring depths, grid
@@ -484,7 +484,7 @@ def test_plans_report_each_kernels_own_launch():
     p = binding.rowsoftmax_plan(x, torch.empty_like(x))
     assert p["kernel"] == "softmax_stream", p
     assert p["cluster"] == 1 and p["smem_bytes"] > 0 and p["stages"] >= 2, p
-    assert p["block_threads"] == 512 and p["grid"] == torch.cuda.get_device_properties(0).multi_processor_count, p
+    assert p["block_threads"] == 480 and p["grid"] == torch.cuda.get_device_properties(0).multi_processor_count, p
     t = binding.rowsoftmax_plan(x, torch.empty_like(x), options={"path": "twopass"})
     assert t["kernel"] == "softmax_threepass", t
     assert t["cluster"] == 1 and t["smem_bytes"] == 0 and t["stages"] == 0, t
