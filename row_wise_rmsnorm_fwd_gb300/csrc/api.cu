@@ -522,7 +522,6 @@ rmsnorm_status_t plan_grid(const Call& c, Plan* P) {
     // wants its slots (fp32 rows of 32 MiB, R = 0 / 2 / 4: 60.6 / 61.8 /
     // 59.4% of the HBM copy peak).
     P->nslots = static_cast<int>(slots);
-
     P->fn = fn;
     P->name = "grid_stream";
     return RMSNORM_OK;
